@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: append + decode attention over a static KV cache.
+
+One step is the whole hot path for every layer of the workload: for each
+layer, kvc_append of the new token's K/V rows at cache_index = valid - 1, then
+kvc_decode_attn of one query row per head over the valid rows.  Every timed
+step recomputes the same decode step (same positions), so all steps move the
+same bytes.  Default workload: the Llama-3-8B-shaped GQA cache (32 layers,
+B=16, H=32, H_kv=8, d_h=128, max_context 8192, bf16, ragged live lengths
+uniform in [1024, 8192]).
+
+Output: one JSON line on rank 0.  ``value`` is the algorithmic HBM traffic
+of the step (K+V of the live rows + q + out for attention; k_new/v_new read
+and written once for the append) per second of step time, summed over ranks.
+
+``--impl reference`` times the fp64 CPU oracle instead (host cores only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from static_kv_cache_gb300 import synth  # noqa: E402
+
+METRIC = "decode-attention HBM GB/s and % of GB300 peak; decode tokens/s per layer"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_internal.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_decode_inst.cu")
+
+
+# --------------------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=600)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("kvc", "reference"), default="kvc")
+    p.add_argument("--workload", default="llama3_8b", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="wall time budget of the CPU-oracle baseline sample")
+    p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a scalar over all ranks (the slowest rank sets the job time)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step_per_rank: float, world: int, max_seconds: float, steps: int) -> float:
+    """Whole-job GB/s: every rank moves the same bytes each step (weak
+    scaling); the job takes as long as its slowest rank."""
+    return bytes_per_step_per_rank * world * steps / max_seconds / 1e9
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from a committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = d.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            sel = str(device_index)
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200", "-i", sel]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- workload
+def step_bytes(w: synth.Workload, lengths) -> dict:
+    """Algorithmic bytes of one layer's decode step (per launch)."""
+    eb = synth.ELEM_BYTES[w.dtype]
+    live = int(np.asarray(lengths, dtype=np.int64).sum())
+    attn = 2 * w.n_kv_heads * w.d_head * eb * live + 2 * w.batch * w.n_heads * w.d_head * eb
+    append = 4 * w.batch * w.n_kv_heads * w.d_head * eb          # read k/v_new, write the rows
+    return {"attn": attn, "append": append}
+
+
+class DeviceState:
+    """Caches, workspace, handle and the per-layer step inputs on one GPU."""
+
+    def __init__(self, w: synth.Workload, device: int):
+        from static_kv_cache_gb300 import kvc
+        self.kvc = kvc
+        self.w = w
+        self.lengths = synth.live_lengths(w)
+        self.maxlen = int(self.lengths.max())
+        tdt = synth.DTYPES[w.dtype]
+        dev = torch.device("cuda", device)
+        shape = (w.n_layers, w.batch, w.n_kv_heads, w.max_context, w.d_head)
+        self.K = torch.empty(shape, dtype=tdt, device=dev)
+        self.V = torch.empty(shape, dtype=tdt, device=dev)
+        synth.poison_(self.K, w.dtype)
+        synth.poison_(self.V, w.dtype)
+        pre = (self.lengths - 1).tolist()
+        for layer in range(w.n_layers):
+            for b in range(w.batch):
+                n = pre[b]
+                if n:
+                    shp = (w.n_kv_heads, n, w.d_head)
+                    self.K[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pk", layer, b), dev)
+                    self.V[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pv", layer, b), dev)
+        L, B = w.n_layers, w.batch
+        self.q = synth.normal((L, B, w.n_heads, w.d_head), w.dtype, synth.sub_seed(w.seed, "q"), dev)
+        self.k_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "kn"), dev)
+        self.v_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "vn"), dev)
+        self.out = torch.empty((L, B, w.n_heads, w.d_head), dtype=tdt, device=dev)
+        self.cache_index = (self.lengths - 1).to(dev)
+        self.valid_len = self.lengths.to(dev)
+        self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
+        self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
+        st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
+        kvc.check(st, "kvc_alloc")
+        torch.cuda.synchronize(dev)
+
+    def step(self, stream, events=None, q=None, k_new=None, v_new=None, ci=None, vl=None, out=None) -> int:
+        """One decode step over all layers; returns the number of kernel launches."""
+        kvc, w = self.kvc, self.w
+        q = self.q if q is None else q
+        k_new = self.k_new if k_new is None else k_new
+        v_new = self.v_new if v_new is None else v_new
+        ci = self.cache_index if ci is None else ci
+        vl = self.valid_len if vl is None else vl
+        out = self.out if out is None else out
+        sp = stream.cuda_stream
+        for layer in range(w.n_layers):
+            st = kvc.kvc_append(self.h, layer, k_new[layer], v_new[layer], ci, 1, sp)
+            if st:
+                raise kvc.KvcError(st, "kvc_append")
+            if events is not None:
+                events[layer][0].record(stream)
+            st = kvc.kvc_decode_attn(self.h, layer, q[layer], vl, self.maxlen, out[layer], sp)
+            if st:
+                raise kvc.KvcError(st, "kvc_decode_attn")
+            if events is not None:
+                events[layer][1].record(stream)
+        return 2 * w.n_layers
+
+    def close(self):
+        self.kvc.kvc_free(self.h)
+
+
+# --------------------------------------------------------------------------- CPU oracle sample
+def cpu_oracle_sample(w: synth.Workload, seconds: float, host=None):
+    """Time the fp64 oracle on a bounded sample of the workload: each sample
+    step is the decode attention of one sequence (cycling over the batch) of
+    layer 0, all its query heads.  Returns (GB/s, samples, seconds, threads)."""
+    import oracle
+    lengths = synth.live_lengths(w).numpy()
+    if host is None:
+        host = cpu_host_inputs(w, lengths)
+    Kh, Vh, qh = host
+    eb = synth.ELEM_BYTES[w.dtype]
+    done_bytes, spent, n = 0, 0.0, 0
+    while spent < seconds or n == 0:
+        b = n % w.batch
+        t0 = time.perf_counter()
+        oracle.decode_attn(qh[b:b + 1], Kh[b:b + 1], Vh[b:b + 1], lengths[b:b + 1], w.dtype)
+        spent += time.perf_counter() - t0
+        done_bytes += 2 * w.n_kv_heads * w.d_head * eb * int(lengths[b]) + 2 * w.n_heads * w.d_head * eb
+        n += 1
+    return done_bytes / spent / 1e9, n, spent, oracle.num_threads()
+
+
+def cpu_host_inputs(w: synth.Workload, lengths):
+    """Layer-0 inputs drawn on the host (same distribution and shapes)."""
+    maxlen = int(np.max(lengths))
+    shape = (w.batch, w.n_kv_heads, maxlen, w.d_head)
+    Kh = synth.to_bits(synth.normal(shape, w.dtype, synth.sub_seed(w.seed, "cpu_k"))).copy()
+    Vh = synth.to_bits(synth.normal(shape, w.dtype, synth.sub_seed(w.seed, "cpu_v"))).copy()
+    qh = synth.to_bits(synth.normal((w.batch, w.n_heads, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu_q")))
+    return Kh, Vh, qh
+
+
+def workload_config(w: synth.Workload, lengths, world: int) -> dict:
+    return {"workload": f"{w.name}: {w.n_layers} layers, B={w.batch}, H={w.n_heads}, "
+                        f"H_kv={w.n_kv_heads}, d_h={w.d_head}, max_context={w.max_context}, "
+                        f"{w.dtype} cache",
+            "n_layers": w.n_layers, "batch": w.batch, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
+            "d_head": w.d_head, "max_context": w.max_context, "cache_dtype": w.dtype,
+            "live_rows_per_kv_head": int(np.asarray(lengths).sum()),
+            "valid_len": "ragged U{%d..%d}" % w.ragged if w.ragged else "uniform %d" % int(lengths[0]),
+            "l2": "inputs larger than L2: each layer's live K/V exceeds the 129 MB L2 and the layers are cycled",
+            "parallelism": f"replicas x{world} (independent batches, no collective on the data path)"}
+
+
+# --------------------------------------------------------------------------- arms
+def bench_kvc(args, rank, world, local):
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    state = DeviceState(w, local)
+    lengths = state.lengths.numpy()
+    per_layer = step_bytes(w, lengths)
+    bytes_step = (per_layer["attn"] + per_layer["append"]) * w.n_layers
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            state.step(stream)
+    torch.cuda.synchronize()
+
+    # --- device-timed region
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(w.n_layers)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = None if args.no_clocks else ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    launches = 0
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s in range(args.steps):
+            launches += state.step(stream, evs[s])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed_max = reduce_max(elapsed, world, device=torch.device("cuda", local))
+    decode_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(w.n_layers)]
+    err = state.kvc.kvc_get_error(state.h, stream.cuda_stream)
+    if err:
+        raise state.kvc.KvcError(err, "device error word after the timed region")
+
+    # --- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        hq, hk, hv = pin(state.q), pin(state.k_new), pin(state.v_new)
+        hci, hvl = pin(state.cache_index), pin(state.valid_len)
+        hout = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(state.q), torch.empty_like(state.k_new), torch.empty_like(state.v_new)
+        dci, dvl = torch.empty_like(state.cache_index), torch.empty_like(state.valid_len)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hci, hvl))
+        d2h = hout.numel() * hout.element_size()
+        e2e_steps = max(3, min(args.steps, 200))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(e2e_steps):
+                for d, hsrc in ((dq, hq), (dk, hk), (dv, hv), (dci, hci), (dvl, hvl)):
+                    d.copy_(hsrc, non_blocking=True)
+                state.step(stream, q=dq, k_new=dk, v_new=dv, ci=dci, vl=dvl)
+                hout.copy_(state.out, non_blocking=True)
+                stream.synchronize()
+        e2e_s = reduce_max(time.perf_counter() - t0, world, device=torch.device("cuda", local))
+        e2e = {"value": round(job_throughput(bytes_step, world, e2e_s, e2e_steps), 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)}
+
+    # --- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbs, n, spent, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle decode attention of layer 0, one sequence (all {w.n_heads} heads) "
+                         f"per sample, cycling over the batch: {n} samples in {spent:.1f} s"}
+
+    value = job_throughput(bytes_step, world, elapsed_max, args.steps)
+    peak, peak_src = load_peaks()
+    mean_decode_s = float(np.mean(decode_ms)) / 1e3
+    achieved = per_layer["attn"] / mean_decode_s / 1e9
+    traffic = recorded_traffic(args.workload)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_max / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w, lengths, world),
+            "tokens_per_s_per_layer": round(world * w.batch * w.n_layers / (elapsed_max / args.steps), 1),
+            "decode_tokens_per_s": round(world * w.batch / (elapsed_max / args.steps), 1),
+            "decode_attn_pct_of_peak": round(100 * achieved / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "decode_split_kernel", "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback 6.8 TB/s",
+                         "bytes_per_launch": per_layer["attn"],
+                         "mean_launch_us": round(mean_decode_s * 1e6, 3)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    state.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_reference(args, rank, world, local):
+    """The oracle, as it stands, on the host cores: rank 0 only."""
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    lengths = synth.live_lengths(w).numpy()
+    host = cpu_host_inputs(w, lengths)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, 0.0, host)
+    import oracle
+    total_bytes, total_s, samples = 0.0, 0.0, 0
+    eb = synth.ELEM_BYTES[w.dtype]
+    for s in range(args.steps):
+        b = s % w.batch
+        t0 = time.perf_counter()
+        oracle.decode_attn(host[2][b:b + 1], host[0][b:b + 1], host[1][b:b + 1], lengths[b:b + 1], w.dtype)
+        total_s += time.perf_counter() - t0
+        total_bytes += 2 * w.n_kv_heads * w.d_head * eb * int(lengths[b]) + 2 * w.n_heads * w.d_head * eb
+        samples += 1
+    value = total_bytes / total_s / 1e9
+    sample = (f"fp64 oracle decode attention of layer 0, one sequence (all {w.n_heads} heads) per step, "
+              f"cycling over the batch; {samples} steps in {total_s:.1f} s")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / samples * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, lengths, world),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, rank, world, local)
+    else:
+        bench_kvc(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

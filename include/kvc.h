@@ -1,0 +1,206 @@
+/*
+ * kvc.h -- C ABI of the static KV-cache decode library (libkvc.so, sm_103a).
+ *
+ * The library implements one decode step over a KV cache that is allocated
+ * once, at full capacity, and never reallocated:
+ *
+ *   1. kvc_append: write the new token's K and V rows into the fixed buffer
+ *      at cache_index (slice assignment, never concatenation);
+ *   2. kvc_decode_attn: one query row per head attends over every live cache
+ *      row, softmax(q K^T / sqrt(d_head)) V, with each KV head shared by
+ *      n_heads / n_kv_heads query heads (grouped-query attention).
+ *
+ * Sources for the operations:
+ *   - "KV-Cache Mechanics" (DantinoX docs), AR Static KV-Cache: the cache is
+ *     pre-allocated at model construction with shape
+ *     [B, H_kv, max_context, head_size] per layer; prefill writes at
+ *     cache_index 0, each decode step at cache_index = tokens so far.
+ *   - "KV Cache Optimization: GQA Audit, In-Place Buffers, Persistent
+ *     Prompts", #2 In-place KV cache updates (After): append slice-assigns
+ *     rows [valid, valid + T_new) of one [B, H, capacity, D] buffer per K and
+ *     V; reads are sliced to the live length so padded rows are not attended.
+ *     #1 GQA-aware KV cache audit: K/V are stored with n_kv_heads heads.
+ *   - "10.3 -- KV cache implementation details", section 5 (the decode loop,
+ *     step-by-step): append k_t, v_t to the layer's cache, then attention of
+ *     the single query row against the entire cache -- "the only place the
+ *     cache is read"; section 4.2: GQA shares each KV head across
+ *     n_heads / g query heads; sections 2 and 4.4: the cache-size formula.
+ *
+ * Conventions for every call:
+ *   - All tensors are dense, row-major, innermost dimension contiguous, in
+ *     the cache's element type (kvc_dtype).  Device pointers are CUDA device
+ *     memory of the device that was current at kvc_alloc; host pointers are
+ *     marked "host".
+ *   - The caller owns every buffer (cache, inputs, outputs, workspace).  The
+ *     library owns only the kvc_cache handle; it never allocates device
+ *     memory and never frees caller memory.
+ *   - Calls that take a stream enqueue asynchronously on it (stream is a
+ *     cudaStream_t passed as void*; NULL means the legacy default stream).
+ *     Their return value reports only errors detectable on the host before
+ *     launch; nothing is enqueued when it is not KVC_OK.  Errors that depend
+ *     on device-resident values (cache_index, valid_len) are recorded in a
+ *     device error word inside the workspace and read with kvc_get_error.
+ *   - The library is stateless with respect to sequence lengths: the caller
+ *     tracks them (passing cache_index to append and valid_len to attention)
+ *     exactly as the optimisation note's KVCache tracks validLengths.
+ *     Rewinding a sequence is lowering its length on the caller's side.
+ *   - Calls on one handle that overlap on the GPU (different streams without
+ *     ordering) race on the workspace; order them on one stream.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+
+/* Status codes.  KVC_OK is 0; every other value is an error. */
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_INVALID = 1,      /* bad argument: null pointer, shape, layer, dtype */
+    KVC_ERR_CAPACITY = 2,     /* an append would pass max_context */
+    KVC_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    KVC_ERR_WORKSPACE = 4,    /* workspace missing or smaller than kvc_workspace_bytes */
+    KVC_ERR_TIMEOUT = 5,      /* a bounded wait inside a kernel gave up (device word) */
+    KVC_ERR_DEVICE_INDEX = 6, /* a device-resident cache_index / valid_len was out of range */
+    KVC_ERR_UNSUPPORTED = 7,  /* configuration outside the compiled kernel set */
+    KVC_ERR_ALIGNMENT = 8     /* a pointer is not 16-byte aligned */
+} kvc_status;
+
+/* Element type of the cache, of q / k_new / v_new, and of the output.
+ * Bytes per element p: bf16 2, fp32 4, fp16 2 ("10.3", section 2). */
+typedef enum { KVC_BF16 = 0, KVC_FP32 = 1, KVC_FP16 = 2 } kvc_dtype;
+
+/* Model shape of one static cache.
+ *   n_layers     L, number of per-layer caches held in one allocation
+ *   batch        B, sequences
+ *   n_heads      H, query heads
+ *   n_kv_heads   H_kv, KV heads; must divide H (g = H / H_kv query heads share one)
+ *   d_head       d_h, head width: 32, 64, 128 or 256
+ *   max_context  T_max, rows allocated per (layer, sequence, KV head)
+ *   dtype        kvc_dtype
+ * Supported head groups g = n_heads / n_kv_heads: 1 to 8. */
+typedef struct {
+    int32_t n_layers;
+    int32_t batch;
+    int32_t n_heads;
+    int32_t n_kv_heads;
+    int32_t d_head;
+    int32_t max_context;
+    int32_t dtype;
+} kvc_config;
+
+typedef struct kvc_cache kvc_cache; /* opaque handle */
+
+/* ---- host-only queries (no GPU needed) -------------------------------- */
+
+/* Library ABI version (KVC_ABI_VERSION). */
+int32_t kvc_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *kvc_status_str(int32_t status);
+
+/* Check a configuration on the host: KVC_OK, KVC_ERR_INVALID (nonsense
+ * shape) or KVC_ERR_UNSUPPORTED (no compiled kernel for it). */
+kvc_status kvc_check_config(const kvc_config *cfg);
+
+/* Bytes of the whole static cache, K and V, all layers:
+ *   2 * n_layers * n_kv_heads * d_head * max_context * batch * p
+ * ("10.3", section 2 boxed formula with n_kv_heads as in section 4.4; the
+ * "Key-value cache" lesson record's payload estimate).  0 if cfg is invalid. */
+uint64_t kvc_cache_bytes(const kvc_config *cfg);
+
+/* Growth of one sequence's cache per token: 2 * n_layers * n_kv_heads *
+ * d_head * p ("10.3", section 2.2; lesson record "per token per sequence").
+ * 0 if cfg is invalid. */
+uint64_t kvc_bytes_per_token(const kvc_config *cfg);
+
+/* Bytes of device workspace kvc_alloc needs for cfg: split partials
+ * (max, sum, accumulator per split of each sequence/KV head/query head),
+ * one counter per (sequence, KV head), and the device error word.
+ * 0 if cfg is invalid. */
+uint64_t kvc_workspace_bytes(const kvc_config *cfg);
+
+/* ---- handle -------------------------------------------------------------- */
+
+/* Bind caller-owned device buffers to a new handle.
+ *   k_base, v_base  device, each n_layers * batch * n_kv_heads * max_context
+ *                   * d_head elements, laid out [L, B, H_kv, T_max, d_h]
+ *                   (layer l's cache starts at element
+ *                   l * B * H_kv * T_max * d_h); 16-byte aligned.
+ *   workspace       device, ws_bytes >= kvc_workspace_bytes(cfg); 16-byte
+ *                   aligned.  kvc_alloc zeroes it (synchronously); it must
+ *                   not be used for anything else while the handle lives.
+ *   out             host; receives the handle on KVC_OK, untouched otherwise.
+ * Uses the current CUDA device; later calls must run with it current.
+ * Returns KVC_ERR_INVALID / _UNSUPPORTED / _ALIGNMENT / _WORKSPACE / _CUDA. */
+kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base,
+                     void *workspace, uint64_t ws_bytes, kvc_cache **out);
+
+/* Release the handle (host memory only).  Caller buffers stay untouched.
+ * NULL is accepted. */
+void kvc_free(kvc_cache *h);
+
+/* Override the number of context splits (CTAs) of kvc_decode_attn: 0 restores
+ * the automatic choice, otherwise 1..1024.  Results agree across split
+ * counts up to fp32 rounding. */
+kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n);
+
+/* ---- the decode step ------------------------------------------------------ */
+
+/* In-place append ("KV Cache Optimization...", #2 After; "10.3", section 5:
+ * "Append k_t, v_t to the layer's KV cache"):
+ *   K_l[b, j, cache_index[b] + t, :] = k_new[b, j, t, :]   for t < T_new
+ * and the same for V, for every sequence b and KV head j.  A pure byte copy;
+ * no other cache row is written.
+ *   layer        0 <= layer < n_layers
+ *   k_new, v_new device, [B, H_kv, T_new, d_h], 16-byte aligned
+ *   cache_index  device int32 [B]: write position of each sequence (its live
+ *                length before the append).  A sequence whose
+ *                cache_index[b] < 0 or cache_index[b] + T_new > max_context is
+ *                skipped and KVC_ERR_DEVICE_INDEX is recorded.
+ *   T_new        rows per sequence, 0 <= T_new <= max_context (0: no-op)
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_CAPACITY (T_new > max_context),
+ * KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new,
+                      const void *v_new, const int32_t *cache_index,
+                      int32_t T_new, void *stream);
+
+/* Single-query decode attention ("10.3", section 5, attention bullet):
+ *   out[b, i, :] = softmax_j( q[b, i, :] . K_l[b, i / g, j, :] / sqrt(d_h) )
+ *                  . V_l[b, i / g, j, :]       over j < valid_len[b]
+ * with g = n_heads / n_kv_heads (query head i reads KV head i / g, the
+ * contiguous grouping).  Rows at or past valid_len[b] are never read.
+ * Arithmetic: fp32 products and accumulation, one round-to-nearest-even to
+ * the cache type at the end.
+ *   layer           0 <= layer < n_layers
+ *   q               device, [B, H, d_h], 16-byte aligned
+ *   valid_len       device int32 [B]: live rows of each sequence, counting
+ *                   this step's appended row.  A sequence with valid_len[b]
+ *                   < 1 or > max_context is skipped (its output rows are left
+ *                   unwritten) and KVC_ERR_DEVICE_INDEX is recorded.
+ *   max_valid_hint  host; 0, or an upper bound on valid_len used only to size
+ *                   the launch without a device-to-host read.
+ *   out             device, [B, H, d_h]
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q,
+                           const int32_t *valid_len, int32_t max_valid_hint,
+                           void *out, void *stream);
+
+/* Synchronise the stream, then read and clear the device error word.
+ * Returns KVC_OK if no kernel recorded an error since the last call,
+ * otherwise the first recorded code (KVC_ERR_DEVICE_INDEX or
+ * KVC_ERR_TIMEOUT).  After KVC_ERR_TIMEOUT the split counters are reset too.
+ * KVC_ERR_CUDA if the synchronisation or the copy fails. */
+kvc_status kvc_get_error(kvc_cache *h, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

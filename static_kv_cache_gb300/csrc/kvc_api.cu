@@ -1,0 +1,250 @@
+// kvc_api.cu -- host side of libkvc.so: argument checks, launch planning and
+// the extern "C" entry points declared in include/kvc.h.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/kvc.h"
+#include "kvc_internal.cuh"
+
+struct kvc_cache {
+    kvc_config cfg;
+    int device;
+    int num_sms;
+    int max_smem;            // opt-in dynamic shared memory per block
+    int elem_bytes;
+    int group;               // n_heads / n_kv_heads
+    int num_splits;          // 0: automatic
+    uint8_t *k_base;
+    uint8_t *v_base;
+    uint8_t *ws;
+    uint64_t ws_bytes;
+    kvc::WorkspaceLayout wl;
+    const kvc::DecodeKernelInfo *decode;
+    int n_stages;
+    int smem_bytes;
+};
+
+namespace {
+
+int elem_bytes_of(int32_t dtype) {
+    switch (dtype) {
+        case KVC_BF16: return 2;
+        case KVC_FP16: return 2;
+        case KVC_FP32: return 4;
+        default: return 0;
+    }
+}
+
+bool shape_ok(const kvc_config *c) {
+    return c && c->n_layers > 0 && c->batch > 0 && c->n_heads > 0 && c->n_kv_heads > 0 &&
+           c->d_head > 0 && c->max_context > 0 && c->n_heads % c->n_kv_heads == 0 &&
+           elem_bytes_of(c->dtype) > 0;
+}
+
+const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
+    const int G = c->n_heads / c->n_kv_heads;
+    const int D = c->d_head;
+#define KVC_PICK(TAG, DD) \
+    if (D == DD) return kvc::decode_kernel_##TAG##_##DD(G);
+    switch (c->dtype) {
+        case KVC_BF16:
+            KVC_PICK(bf16, 32) KVC_PICK(bf16, 64) KVC_PICK(bf16, 128) KVC_PICK(bf16, 256) break;
+        case KVC_FP16:
+            KVC_PICK(f16, 32) KVC_PICK(f16, 64) KVC_PICK(f16, 128) KVC_PICK(f16, 256) break;
+        case KVC_FP32:
+            KVC_PICK(f32, 32) KVC_PICK(f32, 64) KVC_PICK(f32, 128) KVC_PICK(f32, 256) break;
+        default: break;
+    }
+#undef KVC_PICK
+    return nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t layer_slab_bytes(const kvc_cache *h) {
+    const kvc_config &c = h->cfg;
+    return uint64_t(c.batch) * c.n_kv_heads * uint64_t(c.max_context) * c.d_head * h->elem_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+const char *kvc_status_str(int32_t s) {
+    switch (s) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_INVALID: return "invalid argument";
+        case KVC_ERR_CAPACITY: return "append would pass max_context";
+        case KVC_ERR_CUDA: return "CUDA runtime error";
+        case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+        case KVC_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+        case KVC_ERR_DEVICE_INDEX: return "device-resident cache_index or valid_len out of range";
+        case KVC_ERR_UNSUPPORTED: return "configuration not supported by the compiled kernels";
+        case KVC_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+kvc_status kvc_check_config(const kvc_config *cfg) {
+    if (!shape_ok(cfg)) return KVC_ERR_INVALID;
+    if (!find_decode(cfg)) return KVC_ERR_UNSUPPORTED;
+    return KVC_OK;
+}
+
+uint64_t kvc_cache_bytes(const kvc_config *c) {
+    if (!shape_ok(c)) return 0;
+    return 2ull * uint64_t(c->n_layers) * uint64_t(c->n_kv_heads) * uint64_t(c->d_head) *
+           uint64_t(c->max_context) * uint64_t(c->batch) * uint64_t(elem_bytes_of(c->dtype));
+}
+
+uint64_t kvc_bytes_per_token(const kvc_config *c) {
+    if (!shape_ok(c)) return 0;
+    return 2ull * uint64_t(c->n_layers) * uint64_t(c->n_kv_heads) * uint64_t(c->d_head) *
+           uint64_t(elem_bytes_of(c->dtype));
+}
+
+uint64_t kvc_workspace_bytes(const kvc_config *c) {
+    if (!shape_ok(c)) return 0;
+    return kvc::workspace_layout(c->batch, c->n_kv_heads, c->n_heads / c->n_kv_heads, c->d_head).total;
+}
+
+kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *workspace,
+                     uint64_t ws_bytes, kvc_cache **out) {
+    if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
+    const kvc::DecodeKernelInfo *info = find_decode(cfg);
+    if (!info) return KVC_ERR_UNSUPPORTED;
+    if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
+        return KVC_ERR_ALIGNMENT;
+    const uint64_t need = kvc_workspace_bytes(cfg);
+    if (!workspace || ws_bytes < need) return KVC_ERR_WORKSPACE;
+
+    int dev = 0, sms = 0, smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return KVC_ERR_CUDA;
+
+    // As many pipeline stages as shared memory holds (at most 32), but at
+    // least one more than there are consumer warps.
+    int n_stages = (smem - info->fixed_smem) / info->stage_bytes;
+    if (n_stages > 32) n_stages = 32;
+    if (n_stages < info->consumer_warps + 1) return KVC_ERR_UNSUPPORTED;
+    const int smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;
+    if (info->set_max_smem(smem_bytes) != cudaSuccess) return KVC_ERR_CUDA;
+
+    // Zero the workspace: error word and per-segment counters start at 0.
+    if (cudaMemsetAsync(workspace, 0, need, 0) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(0) != cudaSuccess) return KVC_ERR_CUDA;
+
+    kvc_cache *h = new (std::nothrow) kvc_cache;
+    if (!h) return KVC_ERR_INVALID;
+    h->cfg = *cfg;
+    h->device = dev;
+    h->num_sms = sms;
+    h->max_smem = smem;
+    h->elem_bytes = elem_bytes_of(cfg->dtype);
+    h->group = cfg->n_heads / cfg->n_kv_heads;
+    h->num_splits = 0;
+    h->k_base = static_cast<uint8_t *>(k_base);
+    h->v_base = static_cast<uint8_t *>(v_base);
+    h->ws = static_cast<uint8_t *>(workspace);
+    h->ws_bytes = ws_bytes;
+    h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads, h->group, cfg->d_head);
+    h->decode = info;
+    h->n_stages = n_stages;
+    h->smem_bytes = smem_bytes;
+    *out = h;
+    return KVC_OK;
+}
+
+void kvc_free(kvc_cache *h) { delete h; }
+
+kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n) {
+    if (!h || n < 0 || n > kvc::MAX_CTAS) return KVC_ERR_INVALID;
+    h->num_splits = n;
+    return KVC_OK;
+}
+
+kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void *v_new,
+                      const int32_t *cache_index, int32_t T_new, void *stream) {
+    if (!h || layer < 0 || layer >= h->cfg.n_layers || T_new < 0) return KVC_ERR_INVALID;
+    if (T_new == 0) return KVC_OK;
+    if (!k_new || !v_new || !cache_index) return KVC_ERR_INVALID;
+    if (T_new > h->cfg.max_context) return KVC_ERR_CAPACITY;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
+    const uint64_t slab = layer_slab_bytes(h);
+    const cudaError_t e = kvc::launch_append(
+        h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
+        static_cast<const uint8_t *>(v_new), cache_index, h->cfg.batch, h->cfg.n_kv_heads, T_new,
+        h->cfg.max_context, h->cfg.d_head * h->elem_bytes, reinterpret_cast<int32_t *>(h->ws),
+        h->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int32_t *valid_len,
+                           int32_t max_valid_hint, void *out, void *stream) {
+    if (!h || layer < 0 || layer >= h->cfg.n_layers || !q || !valid_len || !out)
+        return KVC_ERR_INVALID;
+    if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
+    if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
+    const kvc_config &c = h->cfg;
+
+    // Splits: every SM streams an equal share of the live rows; tiny
+    // problems use fewer CTAs so that each still gets several tiles.
+    int grid = h->num_splits;
+    if (grid == 0) {
+        const int64_t upper_rows =
+            int64_t(c.batch) * c.n_kv_heads * (max_valid_hint > 0 ? max_valid_hint : c.max_context);
+        const int64_t min_rows = 4 * int64_t(h->decode->tile_rows);
+        int64_t want = (upper_rows + min_rows - 1) / min_rows;
+        if (want > h->num_sms) want = h->num_sms;
+        if (want < 1) want = 1;
+        grid = int(want);
+    }
+    if (grid > kvc::MAX_CTAS) grid = kvc::MAX_CTAS;
+
+    const uint64_t slab = layer_slab_bytes(h);
+    kvc::DecodeArgs a;
+    a.K = h->k_base + slab * layer;
+    a.V = h->v_base + slab * layer;
+    a.q = q;
+    a.out = out;
+    a.valid_len = valid_len;
+    a.part_ml = reinterpret_cast<float *>(h->ws + h->wl.part_ml);
+    a.part_acc = reinterpret_cast<float *>(h->ws + h->wl.part_acc);
+    a.tickets = reinterpret_cast<int32_t *>(h->ws + h->wl.tickets);
+    a.err = reinterpret_cast<int32_t *>(h->ws);
+    a.B = c.batch;
+    a.H_kv = c.n_kv_heads;
+    a.max_ctx = c.max_context;
+    a.n_stages = h->n_stages;
+    a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
+    a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+kvc_status kvc_get_error(kvc_cache *h, void *stream) {
+    if (!h) return KVC_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, h->ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(h->ws, 0, sizeof word) != cudaSuccess) return KVC_ERR_CUDA;
+        if (word == KVC_ERR_TIMEOUT) {
+            const uint64_t n = uint64_t(h->cfg.batch) * h->cfg.n_kv_heads * 4;
+            if (cudaMemset(h->ws + h->wl.tickets, 0, n) != cudaSuccess) return KVC_ERR_CUDA;
+        }
+        if (cudaDeviceSynchronize() != cudaSuccess) return KVC_ERR_CUDA;
+    }
+    return static_cast<kvc_status>(word);
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// kvc_append.cu -- in-place append of new K/V rows into the static cache.
+//
+// "KV Cache Optimization: GQA Audit, In-Place Buffers, Persistent Prompts",
+// #2 In-place KV cache updates (After): rows [valid, valid + T_new) of the
+// pre-allocated [B, H, capacity, D] buffer are slice-assigned; nothing is
+// concatenated or reallocated.  "10.3 -- KV cache implementation details",
+// section 5: appending k_t, v_t is the only cache write of a decode step.
+//
+// For every (sequence b, KV head j) the T_new source rows k_new[b, j, :, :]
+// and the destination rows K[b, j, cache_index[b] : cache_index[b] + T_new, :]
+// are both contiguous runs of T_new * row_bytes bytes, so the whole append is
+// a set of contiguous copies.  One thread moves one 16-byte vector;
+// consecutive threads move consecutive vectors of a run (coalesced on both
+// sides).  K and V are handled by the same launch.
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+__global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, uint8_t *__restrict__ V,
+                                                     const uint8_t *__restrict__ k_new,
+                                                     const uint8_t *__restrict__ v_new,
+                                                     const int32_t *__restrict__ cache_index, int B,
+                                                     int H_kv, int T_new, int max_ctx, int row_vecs,
+                                                     int32_t *err) {
+    const int64_t run = int64_t(T_new) * row_vecs;   // vectors per (b, j)
+    const int64_t per_tensor = int64_t(B) * H_kv * run;
+    const int64_t total = 2 * per_tensor;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const bool is_v = i >= per_tensor;
+        const int64_t r = is_v ? i - per_tensor : i;
+        const int64_t seg = r / run;                 // b * H_kv + j
+        const int64_t off = r - seg * run;           // vector within the run
+        const int b = int(seg / H_kv);
+        const int ci = __ldg(cache_index + b);
+        if (ci < 0 || ci > max_ctx - T_new) {
+            if (off == 0 && seg % H_kv == 0 && !is_v) atomicCAS(err, 0, ERR_DEVICE_INDEX);
+            continue;
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(is_v ? v_new : k_new) + seg * run + off;
+        uint4 *dst = reinterpret_cast<uint4 *>(is_v ? V : K) +
+                     (seg * max_ctx + ci) * int64_t(row_vecs) + off;
+        *dst = __ldg(src);
+    }
+}
+
+cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
+                          const uint8_t *v_new, const int32_t *cache_index, int B, int H_kv,
+                          int T_new, int max_ctx, int row_bytes, int32_t *err, int num_sms,
+                          cudaStream_t stream) {
+    const int row_vecs = row_bytes / 16;
+    const int64_t total = 2 * int64_t(B) * H_kv * T_new * row_vecs;
+    if (total == 0) return cudaSuccess;
+    const int64_t want = (total + 255) / 256;
+    const int64_t cap = int64_t(num_sms) * 8;
+    const int grid = int(want < cap ? want : cap);
+    append_kernel<<<grid, 256, 0, stream>>>(K_layer, V_layer, k_new, v_new, cache_index, B, H_kv, T_new,
+                                            max_ctx, row_vecs, err);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,44 @@
+// kvc_decode_inst.cu -- explicit decode kernels for one (element type, head
+// width), selected at compile time by KVC_INST_TYPE (0 bf16, 1 fp16, 2 fp32)
+// and KVC_INST_D.  The build compiles this file once per pair, in parallel.
+#include "kvc_decode.cuh"
+
+#ifndef KVC_INST_TYPE
+#error "KVC_INST_TYPE must be defined"
+#endif
+#ifndef KVC_INST_D
+#error "KVC_INST_D must be defined"
+#endif
+
+#if KVC_INST_TYPE == 0
+#define KVC_ELEM __nv_bfloat16
+#define KVC_TAG bf16
+#elif KVC_INST_TYPE == 1
+#define KVC_ELEM __half
+#define KVC_TAG f16
+#else
+#define KVC_ELEM float
+#define KVC_TAG f32
+#endif
+
+#define KVC_CAT2(a, b, c) decode_kernel_##a##_##b
+#define KVC_CAT(a, b) KVC_CAT2(a, b, 0)
+#define KVC_TABLE_FN KVC_CAT(KVC_TAG, KVC_INST_D)
+
+namespace kvc {
+
+const DecodeKernelInfo *KVC_TABLE_FN(int G) {
+    switch (G) {
+        case 1: return decode_info<KVC_ELEM, KVC_INST_D, 1>();
+        case 2: return decode_info<KVC_ELEM, KVC_INST_D, 2>();
+        case 3: return decode_info<KVC_ELEM, KVC_INST_D, 3>();
+        case 4: return decode_info<KVC_ELEM, KVC_INST_D, 4>();
+        case 5: return decode_info<KVC_ELEM, KVC_INST_D, 5>();
+        case 6: return decode_info<KVC_ELEM, KVC_INST_D, 6>();
+        case 7: return decode_info<KVC_ELEM, KVC_INST_D, 7>();
+        case 8: return decode_info<KVC_ELEM, KVC_INST_D, 8>();
+        default: return nullptr;
+    }
+}
+
+}  // namespace kvc

@@ -1,0 +1,185 @@
+// kvc_internal.cuh -- definitions shared by the kernels and the host API of
+// libkvc.so.  Not part of the public ABI (see include/kvc.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvc {
+
+// Device error codes written to the workspace error word (match kvc_status).
+constexpr int32_t ERR_TIMEOUT = 5;
+constexpr int32_t ERR_DEVICE_INDEX = 6;
+
+// Upper bound on the CTAs of one decode launch; sizes the split partials.
+constexpr int MAX_CTAS = 1024;
+
+// Default bound on any single wait inside a kernel.
+constexpr unsigned long long WAIT_TIMEOUT_NS = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// ---------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned):
+//   [0, 256)            error word (int32) + padding
+//   tickets             int32 [B * H_kv]         arrivals per (sequence, KV head)
+//   part_ml             float [slots][G][2]      (running max, sum) per split
+//   part_acc            float [slots][G][D]      unnormalised output per split
+// slots = MAX_CTAS + B * H_kv: split c of segment s uses slot c + s, which is
+// unique because the splits and the segments are both contiguous ranges of
+// one flattened row space (every new piece starts a new split, a new
+// segment, or both).
+// ---------------------------------------------------------------------------
+struct WorkspaceLayout {
+    uint64_t tickets, part_ml, part_acc, total;
+};
+
+inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+inline WorkspaceLayout workspace_layout(int B, int H_kv, int G, int D) {
+    WorkspaceLayout w;
+    const uint64_t segs = uint64_t(B) * H_kv;
+    const uint64_t slots = uint64_t(MAX_CTAS) + segs;
+    w.tickets = 256;
+    w.part_ml = align256(w.tickets + segs * 4);
+    w.part_acc = align256(w.part_ml + slots * G * 2 * 4);
+    w.total = align256(w.part_acc + slots * G * uint64_t(D) * 4);
+    return w;
+}
+
+// Arguments of the decode kernel (passed by value as a grid constant).
+struct DecodeArgs {
+    const uint8_t *K;          // layer slab of the K cache, [B, H_kv, max_ctx, D]
+    const uint8_t *V;          // layer slab of the V cache
+    const void *q;             // [B, H, D]
+    void *out;                 // [B, H, D]
+    const int32_t *valid_len;  // [B]
+    float *part_ml;
+    float *part_acc;
+    int32_t *tickets;
+    int32_t *err;
+    int32_t B, H_kv, max_ctx;
+    int32_t n_stages;
+    float scale_log2;          // log2(e) / sqrt(D)
+    unsigned long long timeout_ns;
+};
+
+// One compiled decode kernel and what the host needs to launch it.
+struct DecodeKernelInfo {
+    int tile_rows;       // rows of K (and of V) per pipeline stage
+    int consumer_warps;  // warps that compute; one more warp issues the copies
+    int stage_bytes;     // K tile + V tile
+    int fixed_smem;      // dynamic shared memory besides the stages
+    cudaError_t (*set_max_smem)(int bytes);
+    cudaError_t (*launch)(const DecodeArgs &a, int grid, int smem, cudaStream_t s);
+};
+
+// Registry of compiled decode kernels, one lookup per (element type, D);
+// each returns nullptr for an unsupported group size.
+#define KVC_DECLARE_DECODE_TABLE(TAG, D) \
+    const DecodeKernelInfo *decode_kernel_##TAG##_##D(int G);
+KVC_DECLARE_DECODE_TABLE(bf16, 32)
+KVC_DECLARE_DECODE_TABLE(bf16, 64)
+KVC_DECLARE_DECODE_TABLE(bf16, 128)
+KVC_DECLARE_DECODE_TABLE(bf16, 256)
+KVC_DECLARE_DECODE_TABLE(f16, 32)
+KVC_DECLARE_DECODE_TABLE(f16, 64)
+KVC_DECLARE_DECODE_TABLE(f16, 128)
+KVC_DECLARE_DECODE_TABLE(f16, 256)
+KVC_DECLARE_DECODE_TABLE(f32, 32)
+KVC_DECLARE_DECODE_TABLE(f32, 64)
+KVC_DECLARE_DECODE_TABLE(f32, 128)
+KVC_DECLARE_DECODE_TABLE(f32, 256)
+#undef KVC_DECLARE_DECODE_TABLE
+
+// Append launcher (kvc_append.cu).
+cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
+                          const uint8_t *v_new, const int32_t *cache_index, int B,
+                          int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err,
+                          int num_sms, cudaStream_t stream);
+
+}  // namespace kvc
+
+// ---------------------------------------------------------------------------
+// Device helpers: inline PTX for mbarriers, bulk (TMA) copies and timers.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace kvc {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) when *abort becomes non-zero, after timeout_ns of wall
+// time, or after 2^30 polls, whichever comes first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int *abort,
+                                                  unsigned long long timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> shared through the TMA unit; completion is
+// signalled on `bar` as transaction bytes.  dst, src and bytes must be
+// multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
+    atomicCAS(err, 0, code);
+}
+
+}  // namespace dev
+}  // namespace kvc
+#endif

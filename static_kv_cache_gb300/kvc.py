@@ -1,0 +1,159 @@
+"""ctypes binding of libkvc.so -- argument marshalling only.
+
+Every function here has the name and argument order of the C function in
+``include/kvc.h`` and returns what it returns (a ``kvc_status`` int, a size,
+or, for ``kvc_alloc``, ``(status, handle)``).  Pointer arguments accept an
+int address or any object with ``data_ptr()`` (a torch tensor); stream
+arguments accept an int handle, ``None`` (legacy default stream) or any object
+with ``cuda_stream`` (a torch stream).  No computation happens in Python.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+KVC_OK = 0
+KVC_ERR_INVALID = 1
+KVC_ERR_CAPACITY = 2
+KVC_ERR_CUDA = 3
+KVC_ERR_WORKSPACE = 4
+KVC_ERR_TIMEOUT = 5
+KVC_ERR_DEVICE_INDEX = 6
+KVC_ERR_UNSUPPORTED = 7
+KVC_ERR_ALIGNMENT = 8
+
+KVC_BF16 = 0
+KVC_FP32 = 1
+KVC_FP16 = 2
+DTYPE_CODES = {"bf16": KVC_BF16, "fp32": KVC_FP32, "fp16": KVC_FP16}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+        "(the decode path has no fallback without its CUDA library)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class kvc_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("d_head", ctypes.c_int32), ("max_context", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class KvcError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        super().__init__(f"{what}: {kvc_status_str(status)} ({status})" if what
+                         else f"{kvc_status_str(status)} ({status})")
+        self.status = status
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_u64 = ctypes.c_uint64
+_cfgp = ctypes.POINTER(kvc_config)
+
+_lib.kvc_abi_version.restype = _i32
+_lib.kvc_status_str.argtypes = [_i32]
+_lib.kvc_status_str.restype = ctypes.c_char_p
+_lib.kvc_check_config.argtypes = [_cfgp]
+_lib.kvc_check_config.restype = _i32
+for _n in ("kvc_cache_bytes", "kvc_bytes_per_token", "kvc_workspace_bytes"):
+    getattr(_lib, _n).argtypes = [_cfgp]
+    getattr(_lib, _n).restype = _u64
+_lib.kvc_alloc.argtypes = [_cfgp, _vp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
+_lib.kvc_alloc.restype = _i32
+_lib.kvc_free.argtypes = [_vp]
+_lib.kvc_free.restype = None
+_lib.kvc_set_num_splits.argtypes = [_vp, _i32]
+_lib.kvc_set_num_splits.restype = _i32
+_lib.kvc_append.argtypes = [_vp, _i32, _vp, _vp, _vp, _i32, _vp]
+_lib.kvc_append.restype = _i32
+_lib.kvc_decode_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _vp, _vp]
+_lib.kvc_decode_attn.restype = _i32
+_lib.kvc_get_error.argtypes = [_vp, _vp]
+_lib.kvc_get_error.restype = _i32
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+def make_config(n_layers, batch, n_heads, n_kv_heads, d_head, max_context, dtype) -> kvc_config:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return kvc_config(n_layers, batch, n_heads, n_kv_heads, d_head, max_context, code)
+
+
+def kvc_abi_version() -> int:
+    return _lib.kvc_abi_version()
+
+
+def kvc_status_str(status: int) -> str:
+    return _lib.kvc_status_str(int(status)).decode()
+
+
+def kvc_check_config(cfg: kvc_config) -> int:
+    return _lib.kvc_check_config(ctypes.byref(cfg))
+
+
+def kvc_cache_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_cache_bytes(ctypes.byref(cfg))
+
+
+def kvc_bytes_per_token(cfg: kvc_config) -> int:
+    return _lib.kvc_bytes_per_token(ctypes.byref(cfg))
+
+
+def kvc_workspace_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_workspace_bytes(ctypes.byref(cfg))
+
+
+def kvc_alloc(cfg: kvc_config, k_base, v_base, workspace, ws_bytes: int):
+    h = _vp()
+    st = _lib.kvc_alloc(ctypes.byref(cfg), _ptr(k_base), _ptr(v_base), _ptr(workspace),
+                        int(ws_bytes), ctypes.byref(h))
+    return st, (h.value if st == KVC_OK else None)
+
+
+def kvc_free(h) -> None:
+    _lib.kvc_free(h)
+
+
+def kvc_set_num_splits(h, n: int) -> int:
+    return _lib.kvc_set_num_splits(h, int(n))
+
+
+def kvc_append(h, layer: int, k_new, v_new, cache_index, T_new: int, stream=None) -> int:
+    return _lib.kvc_append(h, int(layer), _ptr(k_new), _ptr(v_new), _ptr(cache_index),
+                           int(T_new), _stream(stream))
+
+
+def kvc_decode_attn(h, layer: int, q, valid_len, max_valid_hint: int, out, stream=None) -> int:
+    return _lib.kvc_decode_attn(h, int(layer), _ptr(q), _ptr(valid_len), int(max_valid_hint),
+                                _ptr(out), _stream(stream))
+
+
+def kvc_get_error(h, stream=None) -> int:
+    return _lib.kvc_get_error(h, _stream(stream))
+
+
+def check(status: int, what: str = "") -> None:
+    """Raise KvcError unless status is KVC_OK."""
+    if status != KVC_OK:
+        raise KvcError(status, what)

@@ -16,3 +16,10 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load_library()
+
+
+@pytest.fixture(scope="session")
+def kvc_library_path():
+    """Build libkvc.so if needed (nvcc cross-compiles without a GPU)."""
+    from static_kv_cache_gb300 import build
+    return build.build()
