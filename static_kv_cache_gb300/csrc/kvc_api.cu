@@ -131,7 +131,8 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
 
     // As many pipeline stages as shared memory holds (at most 32), but at
     // least one more than there are consumer warps.
-    int n_stages = (smem - info->fixed_smem) / info->stage_bytes;
+    const int budget = smem < kvc::SMEM_BUDGET ? smem : kvc::SMEM_BUDGET;
+    int n_stages = (budget - info->fixed_smem) / info->stage_bytes;
     if (n_stages > 32) n_stages = 32;
     if (n_stages < info->consumer_warps + 1) return KVC_ERR_UNSUPPORTED;
     const int smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;

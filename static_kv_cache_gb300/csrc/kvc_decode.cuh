@@ -117,8 +117,9 @@ struct DecodeCfg {
     static constexpr int SHIFT = ilog2(LPR / NPASS);
     static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
-    static constexpr int NW = 8;                        // consumer warps
-    static constexpr int PBUF_FLOATS = NW * TILE * G;
+    static constexpr int NW = 7;                        // consumer warps (+1 producer = 256 threads)
+    static constexpr int GP = (G + 3) & ~3;             // probabilities per row, padded to 16 bytes
+    static constexpr int PBUF_FLOATS = NW * TILE * GP;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
     static constexpr int FIXED_SMEM = 4 * (PBUF_FLOATS + SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
@@ -241,6 +242,57 @@ struct Walker {
     }
 };
 
+// The producer: one thread walks the CTA's pieces and streams every tile of
+// K and V into the stage ring with 1-D bulk copies.
+template <typename C>
+__device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker walk, uint32_t stage0,
+                                                  uint32_t bar0, int ns, int64_t kv_slab,
+                                                  volatile int *flags) {
+    constexpr int TILE = C::TILE;
+    uint32_t issued = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    Piece pc;
+    while (ok && walk.next(a, pc)) {
+        const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
+        const uint8_t *kseg = a.K + seg * kv_slab;
+        const uint8_t *vseg = a.V + seg * kv_slab;
+        for (int row = pc.lo; row < pc.hi; row += TILE) {
+            const int nr = min(TILE, pc.hi - row);
+            if (round > 0 &&
+                !dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns)) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+                ok = false;
+                break;
+            }
+            const uint32_t bytes = uint32_t(nr) * C::ROW_BYTES;
+            const uint32_t full = bar0 + 8 * stage;
+            const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
+            dev::mbar_arrive_expect_tx(full, 2 * bytes);
+            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            ++issued;
+            if (++stage == ns) {
+                stage = 0;
+                ++round;
+            }
+        }
+    }
+    return issued;
+}
+
+// After an abort, wait (bounded) for the copies of the last ns issued tiles,
+// the only ones that can still be in flight, before shared memory is freed.
+__device__ __forceinline__ void drain_copies(uint32_t bar0, int ns, uint32_t issued,
+                                             unsigned long long timeout_ns) {
+    const volatile int never = 0;
+    const uint32_t first = issued > uint32_t(ns) ? issued - ns : 0;
+    for (uint32_t t = first; t < issued; ++t)
+        dev::mbar_wait_bounded(bar0 + 8 * (t % ns), (t / ns) & 1, &never, timeout_ns);
+}
+
 // --------------------------------------------------------------------------
 // The kernel.
 // --------------------------------------------------------------------------
@@ -284,46 +336,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
-        if (lane != 0) return;
         uint32_t issued = 0;
-        int stage = 0;
-        uint32_t round = 0;
-        bool ok = true;
-        Piece pc;
-        while (ok && walk.next(a, pc)) {
-            const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
-            const uint8_t *kseg = a.K + seg * kv_slab;
-            const uint8_t *vseg = a.V + seg * kv_slab;
-            for (int row = pc.lo; row < pc.hi; row += TILE) {
-                const int nr = min(TILE, pc.hi - row);
-                if (round > 0 &&
-                    !dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns)) {
-                    if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
-                    flags[0] = 1;
-                    ok = false;
-                    break;
-                }
-                const uint32_t bytes = uint32_t(nr) * C::ROW_BYTES;
-                const uint32_t full = bar0 + 8 * stage;
-                const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
-                dev::mbar_arrive_expect_tx(full, 2 * bytes);
-                dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
-                dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
-                ++issued;
-                if (++stage == ns) {
-                    stage = 0;
-                    ++round;
-                }
-            }
-        }
-        if (flags[0]) {
-            // Aborted: let the copies still in flight land before the CTA's
-            // shared memory is released.
-            const volatile int never = 0;
-            const uint32_t first = issued > uint32_t(ns) ? issued - ns : 0;
-            for (uint32_t t = first; t < issued; ++t)
-                dev::mbar_wait_bounded(bar0 + 8 * (t % ns), (t / ns) & 1, &never, a.timeout_ns);
-        }
+        if (lane == 0) issued = produce_tiles<C>(a, walk, stage0, bar0, ns, kv_slab, flags);
+        __syncwarp();
+        dev::named_barrier_sync(2, C::THREADS);  // every warp is done
+        if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);
+        __syncwarp();
         return;
     }
 
@@ -334,7 +352,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
     const int sub = lane % LPR;
     const int my_row = (sub >> SHIFT) * RPW + grp;            // row held after the reduction
     const bool owner = (sub & ((1 << SHIFT) - 1)) == 0;       // one lane per row counts it
-    float *pb = pbuf + cw * TILE * G;
+    float *pb = pbuf + cw * TILE * C::GP;
     const int H = a.H_kv * G;
 
     float qr[G][E], acc[G][E], m[G], l[G];
@@ -430,7 +448,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
                 m[h] = mn;
                 const float p = exp2f(sc - mn);
                 l[h] = fmaf(l[h], corr[h], owner ? p : 0.f);
-                if (owner) pb[my_row * G + h] = p;
+                if (owner) pb[my_row * C::GP + h] = p;
             }
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -445,7 +463,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
                     const int row = i * RPW + grp;
                     float pw[G], vf[E];
 #pragma unroll
-                    for (int h = 0; h < G; ++h) pw[h] = pb[row * G + h];
+                    for (int h = 0; h < G; ++h) pw[h] = pb[row * C::GP + h];
                     const uint8_t *rp = vs + row * C::ROW_BYTES;
 #pragma unroll
                     for (int c = 0; c < CPL; ++c)
@@ -462,7 +480,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
                     if (row < nr) {  // rows past the copied ones hold stale bytes
                         float pw[G], vf[E];
 #pragma unroll
-                        for (int h = 0; h < G; ++h) pw[h] = pb[row * G + h];
+                        for (int h = 0; h < G; ++h) pw[h] = pb[row * C::GP + h];
                         const uint8_t *rp = vs + row * C::ROW_BYTES;
 #pragma unroll
                         for (int c = 0; c < CPL; ++c)
@@ -570,6 +588,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
         }
         dev::named_barrier_sync(1, NW * 32);
     }
+    dev::named_barrier_sync(2, C::THREADS);
 }
 
 template <typename T, int D, int G>

@@ -66,7 +66,7 @@ def test_append_ragged_positions():
     w = synth.Workload("ragged_append", 2, 5, 8, 4, 64, 300, "bf16", steps=1, seed=77)
     hn = _gpu.Harness(w)
     lc = ListAppendCache(w.n_layers, w.batch, w.n_kv_heads, w.row_bytes)
-    lengths = [0, 3, 17, 250, 296]
+    lengths = [0, 3, 17, 250, 295]          # 295 + 1 + 4 = max_context
     for layer in range(w.n_layers):
         _gpu.fill_prefix(hn, layer, lengths)
         for b, n in enumerate(lengths):
