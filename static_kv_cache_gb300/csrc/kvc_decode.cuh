@@ -271,8 +271,8 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             dev::mbar_arrive_expect_tx(full, 2 * bytes);
-            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
-            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s_paged(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s_paged(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
             ++issued;
             if (++stage == ns) {
                 stage = 0;
