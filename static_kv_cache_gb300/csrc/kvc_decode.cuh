@@ -271,8 +271,8 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             dev::mbar_arrive_expect_tx(full, 2 * bytes);
-            dev::bulk_copy_g2s_paged(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
-            dev::bulk_copy_g2s_paged(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
             ++issued;
             if (++stage == ns) {
                 stage = 0;
@@ -390,8 +390,21 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
             }
             if (int(t % NW) != cw) continue;
             const int nr = min(TILE, pc.hi - row0);
+            // The previous use of this stage (tile t - ns) belongs to another
+            // warp and copies may land out of order, so when this warp gets
+            // here the full barrier may be in phase r-1 (t - ns still landing),
+            // r, or r+1 (t already landed): r-1 and r+1 share a parity.  So
+            // first wait until tile t - ns has been released (empty barrier,
+            // phase r-1).  That barrier can only be in phase r-1 or r: t - ns
+            // was issued before this warp's previous tile, and only this warp
+            // can release t.  Once t - ns is released its data had landed, so
+            // the full barrier is in phase r or r+1 and its parity wait is exact.
+            const uint32_t full_bar = bar0 + 8 * cur_stage;
+            const uint32_t empty_bar = bar0 + 8 * (ns + cur_stage);
             bool ok = !flags[0] &&
-                      dev::mbar_wait_bounded(bar0 + 8 * cur_stage, cur_round & 1, flags, a.timeout_ns);
+                      (cur_round == 0 ||
+                       dev::mbar_wait_bounded(empty_bar, (cur_round - 1) & 1, flags, a.timeout_ns)) &&
+                      dev::mbar_wait_bounded(full_bar, cur_round & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
             if (!ok) {
                 if (lane == 0) {

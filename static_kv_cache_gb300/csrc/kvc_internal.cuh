@@ -175,26 +175,6 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
-// The same copy issued as at most two bulk copies so that no single copy's
-// source range crosses a 2 MiB-aligned address (the large-page size).  Both
-// halves signal the same mbarrier, so the expected transaction count is still
-// `bytes`.  A tile is far smaller than 2 MiB, so one split is enough; the split
-// point is 2 MiB-aligned and src is 16-byte aligned, so both halves stay
-// multiples of 16 bytes.
-__device__ __forceinline__ void bulk_copy_g2s_paged(uint32_t dst, const uint8_t *src, uint32_t bytes,
-                                                    uint32_t bar) {
-    constexpr uint64_t kPage = 2ull << 20;
-    const uint64_t a = reinterpret_cast<uint64_t>(src);
-    const uint64_t next = (a | (kPage - 1)) + 1;
-    if (a + bytes <= next) {
-        bulk_copy_g2s(dst, src, bytes, bar);
-        return;
-    }
-    const uint32_t first = uint32_t(next - a);
-    bulk_copy_g2s(dst, src, first, bar);
-    bulk_copy_g2s(dst + first, src + first, bytes - first, bar);
-}
-
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
