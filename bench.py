@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("kvc", "reference"), default="kvc")
     p.add_argument("--workload", default="llama3_8b", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--layers", type=int, default=0,
+                   help="use only this many layers of the workload (profiling small cases)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="wall time budget of the CPU-oracle baseline sample")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
@@ -301,6 +303,8 @@ def bench_kvc(args, rank, world, local):
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
     state = DeviceState(w, local)
     lengths = state.lengths.numpy()
     per_layer = step_bytes(w, lengths)
