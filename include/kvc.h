@@ -192,6 +192,45 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q,
                            const int32_t *valid_len, int32_t max_valid_hint,
                            void *out, void *stream);
 
+/* ---- decode without any device allocation ------------------------------- */
+
+/* Size of the library's built-in scratch array used by kvc_decode_attn_static:
+ * 4 MiB of device memory, held on every GPU that loads the library until the
+ * process exits. */
+#define KVC_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/* The pages have no counterpart to this call; it exists for users of the
+ * library, not for the method.
+ *
+ * Same attention as kvc_decode_attn, for callers that cannot allocate device
+ * memory: code whose device memory is owned by someone else (a host framework
+ * that budgets every byte itself, a plugin interface that passes only the
+ * tensors of the call) can neither call cudaMalloc nor hand the library the
+ * workspace that kvc_alloc binds.  This call needs no handle and no
+ * workspace: it keeps the split partials and per-(sequence, KV head)
+ * counters in a fixed array compiled into the library
+ * (KVC_STATIC_SCRATCH_BYTES) and allocates nothing.
+ *   cfg             host; the cache shape, as for kvc_alloc
+ *   layer           0 <= layer < cfg->n_layers
+ *   k_base, v_base  device caches laid out as for kvc_alloc, 16-byte aligned
+ *   q, valid_len, max_valid_hint, out, stream   as for kvc_decode_attn
+ * Returns KVC_ERR_WORKSPACE when the configuration needs more scratch than
+ * the array holds (about (152 + B*H_kv) * (H/H_kv) * (d_head + 2) * 4 bytes
+ * on a 152-SM GPU); KVC_ERR_INVALID, _ALIGNMENT, _UNSUPPORTED, _CUDA as
+ * kvc_decode_attn.
+ * The first call on a device does a one-time set-up there (looks up the
+ * array's device address and the device limits); make that first call before
+ * any stream capture.  Every call shares the one array and clears its
+ * counters on the stream first, so calls that overlap on the GPU (streams
+ * without ordering between them) race; order them on one stream.  A sequence
+ * with valid_len[b] outside [1, max_context] is skipped (its output rows are
+ * left unwritten); this call has no handle, so that is not reported through
+ * kvc_get_error. */
+kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t layer,
+                                  const void *k_base, const void *v_base,
+                                  const void *q, const int32_t *valid_len,
+                                  int32_t max_valid_hint, void *out, void *stream);
+
 /* Synchronise the stream, then read and clear the device error word.
  * Returns KVC_OK if no kernel recorded an error since the last call,
  * otherwise the first recorded code (KVC_ERR_DEVICE_INDEX or

@@ -37,7 +37,7 @@ def nvcc() -> str:
 
 def _units():
     units = []
-    for src in ("kvc_api.cu", "kvc_append.cu"):
+    for src in ("kvc_api.cu", "kvc_append.cu", "kvc_noalloc.cu"):
         units.append((os.path.join(CSRC, src), os.path.join(BUILD, src.replace(".cu", ".o")), []))
     inst = os.path.join(CSRC, "kvc_decode_inst.cu")
     for tag, code in ELEM_TYPES.items():
