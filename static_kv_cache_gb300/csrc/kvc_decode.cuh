@@ -65,6 +65,13 @@ struct ElemOps<__nv_bfloat16> {
         f[6] = __uint_as_float(v.w << 16);
         f[7] = __uint_as_float(v.w & 0xffff0000u);
     }
+    // Widened pairs (element 2i, element 2i+1) for the packed fp32 FMA.
+    __device__ __forceinline__ static void unpack2(const uint4 &v, float2 *f) {
+        f[0] = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+        f[1] = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        f[2] = make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+        f[3] = make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+    }
     __device__ __forceinline__ static __nv_bfloat16 round(float x) { return __float2bfloat16_rn(x); }
 };
 
@@ -80,6 +87,11 @@ struct ElemOps<__half> {
             f[2 * i + 1] = t.y;
         }
     }
+    __device__ __forceinline__ static void unpack2(const uint4 &v, float2 *f) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = __half22float2(h[i]);
+    }
     __device__ __forceinline__ static __half round(float x) { return __float2half_rn(x); }
 };
 
@@ -91,6 +103,10 @@ struct ElemOps<float> {
         f[1] = __uint_as_float(v.y);
         f[2] = __uint_as_float(v.z);
         f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static void unpack2(const uint4 &v, float2 *f) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
     }
     __device__ __forceinline__ static float round(float x) { return x; }
 };
@@ -118,7 +134,9 @@ struct DecodeCfg {
     static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
     static constexpr int NW = 7;                        // consumer warps (+1 producer = 256 threads)
-    static constexpr int GP = (G + 3) & ~3;             // probabilities per row, padded to 16 bytes
+    static constexpr int E2 = E / 2;                    // element pairs of a row per lane
+    static constexpr int PC = EPC / 2;                  // pairs per 16-byte chunk
+    static constexpr int GP = 2 * ((G + 1) & ~1);       // per row: (p, p) for each head, 16-byte padded
     static constexpr int PBUF_FLOATS = NW * TILE * GP;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
@@ -355,7 +373,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
     float *pb = pbuf + cw * TILE * C::GP;
     const int H = a.H_kv * G;
 
-    float qr[G][E], acc[G][E], m[G], l[G];
+    constexpr int E2 = C::E2, PC = C::PC, GP = C::GP;
+    float2 qr[G][E2], acc[G][E2];
+    float m[G], l[G];
     uint32_t t = 0;
     int stage = 0;
     uint32_t round = 0;
@@ -369,12 +389,13 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) {
                     const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qb + h * D) + sub + c * LPR);
-                    Ops::unpack(raw, &qr[h][c * EPC]);
+                    Ops::unpack2(raw, &qr[h][c * PC]);
                 }
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    qr[h][e] *= a.scale_log2;
-                    acc[h][e] = 0.f;
+                for (int e = 0; e < E2; ++e) {
+                    qr[h][e].x *= a.scale_log2;
+                    qr[h][e].y *= a.scale_log2;
+                    acc[h][e] = make_float2(0.f, 0.f);
                 }
                 m[h] = -INFINITY;
                 l[h] = 0.f;
@@ -422,16 +443,17 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
             for (int j = 0; j < NPASS; ++j) {
                 const int row = (j ^ (sub >> SHIFT)) * RPW + grp;
                 const uint8_t *rp = ks + row * C::ROW_BYTES;
-                float kf[E];
+                float2 kf[E2];
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
-                    Ops::unpack(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16), &kf[c * EPC]);
+                    Ops::unpack2(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16), &kf[c * PC]);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float d = 0.f;
+                    // even and odd elements in the two halves of a packed FMA
+                    float2 d = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], kf[e], d);
-                    s[j][h] = d;
+                    for (int e = 0; e < E2; ++e) d = __ffma2_rn(qr[h][e], kf[e], d);
+                    s[j][h] = d.x + d.y;
                 }
             }
 #pragma unroll
@@ -461,12 +483,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
                 m[h] = mn;
                 const float p = exp2f(sc - mn);
                 l[h] = fmaf(l[h], corr[h], owner ? p : 0.f);
-                if (owner) pb[my_row * C::GP + h] = p;
+                if (owner) *reinterpret_cast<float2 *>(pb + my_row * GP + 2 * h) = make_float2(p, p);
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < G; ++h) {
+                const float2 c2 = make_float2(corr[h], corr[h]);
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[h][e] *= corr[h];
+                for (int e = 0; e < E2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], c2);
+            }
             __syncwarp();
 
             // ---- P.V: each lane accumulates its 8 dimensions over its rows
@@ -474,35 +498,36 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < NPASS; ++i) {
                     const int row = i * RPW + grp;
-                    float pw[G], vf[E];
+                    float2 pw[G], vf[E2];
 #pragma unroll
-                    for (int h = 0; h < G; ++h) pw[h] = pb[row * C::GP + h];
+                    for (int h = 0; h < G; ++h) pw[h] = *reinterpret_cast<const float2 *>(pb + row * GP + 2 * h);
                     const uint8_t *rp = vs + row * C::ROW_BYTES;
 #pragma unroll
                     for (int c = 0; c < CPL; ++c)
-                        Ops::unpack(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16), &vf[c * EPC]);
+                        Ops::unpack2(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16), &vf[c * PC]);
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
-                        for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pw[h], vf[e], acc[h][e]);
+                        for (int e = 0; e < E2; ++e) acc[h][e] = __ffma2_rn(pw[h], vf[e], acc[h][e]);
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < NPASS; ++i) {
                     const int row = i * RPW + grp;
                     if (row < nr) {  // rows past the copied ones hold stale bytes
-                        float pw[G], vf[E];
+                        float2 pw[G], vf[E2];
 #pragma unroll
-                        for (int h = 0; h < G; ++h) pw[h] = pb[row * C::GP + h];
+                        for (int h = 0; h < G; ++h)
+                            pw[h] = *reinterpret_cast<const float2 *>(pb + row * GP + 2 * h);
                         const uint8_t *rp = vs + row * C::ROW_BYTES;
 #pragma unroll
                         for (int c = 0; c < CPL; ++c)
-                            Ops::unpack(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16),
-                                        &vf[c * EPC]);
+                            Ops::unpack2(*reinterpret_cast<const uint4 *>(rp + (sub + c * LPR) * 16),
+                                         &vf[c * PC]);
 #pragma unroll
                         for (int h = 0; h < G; ++h)
 #pragma unroll
-                            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pw[h], vf[e], acc[h][e]);
+                            for (int e = 0; e < E2; ++e) acc[h][e] = __ffma2_rn(pw[h], vf[e], acc[h][e]);
                     }
                 }
             }
@@ -521,15 +546,19 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[h][e] += __shfl_xor_sync(FULL, acc[h][e], o);
+                for (int e = 0; e < E2; ++e) {
+                    acc[h][e].x += __shfl_xor_sync(FULL, acc[h][e].x, o);
+                    acc[h][e].y += __shfl_xor_sync(FULL, acc[h][e].y, o);
+                }
         if (grp == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
 #pragma unroll
-                    for (int i = 0; i < EPC; ++i)
-                        scr_acc[(cw * G + h) * D + (sub + c * LPR) * EPC + i] = acc[h][c * EPC + i];
+                    for (int i = 0; i < PC; ++i)
+                        *reinterpret_cast<float2 *>(scr_acc + (cw * G + h) * D + (sub + c * LPR) * EPC + 2 * i) =
+                            acc[h][c * PC + i];
         }
         if (lane == 0) {
 #pragma unroll

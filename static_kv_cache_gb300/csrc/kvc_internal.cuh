@@ -14,8 +14,9 @@ constexpr int32_t ERR_DEVICE_INDEX = 6;
 // Upper bound on the CTAs of one decode launch; sizes the split partials.
 constexpr int MAX_CTAS = 1024;
 
-// Dynamic shared memory a decode CTA may use (stages + scratch).
-constexpr int SMEM_BUDGET = 212 * 1024;
+// Dynamic shared memory a decode CTA may use (stages + scratch): the whole
+// opt-in limit of one block (227 KB on sm_100-class GPUs).
+constexpr int SMEM_BUDGET = 227 * 1024;
 
 // Default bound on any single wait inside a kernel.
 constexpr unsigned long long WAIT_TIMEOUT_NS = 1000ull * 1000ull * 1000ull;  // 1 s
