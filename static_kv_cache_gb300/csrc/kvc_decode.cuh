@@ -311,6 +311,81 @@ __device__ __forceinline__ void drain_copies(uint32_t bar0, int ns, uint32_t iss
         dev::mbar_wait_bounded(bar0 + 8 * (t % ns), (t / ns) & 1, &never, timeout_ns);
 }
 
+// End of a piece, after every consumer warp has written its softmax state
+// (max m, sum l, unnormalised accumulator) for the piece's G heads to
+// scr_ml [NW][G][2] and scr_acc [NW][G][D]: merge the warps' states, then
+// either normalise and write the output (the piece is a whole segment) or
+// store a split partial; the last CTA to finish a segment merges its
+// partials and writes the output.  Called by the NW consumer warps only.
+template <typename T, int D, int G, int NW>
+__device__ __forceinline__ void merge_piece(const DecodeArgs &a, const Plan &plan, const Piece &pc,
+                                            const float *scr_acc, const float *scr_ml,
+                                            volatile int *flags, int ctid) {
+    using Ops = ElemOps<T>;
+    const int H = a.H_kv * G;
+
+    const int seg = pc.b * a.H_kv + pc.kv;
+    const int c0 = int(pc.seg_start / plan.chunk);
+    const int c1 = int((pc.seg_start + pc.n - 1) / plan.chunk);
+    const bool whole = (c0 == c1);
+    T *ob = reinterpret_cast<T *>(a.out) + (int64_t(pc.b) * H + pc.kv * G) * D;
+    const bool aborted = flags[0] != 0;
+    if (!aborted) {
+        for (int idx = ctid; idx < G * D; idx += NW * 32) {
+            const int h = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, scr_ml[(w * G + h) * 2]);
+            float L = 0.f, A = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float e = exp2f(scr_ml[(w * G + h) * 2] - M);
+                L = fmaf(scr_ml[(w * G + h) * 2 + 1], e, L);
+                A = fmaf(scr_acc[(w * G + h) * D + d], e, A);
+            }
+            if (whole) {
+                ob[h * D + d] = Ops::round(A / L);
+            } else {
+                const int slot = int(blockIdx.x) + seg;
+                a.part_acc[(int64_t(slot) * G + h) * D + d] = A;
+                if (d == 0) {
+                    a.part_ml[(int64_t(slot) * G + h) * 2] = M;
+                    a.part_ml[(int64_t(slot) * G + h) * 2 + 1] = L;
+                }
+            }
+        }
+    }
+    if (!whole) {
+        __threadfence();
+        dev::named_barrier_sync(1, NW * 32);
+        if (ctid == 0) {
+            int last = 0;
+            if (!flags[0]) last = atomicAdd(a.tickets + seg, 1) == c1 - c0;
+            flags[1] = last;
+        }
+        dev::named_barrier_sync(1, NW * 32);
+        if (flags[1]) {
+            __threadfence();
+            for (int idx = ctid; idx < G * D; idx += NW * 32) {
+                const int h = idx / D, d = idx % D;
+                float M = -INFINITY;
+                for (int c = c0; c <= c1; ++c)
+                    M = fmaxf(M, __ldcg(a.part_ml + (int64_t(c + seg) * G + h) * 2));
+                float L = 0.f, A = 0.f;
+                for (int c = c0; c <= c1; ++c) {
+                    const int64_t sl = int64_t(c + seg) * G + h;
+                    const float e = exp2f(__ldcg(a.part_ml + sl * 2) - M);
+                    L = fmaf(__ldcg(a.part_ml + sl * 2 + 1), e, L);
+                    A = fmaf(__ldcg(a.part_acc + sl * D + d), e, A);
+                }
+                ob[h * D + d] = Ops::round(A / L);
+            }
+            if (ctid == 0) a.tickets[seg] = 0;
+        }
+    }
+    dev::named_barrier_sync(1, NW * 32);
+}
+
 // --------------------------------------------------------------------------
 // The kernel.
 // --------------------------------------------------------------------------
@@ -568,67 +643,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
             }
         }
         dev::named_barrier_sync(1, NW * 32);
-
-        const int seg = pc.b * a.H_kv + pc.kv;
-        const int c0 = int(pc.seg_start / plan.chunk);
-        const int c1 = int((pc.seg_start + pc.n - 1) / plan.chunk);
-        const bool whole = (c0 == c1);
-        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(pc.b) * H + pc.kv * G) * D;
-        const bool aborted = flags[0] != 0;
-        if (!aborted) {
-            for (int idx = ctid; idx < G * D; idx += NW * 32) {
-                const int h = idx / D, d = idx % D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < NW; ++w) M = fmaxf(M, scr_ml[(w * G + h) * 2]);
-                float L = 0.f, A = 0.f;
-#pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const float e = exp2f(scr_ml[(w * G + h) * 2] - M);
-                    L = fmaf(scr_ml[(w * G + h) * 2 + 1], e, L);
-                    A = fmaf(scr_acc[(w * G + h) * D + d], e, A);
-                }
-                if (whole) {
-                    ob[h * D + d] = Ops::round(A / L);
-                } else {
-                    const int slot = int(blockIdx.x) + seg;
-                    a.part_acc[(int64_t(slot) * G + h) * D + d] = A;
-                    if (d == 0) {
-                        a.part_ml[(int64_t(slot) * G + h) * 2] = M;
-                        a.part_ml[(int64_t(slot) * G + h) * 2 + 1] = L;
-                    }
-                }
-            }
-        }
-        if (!whole) {
-            __threadfence();
-            dev::named_barrier_sync(1, NW * 32);
-            if (ctid == 0) {
-                int last = 0;
-                if (!flags[0]) last = atomicAdd(a.tickets + seg, 1) == c1 - c0;
-                flags[1] = last;
-            }
-            dev::named_barrier_sync(1, NW * 32);
-            if (flags[1]) {
-                __threadfence();
-                for (int idx = ctid; idx < G * D; idx += NW * 32) {
-                    const int h = idx / D, d = idx % D;
-                    float M = -INFINITY;
-                    for (int c = c0; c <= c1; ++c)
-                        M = fmaxf(M, __ldcg(a.part_ml + (int64_t(c + seg) * G + h) * 2));
-                    float L = 0.f, A = 0.f;
-                    for (int c = c0; c <= c1; ++c) {
-                        const int64_t sl = int64_t(c + seg) * G + h;
-                        const float e = exp2f(__ldcg(a.part_ml + sl * 2) - M);
-                        L = fmaf(__ldcg(a.part_ml + sl * 2 + 1), e, L);
-                        A = fmaf(__ldcg(a.part_acc + sl * D + d), e, A);
-                    }
-                    ob[h * D + d] = Ops::round(A / L);
-                }
-                if (ctid == 0) a.tickets[seg] = 0;
-            }
-        }
-        dev::named_barrier_sync(1, NW * 32);
+        merge_piece<T, D, G, NW>(a, plan, pc, scr_acc, scr_ml, flags, ctid);
     }
     dev::named_barrier_sync(2, C::THREADS);
 }

@@ -1,7 +1,7 @@
 // kvc_decode_inst.cu -- explicit decode kernels for one (element type, head
 // width), selected at compile time by KVC_INST_TYPE (0 bf16, 1 fp16, 2 fp32)
 // and KVC_INST_D.  The build compiles this file once per pair, in parallel.
-#include "kvc_decode.cuh"
+#include "kvc_decode_mma.cuh"
 
 #ifndef KVC_INST_TYPE
 #error "KVC_INST_TYPE must be defined"
@@ -27,16 +27,25 @@
 
 namespace kvc {
 
+// 16-bit caches with 2 to 8 query heads per KV head and d_h up to 128 run the
+// tensor-core kernel; one query head per KV head, fp32 caches and d_h = 256
+// run the CUDA-core kernel.
+#if KVC_INST_TYPE != 2 && KVC_INST_D <= 128
+#define KVC_GROUPED(G) mma_decode_info<KVC_ELEM, KVC_INST_D, G>()
+#else
+#define KVC_GROUPED(G) decode_info<KVC_ELEM, KVC_INST_D, G>()
+#endif
+
 const DecodeKernelInfo *KVC_TABLE_FN(int G) {
     switch (G) {
         case 1: return decode_info<KVC_ELEM, KVC_INST_D, 1>();
-        case 2: return decode_info<KVC_ELEM, KVC_INST_D, 2>();
-        case 3: return decode_info<KVC_ELEM, KVC_INST_D, 3>();
-        case 4: return decode_info<KVC_ELEM, KVC_INST_D, 4>();
-        case 5: return decode_info<KVC_ELEM, KVC_INST_D, 5>();
-        case 6: return decode_info<KVC_ELEM, KVC_INST_D, 6>();
-        case 7: return decode_info<KVC_ELEM, KVC_INST_D, 7>();
-        case 8: return decode_info<KVC_ELEM, KVC_INST_D, 8>();
+        case 2: return KVC_GROUPED(2);
+        case 3: return KVC_GROUPED(3);
+        case 4: return KVC_GROUPED(4);
+        case 5: return KVC_GROUPED(5);
+        case 6: return KVC_GROUPED(6);
+        case 7: return KVC_GROUPED(7);
+        case 8: return KVC_GROUPED(8);
         default: return nullptr;
     }
 }
