@@ -3,7 +3,10 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/kvc.h"
 #include "kvc_internal.cuh"
@@ -24,6 +27,7 @@ struct kvc_cache {
     const kvc::DecodeKernelInfo *decode;
     int n_stages;
     int smem_bytes;
+    CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
 };
 
 namespace {
@@ -68,7 +72,43 @@ uint64_t layer_slab_bytes(const kvc_cache *h) {
     return uint64_t(c.batch) * c.n_kv_heads * uint64_t(c.max_context) * c.d_head * h->elem_bytes;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 }  // namespace
+
+bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
+                            const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
+                            CUtensorMap *v8) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return false;
+    const CUtensorMapDataType dt =
+        dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(max_ctx) * D * 2};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
+    const Job jobs[4] = {{k_base, 32, k32}, {k_base, 8, k8}, {v_base, 32, v32}, {v_base, 8, v8}};
+    for (const Job &j : jobs) {
+        const cuuint32_t box[3] = {64, j.rows, 1};
+        if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
 
 extern "C" {
 
@@ -159,6 +199,13 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
     h->decode = info;
     h->n_stages = n_stages;
     h->smem_bytes = smem_bytes;
+    if (info->tensor_maps &&
+        !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
+                                int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
+                                &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
+        delete h;
+        return KVC_ERR_CUDA;
+    }
     *out = h;
     return KVC_OK;
 }
@@ -226,6 +273,13 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int
     a.n_stages = h->n_stages;
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    a.seg_base = layer * c.batch * c.n_kv_heads;
+    if (h->decode->tensor_maps) {
+        a.tm_k32 = h->tm_k32;
+        a.tm_k8 = h->tm_k8;
+        a.tm_v32 = h->tm_v32;
+        a.tm_v8 = h->tm_v8;
+    }
     const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

@@ -663,8 +663,8 @@ cudaError_t launch_decode(const DecodeArgs &a, int grid, int smem, cudaStream_t 
 template <typename T, int D, int G>
 const DecodeKernelInfo *decode_info() {
     using C = DecodeCfg<T, D, G>;
-    static const DecodeKernelInfo info = {C::TILE,        C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
-                                          &set_decode_max_smem<T, D, G>, &launch_decode<T, D, G>};
+    static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
+                                          &set_decode_max_smem<T, D, G>, &launch_decode<T, D, G>, false};
     return &info;
 }
 

@@ -27,10 +27,10 @@
 
 namespace kvc {
 
-// 16-bit caches with 2 to 8 query heads per KV head and d_h up to 128 run the
-// tensor-core kernel; one query head per KV head, fp32 caches and d_h = 256
-// run the CUDA-core kernel.
-#if KVC_INST_TYPE != 2 && KVC_INST_D <= 128
+// 16-bit caches with 2 to 8 query heads per KV head and d_h of 64 or 128 run
+// the tensor-core kernel; one query head per KV head, fp32 caches and the
+// other head widths run the CUDA-core kernel.
+#if KVC_INST_TYPE != 2 && (KVC_INST_D == 64 || KVC_INST_D == 128)
 #define KVC_GROUPED(G) mma_decode_info<KVC_ELEM, KVC_INST_D, G>()
 #else
 #define KVC_GROUPED(G) decode_info<KVC_ELEM, KVC_INST_D, G>()

@@ -24,12 +24,15 @@
 //   O[16 x D] += P . V : the S accumulator layout is the A-operand layout, so
 //     P is rounded to the cache's 16-bit type in place; B = V via ldmatrix
 //     .trans; 2 k-steps x D/8 n-tiles.
-// K and V rows are copied one row per lane by the producer warp into a
-// shared-memory tile whose row pitch is the row size + 16 bytes: consecutive
-// rows then start in different 16-byte bank groups, so every ldmatrix is
-// conflict-free.  Rows past the copied ones in a tail tile hold stale bytes:
-// their scores are replaced by -inf and their V fragments are zeroed in
-// registers.
+// K and V tiles reach shared memory through TMA tensor copies with the
+// 128-byte swizzle (16-byte chunk c of row r of each 64-column block stored at
+// chunk c ^ (r mod 8)), which makes every ldmatrix conflict-free.  A box only
+// ever covers 8-row groups inside the live range (32 rows for a full tile, 8
+// for the groups of a tail tile); the last (rows mod 8) rows of a tail tile
+// are loaded by the producer warp's other lanes with plain 16-byte loads and
+// stored at their swizzled positions, so rows past valid_len are never read.
+// Rows past the copied ones in a tail tile hold stale bytes: their scores are
+// replaced by -inf and their V fragments are zeroed in registers.
 #pragma once
 
 #include "kvc_decode.cuh"
@@ -66,40 +69,50 @@ struct MmaOps<__half> {
 template <typename T, int D, int G>
 struct MmaCfg {
     static constexpr int ROW_BYTES = D * 2;
-    static constexpr int PITCH = ROW_BYTES + 16;        // shared-memory row pitch
     static constexpr int TILE = 32;                     // keys per tile
-    static constexpr int TILE_BYTES = TILE * PITCH;
+    static constexpr int BLOCK_BYTES = TILE * 128;      // one 64-column block of a tile
+    static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
+    static constexpr int CHUNKS = ROW_BYTES / 16;       // 16-byte chunks of a row
     static constexpr int KSTEPS = D / 16;               // k-steps of the score product
     static constexpr int NTD = D / 8;                   // n-tiles of the P.V product
     static constexpr int NW = 7;                        // consumer warps (+1 producer)
     static constexpr int THREADS = (NW + 1) * 32;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
-    static constexpr int FIXED_SMEM = 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
+    // 1 KB of slack to align the stages to the 1024-byte swizzle atom
+    static constexpr int FIXED_SMEM = 1024 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
 
     static_assert(sizeof(T) == 2, "the tensor-core path takes 16-bit caches");
     static_assert(G >= 1 && G <= 8, "the query group must fit the 8 live rows of an m16 tile");
-    static_assert(D % 16 == 0 && D >= 32, "head width must be a multiple of 16");
-    static_assert(STAGE_BYTES % 128 == 0, "stages must keep 128-byte alignment");
+    static_assert(D % 64 == 0, "head width must be a multiple of 64 (128-byte swizzle blocks)");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the swizzle-atom alignment");
+
+    // Shared-memory address of (row r, element col) in a swizzled tile; col
+    // is a multiple of 8 (one 16-byte chunk).
+    __device__ __forceinline__ static uint32_t swz(uint32_t tile, int r, int col) {
+        return tile + uint32_t(col >> 6) * BLOCK_BYTES + uint32_t(r) * 128 +
+               uint32_t((((col >> 3) & 7) ^ (r & 7)) << 4);
+    }
 };
 
-// The producer warp: walks the CTA's pieces and copies each K and V row of a
-// tile with its own 1-D bulk copy (one row per lane) into the padded tile.
+// The producer warp: walks the CTA's pieces; for each tile one lane issues
+// the TMA boxes and the other lanes load the tail rows no box may cover.
 template <typename C>
-__device__ __forceinline__ uint32_t produce_rows(const DecodeArgs &a, Walker walk, uint32_t stage0,
-                                                 uint32_t bar0, int ns, int64_t kv_slab,
-                                                 volatile int *flags, int lane) {
-    constexpr int TILE = C::TILE;
+__device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walker walk, uint32_t stage0,
+                                                      uint32_t bar0, int ns, int64_t kv_slab,
+                                                      volatile int *flags, int lane) {
+    constexpr int TILE = C::TILE, CB = C::ROW_BYTES / 128;
     uint32_t issued = 0;
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
     Piece pc;
     while (ok && walk.next(a, pc)) {
-        const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
-        const uint8_t *kseg = a.K + seg * kv_slab;
-        const uint8_t *vseg = a.V + seg * kv_slab;
+        const int seg = pc.b * a.H_kv + pc.kv;
+        const int z = a.seg_base + seg;  // tensor-map segment coordinate
+        const uint8_t *kseg = a.K + int64_t(seg) * kv_slab;
+        const uint8_t *vseg = a.V + int64_t(seg) * kv_slab;
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE) {
             const int nr = min(TILE, pc.hi - row0);
             if (round > 0) {
@@ -115,15 +128,41 @@ __device__ __forceinline__ uint32_t produce_rows(const DecodeArgs &a, Walker wal
                 }
             }
             const uint32_t full = bar0 + 8 * stage;
-            const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
-            if (lane == 0) dev::mbar_arrive_expect_tx(full, 2u * uint32_t(nr) * C::ROW_BYTES);
-            __syncwarp();
-            if (lane < nr) {
-                const int64_t src = int64_t(row0 + lane) * C::ROW_BYTES;
-                dev::bulk_copy_g2s(dst + uint32_t(lane) * C::PITCH, kseg + src, C::ROW_BYTES, full);
-                dev::bulk_copy_g2s(dst + C::TILE_BYTES + uint32_t(lane) * C::PITCH, vseg + src,
-                                   C::ROW_BYTES, full);
+            const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
+            const uint32_t vdst = kdst + C::TILE_BYTES;
+            const int q = nr >> 3, rem = nr & 7;  // 8-row groups, rows after them
+            if (lane == 0) {
+                dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
+                if (q == 4) {
+#pragma unroll
+                    for (int cb = 0; cb < CB; ++cb) {
+                        dev::tma_load_3d(kdst + cb * C::BLOCK_BYTES, &a.tm_k32, cb * 64, row0, z, full);
+                        dev::tma_load_3d(vdst + cb * C::BLOCK_BYTES, &a.tm_v32, cb * 64, row0, z, full);
+                    }
+                } else {
+                    for (int j = 0; j < q; ++j)
+#pragma unroll
+                        for (int cb = 0; cb < CB; ++cb) {
+                            const uint32_t off = cb * C::BLOCK_BYTES + j * 8 * 128;
+                            dev::tma_load_3d(kdst + off, &a.tm_k8, cb * 64, row0 + 8 * j, z, full);
+                            dev::tma_load_3d(vdst + off, &a.tm_v8, cb * 64, row0 + 8 * j, z, full);
+                        }
+                }
             }
+            if (rem) {
+                const int per = rem * C::CHUNKS;  // 16-byte chunks per tensor
+                for (int i = lane; i < 2 * per; i += 32) {
+                    const bool is_v = i >= per;
+                    const int j = is_v ? i - per : i;
+                    const int r = 8 * q + j / C::CHUNKS, c16 = j % C::CHUNKS;
+                    const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    dev::st_shared_v4(C::swz(is_v ? vdst : kdst, r, c16 * 8), v);
+                }
+                dev::fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(full);
             ++issued;
             if (++stage == ns) {
                 stage = 0;
@@ -144,10 +183,11 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
     using C = MmaCfg<T, D, G>;
     using Ops = MmaOps<T>;
-    constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS, NTD = C::NTD, PITCH = C::PITCH;
+    constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS, NTD = C::NTD;
     constexpr unsigned FULL = 0xffffffffu;
 
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
     const int ns = a.n_stages;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -177,7 +217,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
-        const uint32_t issued = produce_rows<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
+        const uint32_t issued = produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
         dev::named_barrier_sync(2, C::THREADS);  // every warp is done
         if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);
@@ -256,7 +296,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t r[4];
-                    dev::ldsm_x4(ks_base + uint32_t(half * 16 + k_key) * PITCH + (ks * 16 + k_col) * 2, r);
+                    dev::ldsm_x4(C::swz(ks_base, half * 16 + k_key, ks * 16 + k_col), r);
                     Ops::mma(sacc[2 * half], afr, r[0], r[1]);
                     Ops::mma(sacc[2 * half + 1], afr, r[2], r[3]);
                 }
@@ -303,7 +343,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int dn = 0; dn < NTD / 2; ++dn) {
                     uint32_t r[4];
-                    dev::ldsm_x4_trans(vs_base + uint32_t(kst * 16 + v_key) * PITCH + (dn * 16 + v_col) * 2, r);
+                    dev::ldsm_x4_trans(C::swz(vs_base, kst * 16 + v_key, dn * 16 + v_col), r);
                     if (nr < TILE) {  // stale rows past the copied ones
                         const int k0 = kst * 16 + 2 * tq;
                         r[0] = live_pair(r[0], k0, nr);
@@ -353,8 +393,8 @@ cudaError_t launch_mma(const DecodeArgs &a, int grid, int smem, cudaStream_t s) 
 template <typename T, int D, int G>
 const DecodeKernelInfo *mma_decode_info() {
     using C = MmaCfg<T, D, G>;
-    static const DecodeKernelInfo info = {C::TILE,        C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
-                                          &set_mma_max_smem<T, D, G>, &launch_mma<T, D, G>};
+    static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
+                                          &set_mma_max_smem<T, D, G>, &launch_mma<T, D, G>, true};
     return &info;
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace kvc {
@@ -64,6 +65,11 @@ struct DecodeArgs {
     int32_t n_stages;
     float scale_log2;          // log2(e) / sqrt(D)
     unsigned long long timeout_ns;
+    // Tensor maps of the whole K and V caches viewed as [L*B*H_kv][T_max][D]
+    // (16-bit caches, tensor-core kernel only): boxes of 64 columns x 32 or
+    // x 8 rows with the 128-byte swizzle.  seg_base = layer * B * H_kv.
+    int32_t seg_base;
+    alignas(64) CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;
 };
 
 // One compiled decode kernel and what the host needs to launch it.
@@ -74,6 +80,7 @@ struct DecodeKernelInfo {
     int fixed_smem;      // dynamic shared memory besides the stages
     cudaError_t (*set_max_smem)(int bytes);
     cudaError_t (*launch)(const DecodeArgs &a, int grid, int smem, cudaStream_t s);
+    bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -93,6 +100,13 @@ KVC_DECLARE_DECODE_TABLE(f32, 64)
 KVC_DECLARE_DECODE_TABLE(f32, 128)
 KVC_DECLARE_DECODE_TABLE(f32, 256)
 #undef KVC_DECLARE_DECODE_TABLE
+
+// Tensor maps of a K and a V cache [n_segs][max_ctx][D] of 16-bit elements
+// (n_segs = L * B * H_kv): boxes of 64 columns x 32 rows and x 8 rows with the
+// 128-byte swizzle.  Host only; returns false if the driver refuses.
+bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
+                       const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
+                       CUtensorMap *v8);
 
 // Append launcher (kvc_append.cu).
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
@@ -212,6 +226,32 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// One box of a 3-D tensor map (coordinates innermost first) into shared
+// memory through the TMA unit, completion signalled on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {

@@ -171,6 +171,15 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     const uint64_t total = round256(off_acc + slots * G * uint64_t(cfg->d_head) * 4);
     if (total > KVC_STATIC_SCRATCH_BYTES) return KVC_ERR_WORKSPACE;
 
+    // Tensor maps of the caches for kernels that read through them (host
+    // computation only).
+    CUtensorMap maps[4];
+    if (info->tensor_maps &&
+        !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
+                                int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
+                                &maps[0], &maps[1], &maps[2], &maps[3]))
+        return KVC_ERR_CUDA;
+
     // The array keeps the previous call's contents: the error word and the
     // counters must start at zero.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -194,6 +203,13 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     a.n_stages = n_stages;
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    a.seg_base = layer * cfg->batch * cfg->n_kv_heads;
+    if (info->tensor_maps) {
+        a.tm_k32 = maps[0];
+        a.tm_k8 = maps[1];
+        a.tm_v32 = maps[2];
+        a.tm_v8 = maps[3];
+    }
     const cudaError_t e = info->launch(a, int(grid), smem_bytes, s);
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
