@@ -38,8 +38,18 @@ METRIC = "decode-attention HBM GB/s and % of GB300 peak; decode tokens/s per lay
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_decode_mma.cuh",
                   "static_kv_cache_gb300/csrc/kvc_internal.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_inst.cu")
+
+
+def decode_kernel_name(w: synth.Workload) -> str:
+    """The decode kernel the library picks for a workload: the tensor-core
+    kernel for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128,
+    the CUDA-core kernel otherwise."""
+    if w.dtype in ("bf16", "fp16") and 2 <= w.group <= 8 and w.d_head in (64, 128):
+        return "decode_mma_kernel"
+    return "decode_split_kernel"
 
 
 # --------------------------------------------------------------------------- helpers
@@ -393,7 +403,7 @@ def bench_kvc(args, rank, world, local):
             "decode_attn_pct_of_peak": round(100 * achieved / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "decode_split_kernel", "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         "kernel": decode_kernel_name(w), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
                          "bytes_per_launch": per_layer["attn"],
                          "mean_launch_us": round(mean_decode_s * 1e6, 3)},

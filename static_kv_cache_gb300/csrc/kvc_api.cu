@@ -266,6 +266,7 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int
     a.part_ml = reinterpret_cast<float *>(h->ws + h->wl.part_ml);
     a.part_acc = reinterpret_cast<float *>(h->ws + h->wl.part_acc);
     a.tickets = reinterpret_cast<int32_t *>(h->ws + h->wl.tickets);
+    a.ready = reinterpret_cast<int32_t *>(h->ws + h->wl.ready);
     a.err = reinterpret_cast<int32_t *>(h->ws);
     a.B = c.batch;
     a.H_kv = c.n_kv_heads;
@@ -294,7 +295,8 @@ kvc_status kvc_get_error(kvc_cache *h, void *stream) {
     if (word != 0) {
         if (cudaMemset(h->ws, 0, sizeof word) != cudaSuccess) return KVC_ERR_CUDA;
         if (word == KVC_ERR_TIMEOUT) {
-            const uint64_t n = uint64_t(h->cfg.batch) * h->cfg.n_kv_heads * 4;
+            // an aborted launch can leave counters and publish flags set
+            const uint64_t n = h->wl.part_ml - h->wl.tickets;
             if (cudaMemset(h->ws + h->wl.tickets, 0, n) != cudaSuccess) return KVC_ERR_CUDA;
         }
         if (cudaDeviceSynchronize() != cudaSuccess) return KVC_ERR_CUDA;

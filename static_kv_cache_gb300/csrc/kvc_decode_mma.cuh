@@ -2,28 +2,30 @@
 // contractions on the warp tensor-core path, for 16-bit caches and head
 // groups of 2 to 8.
 //
-// Same mathematics, decomposition, pipeline protocol and merge as
+// Same mathematics, decomposition and pipeline protocol as
 // decode_split_kernel ("10.3 -- KV cache implementation details", section 5,
-// attention bullet; GQA per section 4.2): only the per-tile arithmetic of a
-// consumer warp changes.  With g query heads sharing a KV head, the tile of
-// scores is a g x TILE product and P.V a g x d_h one.  On CUDA cores every
-// cached element costs a widening instruction plus g/2 packed FMAs per
-// contraction, which at g >= 2 keeps the SM busy issuing arithmetic rather
-// than streaming; the mma.sync m16n8k16 tile (M = the g query rows, padded to
-// 16) does the same work in a few instructions per 16 keys, with fp32
-// accumulation exactly as before.
+// attention bullet; GQA per section 4.2).  With g query heads sharing a KV
+// head, the tile of scores is a g x TILE product and P.V a g x d_h one.  On
+// CUDA cores every cached element costs a widening instruction plus g/2
+// packed FMAs per contraction, which at g >= 2 keeps the SM busy issuing
+// arithmetic rather than streaming; the mma.sync m16n8k16 tile does the same
+// work in a few instructions per 16 keys, with fp32 accumulation.
 //
-// Per 32-key tile a consumer warp (lane = 4 * gr + tq):
-//   S[16 x 32] = Q[16 x D] . K^T : A = Q fragments (rows gr < g, loaded once
-//     per piece), B = K rows via ldmatrix (K is row-major [key][d], which is
-//     the column-major B operand), 4 n-tiles x D/16 k-steps.
-//   softmax on the accumulator fragments: lane (gr, tq) holds scores of head
-//     gr for keys 8n + 2tq + {0, 1}; a head's row lives in 4 lanes, so the
-//     tile maximum takes two shuffles; scores are scaled by log2(e)/sqrt(D)
-//     in fp32 after the product.
-//   O[16 x D] += P . V : the S accumulator layout is the A-operand layout, so
-//     P is rounded to the cache's 16-bit type in place; B = V via ldmatrix
-//     .trans; 2 k-steps x D/8 n-tiles.
+// Both products are taken transposed, so that the cached rows fill the M = 16
+// side of the tile and the g query heads the N = 8 side (g <= 8, no padding to
+// 16).  Per 32-key tile a consumer warp (lane = 4 * gq + tq):
+//   S^T[32 x 8] = K[32 x D] . Q^T : A = K rows via ldmatrix (row-major
+//     [key][d]), B = Q^T fragments (head gq, loaded once per piece); 2 m-tiles
+//     x D/16 k-steps.  Lane (gq, tq) holds the scores of heads 2tq, 2tq+1 for
+//     keys 16 mt + gq and 16 mt + gq + 8.
+//   softmax per head over the keys: a head's column lives in the 8 lanes of
+//     one tq, so the tile maximum takes three shuffles; the running sum stays
+//     per lane until the end of the piece.  Scores are scaled by
+//     log2(e)/sqrt(D) in fp32 after the product.
+//   O^T[D x 8] += V^T . P^T : A = V^T via ldmatrix .trans on the same [key][d]
+//     rows, B = P^T.  The S^T accumulator holds P^T with the keys along the
+//     rows; one movmatrix.trans per 8x8 block turns it into the B-operand
+//     layout (keys along the columns).  D/16 m-tiles x 2 k-steps.
 // K and V tiles reach shared memory through TMA tensor copies with the
 // 128-byte swizzle (16-byte chunk c of row r of each 64-column block stored at
 // chunk c ^ (r mod 8)), which makes every ldmatrix conflict-free.  A box only
@@ -33,6 +35,12 @@
 // stored at their swizzled positions, so rows past valid_len are never read.
 // Rows past the copied ones in a tail tile hold stale bytes: their scores are
 // replaced by -inf and their V fragments are zeroed in registers.
+//
+// Merging is taken off the consumers: at the end of a piece each consumer
+// warp leaves its softmax state in shared memory and goes on with the next
+// piece; a merge warp combines the NW states, then writes the output or the
+// split partial (and, for the last CTA of a segment, combines the partials)
+// while the consumers keep the stage ring draining.
 #pragma once
 
 #include "kvc_decode.cuh"
@@ -74,17 +82,17 @@ struct MmaCfg {
     static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
     static constexpr int CHUNKS = ROW_BYTES / 16;       // 16-byte chunks of a row
-    static constexpr int KSTEPS = D / 16;               // k-steps of the score product
-    static constexpr int NTD = D / 8;                   // n-tiles of the P.V product
-    static constexpr int NW = 7;                        // consumer warps (+1 producer)
-    static constexpr int THREADS = (NW + 1) * 32;
+    static constexpr int KSTEPS = D / 16;               // k-steps of S^T, m-tiles of O^T
+    static constexpr int NW = 8;                        // consumer warps (+ producer + merger)
+    static constexpr int THREADS = (NW + 2) * 32;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
-    // 1 KB of slack to align the stages to the 1024-byte swizzle atom
-    static constexpr int FIXED_SMEM = 1024 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
+    // 1 KB of slack to align the stages to the 1024-byte swizzle atom, the two
+    // merge barriers, the consumers' states, the abort flag
+    static constexpr int FIXED_SMEM = 1024 + 16 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
 
     static_assert(sizeof(T) == 2, "the tensor-core path takes 16-bit caches");
-    static_assert(G >= 1 && G <= 8, "the query group must fit the 8 live rows of an m16 tile");
+    static_assert(G >= 1 && G <= 8, "the query group must fit the N = 8 side of the tile");
     static_assert(D % 64 == 0, "head width must be a multiple of 64 (128-byte swizzle blocks)");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the swizzle-atom alignment");
 
@@ -178,12 +186,176 @@ __device__ __forceinline__ uint32_t live_pair(uint32_t r, int k, int nr) {
     return r & ((k < nr ? 0x0000ffffu : 0u) | (k + 1 < nr ? 0xffff0000u : 0u));
 }
 
+// Byte offset, inside a swizzled tile, of the 16-byte chunk that lane-row
+// `row` (row mod 8 == lane mod 8) reads at column 16 * step + 8 * half, for
+// step mod 4 == j: the chunk index (2 j + half) is XOR-ed with (row mod 8).
+__device__ __forceinline__ uint32_t swz_lane_offset(int row, int half, int lane, int j) {
+    return uint32_t(row) * 128 + ((uint32_t(2 * j) ^ uint32_t(half ^ (lane & 7))) << 4);
+}
+
+// The merge warp: for each piece of the CTA, wait for the NW consumer states,
+// combine them (lane l owns columns [l * D/32, (l + 1) * D/32) of every head)
+// and free the states.  A piece that is a whole segment writes its output.
+// A split takes a ticket on the segment's counter first: every split but the
+// last publishes its partial (data, fence, then its ready flag); the last one
+// waits for the others' flags -- their CTAs are past their tickets, so the
+// wait is short and needs no co-residency -- and folds their partials into
+// its own state, still in registers, then writes the output and resets the
+// counter and the flags for the next launch.
+template <typename T, int D, int G, int NW>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs &a, const Plan &plan, Walker walk,
+                                             const float *scr_acc, const float *scr_ml, uint32_t scr_full,
+                                             uint32_t scr_free, volatile int *flags, int lane) {
+    using Ops = ElemOps<T>;
+    constexpr int DPL = D / 32;
+    constexpr unsigned FULL = 0xffffffffu;
+    static_assert(DPL == 2 || DPL == 4, "merge lanes own 2 or 4 columns");
+    const int H = a.H_kv * G;
+    uint32_t piece = 0;
+    Piece pc;
+    while (walk.next(a, pc)) {
+        bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
+        ok = __all_sync(FULL, ok);
+        if (!ok) {
+            if (lane == 0) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            return;
+        }
+        float acc[G][DPL], Ms[G], Ls[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, scr_ml[(w * G + h) * 2]);
+            float L = 0.f;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float e = exp2f(scr_ml[(w * G + h) * 2] - M);
+                L = fmaf(scr_ml[(w * G + h) * 2 + 1], e, L);
+                const float *src = scr_acc + (w * G + h) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    acc[h][0] = fmaf(v.x, e, acc[h][0]);
+                    acc[h][1] = fmaf(v.y, e, acc[h][1]);
+                    acc[h][2] = fmaf(v.z, e, acc[h][2]);
+                    acc[h][3] = fmaf(v.w, e, acc[h][3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    acc[h][0] = fmaf(v.x, e, acc[h][0]);
+                    acc[h][1] = fmaf(v.y, e, acc[h][1]);
+                }
+            }
+            Ms[h] = M;
+            Ls[h] = L;
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(scr_free);
+        ++piece;
+
+        const int seg = pc.b * a.H_kv + pc.kv;
+        const int c0 = int(pc.seg_start / plan.chunk);
+        const int c1 = int((pc.seg_start + pc.n - 1) / plan.chunk);
+        const int me = int(blockIdx.x);
+        if (c0 != c1) {
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(a.tickets + seg, 1);
+            ticket = __shfl_sync(FULL, ticket, 0);
+            if (ticket < c1 - c0) {
+                // not the last split: publish the partial
+                const int64_t sl = int64_t(me + seg) * G;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float *dst = a.part_acc + (sl + h) * D + lane * DPL;
+                    if constexpr (DPL == 4)
+                        *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+                    else
+                        *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
+                }
+                if (lane < G) {
+                    float mv = Ms[0], lv = Ls[0];
+#pragma unroll
+                    for (int h = 1; h < G; ++h)
+                        if (lane == h) {
+                            mv = Ms[h];
+                            lv = Ls[h];
+                        }
+                    *reinterpret_cast<float2 *>(a.part_ml + (sl + lane) * 2) = make_float2(mv, lv);
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) dev::flag_store(a.ready + me + seg, 1);
+                continue;
+            }
+            // the last split: wait for the others' partials
+            bool pub = true;
+            for (int c = c0 + lane; c <= c1; c += 32)
+                if (c != me) pub = pub && dev::flag_wait_bounded(a.ready + c + seg, flags, a.timeout_ns);
+            pub = __all_sync(FULL, pub);
+            if (!pub) {
+                if (lane == 0) {
+                    if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                    flags[0] = 1;
+                }
+                return;
+            }
+            __threadfence();
+#pragma unroll 2
+            for (int c = c0; c <= c1; ++c) {
+                if (c == me) continue;
+                const int64_t sl = int64_t(c + seg) * G;
+                float pm[G], pl[G], pa[G][DPL];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + (sl + h) * 2));
+                    pm[h] = ml.x;
+                    pl[h] = ml.y;
+                    const float *src = a.part_acc + (sl + h) * D + lane * DPL;
+                    if constexpr (DPL == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                        pa[h][0] = v.x;
+                        pa[h][1] = v.y;
+                        pa[h][2] = v.z;
+                        pa[h][3] = v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                        pa[h][0] = v.x;
+                        pa[h][1] = v.y;
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float Mn = fmaxf(Ms[h], pm[h]);
+                    const float so = exp2f(Ms[h] - Mn), sn = exp2f(pm[h] - Mn);
+                    Ls[h] = fmaf(Ls[h], so, pl[h] * sn);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(acc[h][i], so, pa[h][i] * sn);
+                    Ms[h] = Mn;
+                }
+            }
+            for (int c = c0 + lane; c <= c1; c += 32)
+                if (c != me) dev::flag_store(a.ready + c + seg, 0);
+            if (lane == 0) a.tickets[seg] = 0;
+        }
+        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(pc.b) * H + pc.kv * G) * D + lane * DPL;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float inv = 1.f / Ls[h];
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) ob[h * D + i] = Ops::round(acc[h][i] * inv);
+        }
+    }
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
     using C = MmaCfg<T, D, G>;
     using Ops = MmaOps<T>;
-    constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS, NTD = C::NTD;
+    constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS;
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -193,17 +365,20 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t stage0 = dev::smem_addr(smem);
     const uint32_t bar0 = stage0 + uint32_t(ns) * C::STAGE_BYTES;  // full[ns], then empty[ns]
-    float *scr_acc = reinterpret_cast<float *>(smem + size_t(ns) * C::STAGE_BYTES + 16 * size_t(ns));
+    const uint32_t scr_full = bar0 + 16 * uint32_t(ns);             // consumer states written
+    const uint32_t scr_free = scr_full + 8;                         // consumer states read
+    float *scr_acc = reinterpret_cast<float *>(smem + size_t(ns) * C::STAGE_BYTES + 16 * size_t(ns) + 16);
     float *scr_ml = scr_acc + C::SCR_ACC_FLOATS;
-    volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);  // abort, last
+    volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);  // abort
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
             dev::mbar_init(bar0 + 8 * s, 1);
             dev::mbar_init(bar0 + 8 * (ns + s), 1);
         }
+        dev::mbar_init(scr_full, NW);
+        dev::mbar_init(scr_free, 1);
         flags[0] = 0;
-        flags[1] = 0;
         dev::fence_mbar_init();
     }
     __syncthreads();
@@ -224,38 +399,51 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         __syncwarp();
         return;
     }
+    // ---------------------------------------------------------------- merger
+    if (warp == 1) {
+        merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
+        __syncwarp();
+        dev::named_barrier_sync(2, C::THREADS);
+        return;
+    }
 
     // ---------------------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int ctid = threadIdx.x - 32;
-    const int gr = lane >> 2;  // row of the m16 tile = query head within the group
+    const int cw = warp - 2;
+    const int gq = lane >> 2;  // fragment row group: query head of B / C columns
     const int tq = lane & 3;   // quad lane
     const int H = a.H_kv * G;
-    // ldmatrix row addresses (see the layouts above)
-    const int k_key = ((lane >> 4) & 1) * 8 + (lane & 7);   // score B: matrices (k0, d0) (k0, d8) (k8, d0) (k8, d8)
-    const int k_col = ((lane >> 3) & 1) * 8;
-    const int v_key = ((lane >> 3) & 1) * 8 + (lane & 7);   // P.V B: matrices (k0, d0) (k8, d0) (k0, d8) (k8, d8)
-    const int v_col = ((lane >> 4) & 1) * 8;
+    // ldmatrix lanes.  S^T operand A from K rows: matrices (keys 0-7, d 0-7)
+    // (keys 8-15, d 0-7) (keys 0-7, d 8-15) (keys 8-15, d 8-15).  O^T operand
+    // A from V rows with .trans: matrices (d 0-7, keys 0-7) (d 8-15, keys 0-7)
+    // (d 0-7, keys 8-15) (d 8-15, keys 8-15).
+    const int k_row = ((lane >> 3) & 1) * 8 + (lane & 7), k_half = (lane >> 4) & 1;
+    const int v_row = ((lane >> 4) & 1) * 8 + (lane & 7), v_half = (lane >> 3) & 1;
+    uint32_t koff[4], voff[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        koff[j] = swz_lane_offset(k_row, k_half, lane, j);
+        voff[j] = swz_lane_offset(v_row, v_half, lane, j);
+    }
 
-    uint32_t qa[KSTEPS][2];
-    float o[NTD][4];
-    float m, l;
-    uint32_t t = 0;
+    uint32_t qb[KSTEPS][2];
+    float o[KSTEPS][4];
+    float m0, m1, l0, l1;  // heads 2tq and 2tq + 1
+    uint32_t t = 0, piece = 0;
     int stage = 0;
     uint32_t round = 0;
     Piece pc;
     while (walk.next(a, pc)) {
         {
-            const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + gr) * D;
+            const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + gq) * D;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                qa[ks][0] = gr < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
-                qa[ks][1] = gr < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
+                qb[ks][0] = gq < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
+                qb[ks][1] = gq < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
             }
 #pragma unroll
-            for (int n = 0; n < NTD; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            m = -INFINITY;
-            l = 0.f;
+            for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
         }
 
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE, ++t) {
@@ -286,94 +474,131 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             const uint32_t ks_base = stage0 + uint32_t(cur_stage) * C::STAGE_BYTES;
             const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
-            // ---- scores S = Q . K^T for 32 keys (4 n-tiles of 8)
-            float sacc[4][4];
+            // ---- S^T = K . Q^T for 32 keys (2 m-tiles of 16)
+            float s[2][4];
 #pragma unroll
-            for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+            for (int mt = 0; mt < 2; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                const uint32_t afr[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int mt = 0; mt < 2; ++mt) {
                     uint32_t r[4];
-                    dev::ldsm_x4(C::swz(ks_base, half * 16 + k_key, ks * 16 + k_col), r);
-                    Ops::mma(sacc[2 * half], afr, r[0], r[1]);
-                    Ops::mma(sacc[2 * half + 1], afr, r[2], r[3]);
+                    dev::ldsm_x4(ks_base + (ks >> 2) * C::BLOCK_BYTES + mt * 2048 + koff[ks & 3], r);
+                    Ops::mma(s[mt], r, qb[ks][0], qb[ks][1]);
                 }
             }
 
-            // ---- online softmax for head gr (row gr of the tile, held by 4 lanes)
-            float p[8];
-            float tmax = -INFINITY;
+            // ---- online softmax per head column (keys along the rows)
+            if (nr < TILE) {
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = n * 8 + 2 * tq + e;
-                    p[n * 2 + e] = key < nr ? sacc[n][e] * a.scale_log2 : -INFINITY;
-                    tmax = fmaxf(tmax, p[n * 2 + e]);
-                }
-            tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 2));
-            const float mn = fmaxf(m, tmax);
-            const float corr = exp2f(m - mn);
-            m = mn;
-            float psum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                p[i] = exp2f(p[i] - mn);
-                psum += p[i];
-            }
-            l = fmaf(l, corr, psum);
-            if (__any_sync(FULL, corr != 1.f)) {
-#pragma unroll
-                for (int n = 0; n < NTD; ++n) {
-                    o[n][0] *= corr;
-                    o[n][1] *= corr;
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int k = 16 * mt + gq;
+                    if (k >= nr) s[mt][0] = s[mt][1] = -INFINITY;
+                    if (k + 8 >= nr) s[mt][2] = s[mt][3] = -INFINITY;
                 }
             }
-            uint32_t pa[4];
+            float x0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+            float x1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
 #pragma unroll
-            for (int n = 0; n < 4; ++n) pa[n] = Ops::pack(p[2 * n], p[2 * n + 1]);
-
-            // ---- O += P . V over the tile's two 16-key steps
+            for (int off = 4; off < 32; off <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
+                x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, off));
+            }
+            const float mn0 = fmaxf(m0, x0 * a.scale_log2), mn1 = fmaxf(m1, x1 * a.scale_log2);
+            const float corr0 = exp2f(m0 - mn0), corr1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float p[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                p[mt][0] = exp2f(fmaf(s[mt][0], a.scale_log2, -mn0));
+                p[mt][1] = exp2f(fmaf(s[mt][1], a.scale_log2, -mn1));
+                p[mt][2] = exp2f(fmaf(s[mt][2], a.scale_log2, -mn0));
+                p[mt][3] = exp2f(fmaf(s[mt][3], a.scale_log2, -mn1));
+            }
+            l0 = fmaf(l0, corr0, (p[0][0] + p[0][2]) + (p[1][0] + p[1][2]));
+            l1 = fmaf(l1, corr1, (p[0][1] + p[0][3]) + (p[1][1] + p[1][3]));
+            if (__any_sync(FULL, (corr0 != 1.f) || (corr1 != 1.f))) {
+                const float2 cc = make_float2(corr0, corr1);
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const float2 lo = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), cc);
+                    const float2 hi = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), cc);
+                    o[mt][0] = lo.x;
+                    o[mt][1] = lo.y;
+                    o[mt][2] = hi.x;
+                    o[mt][3] = hi.y;
+                }
+            }
+            // P^T blocks (keys x heads) -> B fragments (keys along k)
+            uint32_t pb[2][2];
 #pragma unroll
             for (int kst = 0; kst < 2; ++kst) {
-                const uint32_t afr[4] = {pa[2 * kst], 0u, pa[2 * kst + 1], 0u};
+                pb[kst][0] = dev::movmatrix_trans(Ops::pack(p[kst][0], p[kst][1]));
+                pb[kst][1] = dev::movmatrix_trans(Ops::pack(p[kst][2], p[kst][3]));
+            }
+
+            // ---- O^T += V^T . P^T over the tile's two 16-key steps
 #pragma unroll
-                for (int dn = 0; dn < NTD / 2; ++dn) {
+            for (int kst = 0; kst < 2; ++kst) {
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
                     uint32_t r[4];
-                    dev::ldsm_x4_trans(C::swz(vs_base, kst * 16 + v_key, dn * 16 + v_col), r);
+                    dev::ldsm_x4_trans(vs_base + (mt >> 2) * C::BLOCK_BYTES + kst * 2048 + voff[mt & 3], r);
                     if (nr < TILE) {  // stale rows past the copied ones
                         const int k0 = kst * 16 + 2 * tq;
                         r[0] = live_pair(r[0], k0, nr);
-                        r[1] = live_pair(r[1], k0 + 8, nr);
-                        r[2] = live_pair(r[2], k0, nr);
+                        r[1] = live_pair(r[1], k0, nr);
+                        r[2] = live_pair(r[2], k0 + 8, nr);
                         r[3] = live_pair(r[3], k0 + 8, nr);
                     }
-                    Ops::mma(o[2 * dn], afr, r[0], r[1]);
-                    Ops::mma(o[2 * dn + 1], afr, r[2], r[3]);
+                    Ops::mma(o[mt], r, pb[kst][0], pb[kst][1]);
                 }
             }
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(empty_bar);
         }
 
-        // ---- end of piece: this warp's state to shared memory, then merge
-        l += __shfl_xor_sync(FULL, l, 1);
-        l += __shfl_xor_sync(FULL, l, 2);
-        if (gr < G) {
+        // ---- end of piece: hand this warp's state to the merge warp
 #pragma unroll
-            for (int n = 0; n < NTD; ++n)
-                *reinterpret_cast<float2 *>(scr_acc + (cw * G + gr) * D + n * 8 + 2 * tq) =
-                    make_float2(o[n][0], o[n][1]);
-            if (tq == 0) {
-                scr_ml[(cw * G + gr) * 2] = m;
-                scr_ml[(cw * G + gr) * 2 + 1] = l;
-            }
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(FULL, l0, off);
+            l1 += __shfl_xor_sync(FULL, l1, off);
         }
-        dev::named_barrier_sync(1, NW * 32);
-        merge_piece<T, D, G, NW>(a, plan, pc, scr_acc, scr_ml, flags, ctid);
+        bool ok = !flags[0] &&
+                  (piece == 0 || dev::mbar_wait_bounded(scr_free, (piece - 1) & 1, flags, a.timeout_ns));
+        ok = __all_sync(FULL, ok);
+        if (ok) {
+            const int h0 = 2 * tq, h1 = 2 * tq + 1;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                const int d = 16 * mt + gq;
+                if (h0 < G) {
+                    scr_acc[(cw * G + h0) * D + d] = o[mt][0];
+                    scr_acc[(cw * G + h0) * D + d + 8] = o[mt][2];
+                }
+                if (h1 < G) {
+                    scr_acc[(cw * G + h1) * D + d] = o[mt][1];
+                    scr_acc[(cw * G + h1) * D + d + 8] = o[mt][3];
+                }
+            }
+            if (gq == 0) {
+                if (h0 < G) {
+                    scr_ml[(cw * G + h0) * 2] = m0;
+                    scr_ml[(cw * G + h0) * 2 + 1] = l0;
+                }
+                if (h1 < G) {
+                    scr_ml[(cw * G + h1) * 2] = m1;
+                    scr_ml[(cw * G + h1) * 2 + 1] = l1;
+                }
+            }
+        } else if (lane == 0) {
+            if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+            flags[0] = 1;
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(scr_full);
+        ++piece;
     }
     dev::named_barrier_sync(2, C::THREADS);
 }

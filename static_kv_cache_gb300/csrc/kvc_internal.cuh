@@ -26,6 +26,7 @@ constexpr unsigned long long WAIT_TIMEOUT_NS = 1000ull * 1000ull * 1000ull;  // 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)            error word (int32) + padding
 //   tickets             int32 [B * H_kv]         arrivals per (sequence, KV head)
+//   ready               int32 [slots]            split partial published (1) or not (0)
 //   part_ml             float [slots][G][2]      (running max, sum) per split
 //   part_acc            float [slots][G][D]      unnormalised output per split
 // slots = MAX_CTAS + B * H_kv: split c of segment s uses slot c + s, which is
@@ -34,7 +35,7 @@ constexpr unsigned long long WAIT_TIMEOUT_NS = 1000ull * 1000ull * 1000ull;  // 
 // segment, or both).
 // ---------------------------------------------------------------------------
 struct WorkspaceLayout {
-    uint64_t tickets, part_ml, part_acc, total;
+    uint64_t tickets, ready, part_ml, part_acc, total;
 };
 
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
@@ -44,7 +45,8 @@ inline WorkspaceLayout workspace_layout(int B, int H_kv, int G, int D) {
     const uint64_t segs = uint64_t(B) * H_kv;
     const uint64_t slots = uint64_t(MAX_CTAS) + segs;
     w.tickets = 256;
-    w.part_ml = align256(w.tickets + segs * 4);
+    w.ready = align256(w.tickets + segs * 4);
+    w.part_ml = align256(w.ready + slots * 4);
     w.part_acc = align256(w.part_ml + slots * G * 2 * 4);
     w.total = align256(w.part_acc + slots * G * uint64_t(D) * 4);
     return w;
@@ -60,6 +62,7 @@ struct DecodeArgs {
     float *part_ml;
     float *part_acc;
     int32_t *tickets;
+    int32_t *ready;            // [slots], zero between launches
     int32_t *err;
     int32_t B, H_kv, max_ctx;
     int32_t n_stages;
@@ -178,6 +181,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// Wait until the global flag *p becomes non-zero (acquire at GPU scope).
+// Gives up like mbar_wait_bounded.
+__device__ __forceinline__ bool flag_wait_bounded(const int32_t *p, const volatile int *abort,
+                                                  unsigned long long timeout_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v != 0) return true;
+        if (*abort) return false;
+        if (it == 0) {
+            t0 = global_timer_ns();
+        } else if (global_timer_ns() - t0 > timeout_ns) {
+            return false;
+        }
+    }
+    return false;
+}
+
+// Store to a global flag that other CTAs poll (after a fence that orders the
+// data it publishes).
+__device__ __forceinline__ void flag_store(int32_t *p, int32_t v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // 1-D bulk copy global -> shared through the TMA unit; completion is
 // signalled on `bar` as transaction bytes.  dst, src and bytes must be
 // multiples of 16.
@@ -226,6 +254,14 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as a warp fragment: lane
+// l holds the pair (row l/4, columns 2*(l%4), 2*(l%4)+1) before and after.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {

@@ -161,12 +161,14 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     if (grid < 1) grid = 1;
 
     // Scratch layout inside the array: error word, one counter per
-    // (sequence, KV head), then the split partials.  Split c of segment s
-    // uses slot c + s, so grid + B * H_kv slots suffice.
+    // (sequence, KV head), one publish flag per split slot, then the split
+    // partials.  Split c of segment s uses slot c + s, so grid + B * H_kv
+    // slots suffice.
     const uint64_t segs = uint64_t(cfg->batch) * cfg->n_kv_heads;
     const uint64_t slots = uint64_t(grid) + segs;
     const uint64_t off_tickets = 256;
-    const uint64_t off_ml = round256(off_tickets + segs * 4);
+    const uint64_t off_ready = round256(off_tickets + segs * 4);
+    const uint64_t off_ml = round256(off_ready + slots * 4);
     const uint64_t off_acc = round256(off_ml + slots * G * 2 * 4);
     const uint64_t total = round256(off_acc + slots * G * uint64_t(cfg->d_head) * 4);
     if (total > KVC_STATIC_SCRATCH_BYTES) return KVC_ERR_WORKSPACE;
@@ -180,8 +182,8 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
                                 &maps[0], &maps[1], &maps[2], &maps[3]))
         return KVC_ERR_CUDA;
 
-    // The array keeps the previous call's contents: the error word and the
-    // counters must start at zero.
+    // The array keeps the previous call's contents: the error word, the
+    // counters and the publish flags must start at zero.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ds->scratch, 0, off_ml, s) != cudaSuccess) return KVC_ERR_CUDA;
 
@@ -196,6 +198,7 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     a.part_ml = reinterpret_cast<float *>(ds->scratch + off_ml);
     a.part_acc = reinterpret_cast<float *>(ds->scratch + off_acc);
     a.tickets = reinterpret_cast<int32_t *>(ds->scratch + off_tickets);
+    a.ready = reinterpret_cast<int32_t *>(ds->scratch + off_ready);
     a.err = reinterpret_cast<int32_t *>(ds->scratch);
     a.B = cfg->batch;
     a.H_kv = cfg->n_kv_heads;
