@@ -160,8 +160,10 @@ struct Plan {
     int n;        // valid_len[b]
 };
 
-__device__ __forceinline__ int live_len(const DecodeArgs &a, int b) {
-    const int v = __ldg(a.valid_len + b);
+// Live rows of sequence b, 0 for an out-of-range length.  `vl` is the
+// valid_len array or a shared-memory copy of it.
+__device__ __forceinline__ int live_len(const DecodeArgs &a, const int32_t *vl, int b) {
+    const int v = vl[b];
     return (v >= 1 && v <= a.max_ctx) ? v : 0;
 }
 
@@ -171,14 +173,14 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
     return v;
 }
 
-__device__ __forceinline__ Plan make_plan(const DecodeArgs &a, int lane) {
+__device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl, int lane) {
     Plan p;
     int64_t total = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
         int n = 0;
         if (b < a.B) {
-            n = live_len(a, b);
+            n = live_len(a, vl, b);
             if (n == 0 && blockIdx.x == 0 && threadIdx.x < 32) dev::record_error(a.err, ERR_DEVICE_INDEX);
         }
         total += warp_sum_i64(n);
@@ -194,7 +196,7 @@ __device__ __forceinline__ Plan make_plan(const DecodeArgs &a, int lane) {
     int64_t base = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
-        const int n = (b < a.B) ? live_len(a, b) : 0;
+        const int n = (b < a.B) ? live_len(a, vl, b) : 0;
         const int64_t w = int64_t(n) * a.H_kv;
         int64_t incl = w;
 #pragma unroll
@@ -224,10 +226,12 @@ struct Piece {
 };
 
 struct Walker {
+    const int32_t *vl;
     int b, kv, n;
     int64_t seg_start, r, r1;
 
-    __device__ __forceinline__ void init(const DecodeArgs &a, const Plan &p) {
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Plan &p, const int32_t *lengths) {
+        vl = lengths;
         b = p.b;
         n = p.n;
         r = p.r0;
@@ -244,7 +248,7 @@ struct Walker {
                 kv = 0;
                 do {
                     ++b;
-                    n = (b < a.B) ? live_len(a, b) : 0;
+                    n = (b < a.B) ? live_len(a, vl, b) : 0;
                 } while (b < a.B && n == 0);
                 if (b >= a.B) return false;
             }
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
     decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     using C = DecodeCfg<T, D, G>;
     using Ops = ElemOps<T>;
-    constexpr int NW = C::NW, LPR = C::LPR, RPW = C::RPW, E = C::E, EPC = C::EPC, CPL = C::CPL;
+    constexpr int NW = C::NW, LPR = C::LPR, RPW = C::RPW, EPC = C::EPC, CPL = C::CPL;
     constexpr int NPASS = C::NPASS, TILE = C::TILE, SHIFT = C::SHIFT;
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -420,11 +424,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
     }
     __syncthreads();
 
-    const Plan plan = make_plan(a, lane);
+    const Plan plan = make_plan(a, a.valid_len, lane);
     if (plan.r0 >= plan.r1 || plan.b >= a.B) return;  // uniform over the CTA
 
     Walker walk;
-    walk.init(a, plan);
+    walk.init(a, plan, a.valid_len);
     const int64_t kv_slab = int64_t(a.max_ctx) * C::ROW_BYTES;  // bytes per (b, kv)
 
     // ---------------------------------------------------------------- producer

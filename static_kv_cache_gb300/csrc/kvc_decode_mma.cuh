@@ -87,9 +87,15 @@ struct MmaCfg {
     static constexpr int THREADS = (NW + 2) * 32;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
+    static constexpr int VL_CACHE = 256;                // valid lengths kept in shared memory
+    static constexpr int N_FLAGS = 8;                   // abort flag, then the final-combine job
     // 1 KB of slack to align the stages to the 1024-byte swizzle atom, the two
-    // merge barriers, the consumers' states, the abort flag
-    static constexpr int FIXED_SMEM = 1024 + 16 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 16;
+    // merge barriers, the consumers' states, the flags, the valid lengths
+    static constexpr int FIXED_SMEM =
+        1024 + 16 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 4 * N_FLAGS + 4 * VL_CACHE;
+    // A final piece whose segment has more than this many other splits is
+    // combined by every warp of the CTA instead of the merge warp alone.
+    static constexpr int HELP_MIN_OTHERS = 4;
 
     static_assert(sizeof(T) == 2, "the tensor-core path takes 16-bit caches");
     static_assert(G >= 1 && G <= 8, "the query group must fit the N = 8 side of the tile");
@@ -114,6 +120,7 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
     uint32_t issued = 0;
     int stage = 0;
     uint32_t round = 0;
+    uint32_t generic_written = 0;  // stages whose last fill used cp.async
     bool ok = true;
     Piece pc;
     while (ok && walk.next(a, pc)) {
@@ -140,6 +147,9 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
             const uint32_t vdst = kdst + C::TILE_BYTES;
             const int q = nr >> 3, rem = nr & 7;  // 8-row groups, rows after them
             if (lane == 0) {
+                // the stage's previous rows came through the generic proxy:
+                // order them before the TMA unit overwrites the stage
+                if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
                 if (q == 4) {
 #pragma unroll
@@ -158,16 +168,20 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
                 }
             }
             if (rem) {
+                // rows no box may cover: 16-byte asynchronous copies, each
+                // lane's completion counted on the stage's barrier
                 const int per = rem * C::CHUNKS;  // 16-byte chunks per tensor
                 for (int i = lane; i < 2 * per; i += 32) {
                     const bool is_v = i >= per;
                     const int j = is_v ? i - per : i;
                     const int r = 8 * q + j / C::CHUNKS, c16 = j % C::CHUNKS;
                     const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
-                    dev::st_shared_v4(C::swz(is_v ? vdst : kdst, r, c16 * 8), v);
+                    dev::cp_async_16(C::swz(is_v ? vdst : kdst, r, c16 * 8), src);
                 }
-                dev::fence_proxy_async_smem();
+                dev::cp_async_arrive(full);
+                generic_written |= 1u << stage;
+            } else {
+                generic_written &= ~(1u << stage);
             }
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(full);
@@ -193,50 +207,40 @@ __device__ __forceinline__ uint32_t swz_lane_offset(int row, int half, int lane,
     return uint32_t(row) * 128 + ((uint32_t(2 * j) ^ uint32_t(half ^ (lane & 7))) << 4);
 }
 
-// The merge warp: for each piece of the CTA, wait for the NW consumer states,
-// combine them (lane l owns columns [l * D/32, (l + 1) * D/32) of every head)
-// and free the states.  A piece that is a whole segment writes its output.
-// A split takes a ticket on the segment's counter first: every split but the
-// last publishes its partial (data, fence, then its ready flag); the last one
-// waits for the others' flags -- their CTAs are past their tickets, so the
-// wait is short and needs no co-residency -- and folds their partials into
-// its own state, still in registers, then writes the output and resets the
-// counter and the flags for the next launch.
-template <typename T, int D, int G, int NW>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs &a, const Plan &plan, Walker walk,
-                                             const float *scr_acc, const float *scr_ml, uint32_t scr_full,
-                                             uint32_t scr_free, volatile int *flags, int lane) {
-    using Ops = ElemOps<T>;
-    constexpr int DPL = D / 32;
-    constexpr unsigned FULL = 0xffffffffu;
-    static_assert(DPL == 2 || DPL == 4, "merge lanes own 2 or 4 columns");
-    const int H = a.H_kv * G;
-    uint32_t piece = 0;
-    Piece pc;
-    while (walk.next(a, pc)) {
-        bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
-        ok = __all_sync(FULL, ok);
-        if (!ok) {
-            if (lane == 0) {
-                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
-                flags[0] = 1;
-            }
-            return;
+// A softmax state over a set of keys for the G heads of one KV head, as the
+// merge lanes hold it: lane l owns columns [l * D/32, (l + 1) * D/32).
+template <int D, int G>
+struct LaneState {
+    static constexpr int DPL = D / 32;
+    float acc[G][DPL];  // unnormalised output
+    float m[G];         // running maximum (log2 domain)
+    float l[G];         // running sum
+
+    __device__ __forceinline__ void clear() {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
         }
-        float acc[G][DPL], Ms[G], Ls[G];
+    }
+
+    // Combine the states of slots [0, n) of a shared-memory array laid out
+    // [slot][G][D] (acc) and [slot][G][2] (max, sum) into this state, which
+    // it replaces.
+    __device__ __forceinline__ void reduce_slots(const float *sacc, const float *sml, int n, int lane) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, scr_ml[(w * G + h) * 2]);
+            for (int w = 0; w < n; ++w) M = fmaxf(M, sml[(w * G + h) * 2]);
             float L = 0.f;
 #pragma unroll
             for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float e = exp2f(scr_ml[(w * G + h) * 2] - M);
-                L = fmaf(scr_ml[(w * G + h) * 2 + 1], e, L);
-                const float *src = scr_acc + (w * G + h) * D + lane * DPL;
+            for (int w = 0; w < n; ++w) {
+                const float e = exp2f(sml[(w * G + h) * 2] - M);
+                L = fmaf(sml[(w * G + h) * 2 + 1], e, L);
+                const float *src = sacc + (w * G + h) * D + lane * DPL;
                 if constexpr (DPL == 4) {
                     const float4 v = *reinterpret_cast<const float4 *>(src);
                     acc[h][0] = fmaf(v.x, e, acc[h][0]);
@@ -249,9 +253,170 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs &a, const Plan &pl
                     acc[h][1] = fmaf(v.y, e, acc[h][1]);
                 }
             }
-            Ms[h] = M;
-            Ls[h] = L;
+            m[h] = M;
+            l[h] = L;
         }
+    }
+
+    // Store this state as slot `slot` of such an array.
+    __device__ __forceinline__ void store_slot(float *sacc, float *sml, int slot, int lane) const {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float *dst = sacc + (slot * G + h) * D + lane * DPL;
+            if constexpr (DPL == 4)
+                *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+            else
+                *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
+        }
+        if (lane < G) {
+            float mv = m[0], lv = l[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h)
+                if (lane == h) {
+                    mv = m[h];
+                    lv = l[h];
+                }
+            *reinterpret_cast<float2 *>(sml + (slot * G + lane) * 2) = make_float2(mv, lv);
+        }
+    }
+
+    // Fold split partials c = first, first + step, ... <= last of segment
+    // `seg` (all but `skip`) from the workspace into this state.  U partials'
+    // loads are issued together.
+    template <int U>
+    __device__ __forceinline__ void fold_partials(const DecodeArgs &a, int seg, int first, int last, int step,
+                                                  int skip, int lane) {
+        for (int c = first; c <= last; c += U * step) {
+            float pm[U][G], pl[U][G], pa[U][G][DPL];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int cu = c + u * step;
+                const bool use = cu <= last && cu != skip;
+                const int64_t sl = int64_t(cu + seg) * G;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    pm[u][h] = -INFINITY;
+                    pl[u][h] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) pa[u][h][i] = 0.f;
+                    if (use) {
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + (sl + h) * 2));
+                        pm[u][h] = ml.x;
+                        pl[u][h] = ml.y;
+                        const float *src = a.part_acc + (sl + h) * D + lane * DPL;
+                        if constexpr (DPL == 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                            pa[u][h][0] = v.x;
+                            pa[u][h][1] = v.y;
+                            pa[u][h][2] = v.z;
+                            pa[u][h][3] = v.w;
+                        } else {
+                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                            pa[u][h][0] = v.x;
+                            pa[u][h][1] = v.y;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    if (pm[u][h] == -INFINITY) continue;  // no partial (every split has a finite max)
+                    const float Mn = fmaxf(m[h], pm[u][h]);
+                    const float so = exp2f(m[h] - Mn), sn = exp2f(pm[u][h] - Mn);
+                    l[h] = fmaf(l[h], so, pl[u][h] * sn);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(acc[h][i], so, pa[u][h][i] * sn);
+                    m[h] = Mn;
+                }
+        }
+    }
+
+    // Publish this state as the split partial of slot `slot`.
+    __device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t slot, int lane) const {
+        const int64_t sl = slot * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float *dst = a.part_acc + (sl + h) * D + lane * DPL;
+            if constexpr (DPL == 4)
+                *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+            else
+                *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
+        }
+        if (lane < G) {
+            float mv = m[0], lv = l[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h)
+                if (lane == h) {
+                    mv = m[h];
+                    lv = l[h];
+                }
+            *reinterpret_cast<float2 *>(a.part_ml + (sl + lane) * 2) = make_float2(mv, lv);
+        }
+    }
+
+    // out[b, kv*G + h, :] = acc / l, rounded once.
+    template <typename T>
+    __device__ __forceinline__ void write_output(const DecodeArgs &a, int b, int kv, int lane) const {
+        using Ops = ElemOps<T>;
+        const int H = a.H_kv * G;
+        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(b) * H + kv * G) * D + lane * DPL;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float inv = 1.f / l[h];
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) ob[h * D + i] = Ops::round(acc[h][i] * inv);
+        }
+    }
+};
+
+// Partials the fold issues together: bounded by the registers they take.
+template <int D, int G>
+__host__ __device__ constexpr int fold_batch() {
+    return (G * (D / 32 + 2)) <= 24 ? 4 : (G * (D / 32 + 2)) <= 36 ? 2 : 1;
+}
+
+// The combine that the final piece of a CTA still owes when its segment has
+// many splits: done by every warp of the CTA after the stream has ended.
+struct FinalCombine {
+    int seg, c0, c1, me, b, kv;
+};
+
+// The merge warp: for each piece of the CTA, wait for the NW consumer states,
+// combine them and free the states.  A piece that is a whole segment writes
+// its output.  A split takes a ticket on the segment's counter first: every
+// split but the last publishes its partial (data, fence, then its ready
+// flag); the last one waits for the others' flags -- their CTAs are past their
+// tickets, so the wait is short and needs no co-residency -- and folds their
+// partials into its own state, then writes the output and resets the counter
+// and the flags for the next launch.  When that last split is the CTA's final
+// piece and the segment has more than HELP_MIN_OTHERS other splits, the fold
+// is left to the whole CTA: the function returns true with the job in `job`
+// and the CTA's own partial in `st`.
+template <typename T, int D, int G, int NW>
+__device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &plan, Walker walk,
+                                             const float *scr_acc, const float *scr_ml, uint32_t scr_full,
+                                             uint32_t scr_free, volatile int *flags, int lane,
+                                             LaneState<D, G> &st, FinalCombine &job) {
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr int HELP_MIN_OTHERS = MmaCfg<T, D, G>::HELP_MIN_OTHERS;
+    uint32_t piece = 0;
+    Piece pc;
+    while (walk.next(a, pc)) {
+        Walker peek = walk;
+        Piece next_pc;
+        const bool final_piece = !peek.next(a, next_pc);
+        bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
+        ok = __all_sync(FULL, ok);
+        if (!ok) {
+            if (lane == 0) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            return false;
+        }
+        st.reduce_slots(scr_acc, scr_ml, NW, lane);
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(scr_free);
         ++piece;
@@ -266,25 +431,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs &a, const Plan &pl
             ticket = __shfl_sync(FULL, ticket, 0);
             if (ticket < c1 - c0) {
                 // not the last split: publish the partial
-                const int64_t sl = int64_t(me + seg) * G;
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float *dst = a.part_acc + (sl + h) * D + lane * DPL;
-                    if constexpr (DPL == 4)
-                        *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-                    else
-                        *reinterpret_cast<float2 *>(dst) = make_float2(acc[h][0], acc[h][1]);
-                }
-                if (lane < G) {
-                    float mv = Ms[0], lv = Ls[0];
-#pragma unroll
-                    for (int h = 1; h < G; ++h)
-                        if (lane == h) {
-                            mv = Ms[h];
-                            lv = Ls[h];
-                        }
-                    *reinterpret_cast<float2 *>(a.part_ml + (sl + lane) * 2) = make_float2(mv, lv);
-                }
+                st.store_partial(a, me + seg, lane);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) dev::flag_store(a.ready + me + seg, 1);
@@ -300,54 +447,21 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs &a, const Plan &pl
                     if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
                     flags[0] = 1;
                 }
-                return;
+                return false;
             }
             __threadfence();
-#pragma unroll 2
-            for (int c = c0; c <= c1; ++c) {
-                if (c == me) continue;
-                const int64_t sl = int64_t(c + seg) * G;
-                float pm[G], pl[G], pa[G][DPL];
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + (sl + h) * 2));
-                    pm[h] = ml.x;
-                    pl[h] = ml.y;
-                    const float *src = a.part_acc + (sl + h) * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                        pa[h][0] = v.x;
-                        pa[h][1] = v.y;
-                        pa[h][2] = v.z;
-                        pa[h][3] = v.w;
-                    } else {
-                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                        pa[h][0] = v.x;
-                        pa[h][1] = v.y;
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float Mn = fmaxf(Ms[h], pm[h]);
-                    const float so = exp2f(Ms[h] - Mn), sn = exp2f(pm[h] - Mn);
-                    Ls[h] = fmaf(Ls[h], so, pl[h] * sn);
-#pragma unroll
-                    for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(acc[h][i], so, pa[h][i] * sn);
-                    Ms[h] = Mn;
-                }
+            if (final_piece && c1 - c0 > HELP_MIN_OTHERS && !flags[0]) {
+                job = FinalCombine{seg, c0, c1, me, pc.b, pc.kv};
+                return true;
             }
+            st.template fold_partials<fold_batch<D, G>()>(a, seg, c0, c1, 1, me, lane);
             for (int c = c0 + lane; c <= c1; c += 32)
                 if (c != me) dev::flag_store(a.ready + c + seg, 0);
             if (lane == 0) a.tickets[seg] = 0;
         }
-        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(pc.b) * H + pc.kv * G) * D + lane * DPL;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float inv = 1.f / Ls[h];
-#pragma unroll
-            for (int i = 0; i < DPL; ++i) ob[h * D + i] = Ops::round(acc[h][i] * inv);
-        }
+        st.template write_output<T>(a, pc.b, pc.kv, lane);
     }
+    return false;
 }
 
 template <typename T, int D, int G>
@@ -369,7 +483,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     const uint32_t scr_free = scr_full + 8;                         // consumer states read
     float *scr_acc = reinterpret_cast<float *>(smem + size_t(ns) * C::STAGE_BYTES + 16 * size_t(ns) + 16);
     float *scr_ml = scr_acc + C::SCR_ACC_FLOATS;
-    volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);  // abort
+    // flags[0]: abort; flags[1]: final combine wanted; flags[2..7]: its job
+    volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);
+    int32_t *vl_cache = reinterpret_cast<int32_t *>(scr_ml + C::SCR_ML_FLOATS) + C::N_FLAGS;
+    const int32_t *vl = a.B <= C::VL_CACHE ? vl_cache : a.valid_len;
+    if (a.B <= C::VL_CACHE)
+        for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -383,11 +502,11 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     }
     __syncthreads();
 
-    const Plan plan = make_plan(a, lane);
+    const Plan plan = make_plan(a, vl, lane);
     if (plan.r0 >= plan.r1 || plan.b >= a.B) return;  // uniform over the CTA
 
     Walker walk;
-    walk.init(a, plan);
+    walk.init(a, plan, vl);
     const int64_t kv_slab = int64_t(a.max_ctx) * C::ROW_BYTES;
 
     // ---------------------------------------------------------------- producer
@@ -399,9 +518,38 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         __syncwarp();
         return;
     }
+    // The stage ring is idle once every consumer has handed over its final
+    // state; the final combine keeps its per-warp states there.
+    float *fin_acc = reinterpret_cast<float *>(smem);
+    float *fin_ml = fin_acc + (NW + 1) * G * D;
+    constexpr int FOLD_U = fold_batch<D, G>();
+
     // ---------------------------------------------------------------- merger
     if (warp == 1) {
-        merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
+        LaneState<D, G> st;
+        FinalCombine job;
+        const bool help = merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
+                                                    lane, st, job);
+        if (lane == 0) {
+            flags[1] = help;
+            flags[2] = job.seg;
+            flags[3] = job.c0;
+            flags[4] = job.c1;
+            flags[5] = job.me;
+        }
+        __syncwarp();
+        dev::named_barrier_sync(3, (NW + 1) * 32);  // consumers and merger
+        if (help) {
+            // the merger's share of the final combine starts from the CTA's own partial
+            st.template fold_partials<FOLD_U>(a, job.seg, job.c0 + NW, job.c1, NW + 1, job.me, lane);
+            st.store_slot(fin_acc, fin_ml, NW, lane);
+            dev::named_barrier_sync(3, (NW + 1) * 32);
+            st.reduce_slots(fin_acc, fin_ml, NW + 1, lane);
+            st.template write_output<T>(a, job.b, job.kv, lane);
+            for (int c = job.c0 + lane; c <= job.c1; c += 32)
+                if (c != job.me) dev::flag_store(a.ready + c + job.seg, 0);
+            if (lane == 0) a.tickets[job.seg] = 0;
+        }
         __syncwarp();
         dev::named_barrier_sync(2, C::THREADS);
         return;
@@ -599,6 +747,17 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(scr_full);
         ++piece;
+    }
+
+    // ---- the final combine, when the merger asks for it
+    dev::named_barrier_sync(3, (NW + 1) * 32);
+    if (flags[1]) {
+        const int seg = flags[2], c0 = flags[3], c1 = flags[4], me = flags[5];
+        LaneState<D, G> st;
+        st.clear();
+        st.template fold_partials<FOLD_U>(a, seg, c0 + cw, c1, NW + 1, me, lane);
+        st.store_slot(fin_acc, fin_ml, cw, lane);
+        dev::named_barrier_sync(3, (NW + 1) * 32);
     }
     dev::named_barrier_sync(2, C::THREADS);
 }

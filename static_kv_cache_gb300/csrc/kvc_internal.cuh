@@ -72,7 +72,7 @@ struct DecodeArgs {
     // (16-bit caches, tensor-core kernel only): boxes of 64 columns x 32 or
     // x 8 rows with the 128-byte swizzle.  seg_base = layer * B * H_kv.
     int32_t seg_base;
-    alignas(64) CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;
+    CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // the type carries its own alignment
 };
 
 // One compiled decode kernel and what the host needs to launch it.
@@ -179,6 +179,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (global_timer_ns() - t0 > timeout_ns) return false;
     }
     return false;
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), tracked by the
+// issuing thread's cp.async group.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
+// barrier's pending count is raised first, so the phase cannot complete
+// before then.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Wait until the global flag *p becomes non-zero (acquire at GPU scope).
