@@ -2,8 +2,10 @@
 """Decode-step benchmark: append + decode attention over a static KV cache.
 
 One step is the whole hot path for every layer of the workload: for each
-layer, kvc_append of the new token's K/V rows at cache_index = valid - 1, then
-kvc_decode_attn of one query row per head over the valid rows.  Every timed
+layer, kvc_decode_step appends the new token's K/V rows at valid - 1 and
+attends with one query row per head over the valid rows (one fused launch on
+the tensor-core kernel, the append and the attention back to back
+otherwise).  Every timed
 step recomputes the same decode step (same positions), so all steps move the
 same bytes.  Default workload: the Llama-3-8B-shaped GQA cache (32 layers,
 B=16, H=32, H_kv=8, d_h=128, max_context 8192, bf16, ragged live lengths
@@ -229,36 +231,36 @@ class DeviceState:
         self.k_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "kn"), dev)
         self.v_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "vn"), dev)
         self.out = torch.empty((L, B, w.n_heads, w.d_head), dtype=tdt, device=dev)
-        self.cache_index = (self.lengths - 1).to(dev)
         self.valid_len = self.lengths.to(dev)
+        # the step is one fused launch on the tensor-core kernel, else append + attention
+        self.launches_per_layer = 1 if decode_kernel_name(w) == "decode_mma_kernel" else 2
         self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
         self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
         st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
         kvc.check(st, "kvc_alloc")
         torch.cuda.synchronize(dev)
 
-    def step(self, stream, events=None, q=None, k_new=None, v_new=None, ci=None, vl=None, out=None) -> int:
-        """One decode step over all layers; returns the number of kernel launches."""
+    def step(self, stream, events=None, q=None, k_new=None, v_new=None, vl=None, out=None) -> int:
+        """One decode step over all layers (append the new rows at valid_len - 1,
+        then attend), one kvc_decode_step call per layer; returns the number
+        of kernel launches."""
         kvc, w = self.kvc, self.w
         q = self.q if q is None else q
         k_new = self.k_new if k_new is None else k_new
         v_new = self.v_new if v_new is None else v_new
-        ci = self.cache_index if ci is None else ci
         vl = self.valid_len if vl is None else vl
         out = self.out if out is None else out
         sp = stream.cuda_stream
         for layer in range(w.n_layers):
-            st = kvc.kvc_append(self.h, layer, k_new[layer], v_new[layer], ci, 1, sp)
-            if st:
-                raise kvc.KvcError(st, "kvc_append")
             if events is not None:
                 events[layer][0].record(stream)
-            st = kvc.kvc_decode_attn(self.h, layer, q[layer], vl, self.maxlen, out[layer], sp)
+            st = kvc.kvc_decode_step(self.h, layer, q[layer], k_new[layer], v_new[layer], vl, self.maxlen,
+                                     out[layer], sp)
             if st:
-                raise kvc.KvcError(st, "kvc_decode_attn")
+                raise kvc.KvcError(st, "kvc_decode_step")
             if events is not None:
                 events[layer][1].record(stream)
-        return 2 * w.n_layers
+        return self.launches_per_layer * w.n_layers
 
     def close(self):
         self.kvc.kvc_free(self.h)
@@ -356,11 +358,11 @@ def bench_kvc(args, rank, world, local):
     if not args.no_e2e:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         hq, hk, hv = pin(state.q), pin(state.k_new), pin(state.v_new)
-        hci, hvl = pin(state.cache_index), pin(state.valid_len)
+        hvl = pin(state.valid_len)
         hout = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
         dq, dk, dv = torch.empty_like(state.q), torch.empty_like(state.k_new), torch.empty_like(state.v_new)
-        dci, dvl = torch.empty_like(state.cache_index), torch.empty_like(state.valid_len)
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hci, hvl))
+        dvl = torch.empty_like(state.valid_len)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hvl))
         d2h = hout.numel() * hout.element_size()
         e2e_steps = max(3, min(args.steps, 200))
         barrier(world)
@@ -368,9 +370,9 @@ def bench_kvc(args, rank, world, local):
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for _ in range(e2e_steps):
-                for d, hsrc in ((dq, hq), (dk, hk), (dv, hv), (dci, hci), (dvl, hvl)):
+                for d, hsrc in ((dq, hq), (dk, hk), (dv, hv), (dvl, hvl)):
                     d.copy_(hsrc, non_blocking=True)
-                state.step(stream, q=dq, k_new=dk, v_new=dv, ci=dci, vl=dvl)
+                state.step(stream, q=dq, k_new=dk, v_new=dv, vl=dvl)
                 hout.copy_(state.out, non_blocking=True)
                 stream.synchronize()
         e2e_s = reduce_max(time.perf_counter() - t0, world, device=torch.device("cuda", local))
@@ -389,7 +391,7 @@ def bench_kvc(args, rank, world, local):
     value = job_throughput(bytes_step, world, elapsed_max, args.steps)
     peak, peak_src = load_peaks()
     mean_decode_s = float(np.mean(decode_ms)) / 1e3
-    achieved = per_layer["attn"] / mean_decode_s / 1e9
+    achieved = (per_layer["attn"] + per_layer["append"]) / mean_decode_s / 1e9
     traffic = recorded_traffic(args.workload)
     if rank == 0:
         line = {
@@ -405,7 +407,7 @@ def bench_kvc(args, rank, world, local):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": decode_kernel_name(w), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
-                         "bytes_per_launch": per_layer["attn"],
+                         "bytes_per_launch": per_layer["attn"] + per_layer["append"],
                          "mean_launch_us": round(mean_decode_s * 1e6, 3)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         }

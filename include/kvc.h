@@ -192,6 +192,29 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q,
                            const int32_t *valid_len, int32_t max_valid_hint,
                            void *out, void *stream);
 
+/* One whole decode step of one layer ("10.3", section 5, the decode loop:
+ * append k_t, v_t to the layer's cache, then attend with the single query
+ * row over the entire cache): for every sequence b the new rows go to
+ * position valid_len[b] - 1, then the attention of kvc_decode_attn runs over
+ * rows [0, valid_len[b]).  The result equals kvc_append(h, layer, k_new,
+ * v_new, valid_len[b] - 1, T_new = 1) followed by kvc_decode_attn with the
+ * same arguments: the cache bytes are identical and the output agrees to
+ * fp32 rounding.  For 16-bit caches with head groups of 2 to 8 and d_h of 64
+ * or 128 it is one launch that reads the new rows straight from k_new /
+ * v_new while it streams the older ones; otherwise it enqueues the append
+ * and the attention back to back.
+ *   layer, q, max_valid_hint, out   as for kvc_decode_attn
+ *   k_new, v_new    device, [B, H_kv, 1, d_h], 16-byte aligned
+ *   valid_len       device int32 [B]: live rows after this step's append.  A
+ *                   sequence with valid_len[b] < 1 or > max_context gets no
+ *                   append and no output, and KVC_ERR_DEVICE_INDEX is
+ *                   recorded.
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q,
+                           const void *k_new, const void *v_new,
+                           const int32_t *valid_len, int32_t max_valid_hint,
+                           void *out, void *stream);
+
 /* ---- decode without any device allocation ------------------------------- */
 
 /* Size of the library's built-in scratch array used by kvc_decode_attn_static:

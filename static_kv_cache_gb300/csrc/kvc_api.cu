@@ -228,18 +228,21 @@ kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void
     const uint64_t slab = layer_slab_bytes(h);
     const cudaError_t e = kvc::launch_append(
         h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
-        static_cast<const uint8_t *>(v_new), cache_index, h->cfg.batch, h->cfg.n_kv_heads, T_new,
+        static_cast<const uint8_t *>(v_new), cache_index, 0, h->cfg.batch, h->cfg.n_kv_heads, T_new,
         h->cfg.max_context, h->cfg.d_head * h->elem_bytes, reinterpret_cast<int32_t *>(h->ws),
         h->num_sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
-kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int32_t *valid_len,
-                           int32_t max_valid_hint, void *out, void *stream) {
-    if (!h || layer < 0 || layer >= h->cfg.n_layers || !q || !valid_len || !out)
-        return KVC_ERR_INVALID;
-    if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
-    if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
+}  // extern "C"
+
+namespace {
+
+// Launch the decode kernel of one layer; k_new / v_new non-null make it the
+// fused step (tensor-core kernel only).  Arguments are already validated.
+kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32_t *valid_len,
+                         int32_t max_valid_hint, void *out, void *stream, const void *k_new,
+                         const void *v_new) {
     const kvc_config &c = h->cfg;
 
     // Splits: every SM streams an equal share of the live rows; tiny
@@ -262,6 +265,8 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int
     a.V = h->v_base + slab * layer;
     a.q = q;
     a.out = out;
+    a.k_new = static_cast<const uint8_t *>(k_new);
+    a.v_new = static_cast<const uint8_t *>(v_new);
     a.valid_len = valid_len;
     a.part_ml = reinterpret_cast<float *>(h->ws + h->wl.part_ml);
     a.part_acc = reinterpret_cast<float *>(h->ws + h->wl.part_acc);
@@ -283,6 +288,38 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int
     }
     const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q, const int32_t *valid_len,
+                           int32_t max_valid_hint, void *out, void *stream) {
+    if (!h || layer < 0 || layer >= h->cfg.n_layers || !q || !valid_len || !out)
+        return KVC_ERR_INVALID;
+    if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
+    if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
+    return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
+}
+
+kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q, const void *k_new, const void *v_new,
+                           const int32_t *valid_len, int32_t max_valid_hint, void *out, void *stream) {
+    if (!h || layer < 0 || layer >= h->cfg.n_layers || !q || !k_new || !v_new || !valid_len || !out)
+        return KVC_ERR_INVALID;
+    if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
+    if (h->decode->tensor_maps)  // one launch: the kernel appends as it streams
+        return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, k_new, v_new);
+    // the CUDA-core kernel: the append, then the attention, on the same stream
+    const uint64_t slab = layer_slab_bytes(h);
+    const cudaError_t e = kvc::launch_append(
+        h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
+        static_cast<const uint8_t *>(v_new), valid_len, -1, h->cfg.batch, h->cfg.n_kv_heads, 1,
+        h->cfg.max_context, h->cfg.d_head * h->elem_bytes, reinterpret_cast<int32_t *>(h->ws), h->num_sms,
+        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return KVC_ERR_CUDA;
+    return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
 }
 
 kvc_status kvc_get_error(kvc_cache *h, void *stream) {

@@ -19,8 +19,8 @@ namespace kvc {
 __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, uint8_t *__restrict__ V,
                                                      const uint8_t *__restrict__ k_new,
                                                      const uint8_t *__restrict__ v_new,
-                                                     const int32_t *__restrict__ cache_index, int B,
-                                                     int H_kv, int T_new, int max_ctx, int row_vecs,
+                                                     const int32_t *__restrict__ cache_index, int index_offset,
+                                                     int B, int H_kv, int T_new, int max_ctx, int row_vecs,
                                                      int32_t *err) {
     const int64_t run = int64_t(T_new) * row_vecs;   // vectors per (b, j)
     const int64_t per_tensor = int64_t(B) * H_kv * run;
@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
         const int64_t seg = r / run;                 // b * H_kv + j
         const int64_t off = r - seg * run;           // vector within the run
         const int b = int(seg / H_kv);
-        const int ci = __ldg(cache_index + b);
+        const int ci = __ldg(cache_index + b) + index_offset;
         if (ci < 0 || ci > max_ctx - T_new) {
             if (off == 0 && seg % H_kv == 0 && !is_v) atomicCAS(err, 0, ERR_DEVICE_INDEX);
             continue;
@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
 }
 
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
-                          const uint8_t *v_new, const int32_t *cache_index, int B, int H_kv,
-                          int T_new, int max_ctx, int row_bytes, int32_t *err, int num_sms,
+                          const uint8_t *v_new, const int32_t *cache_index, int index_offset, int B,
+                          int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err, int num_sms,
                           cudaStream_t stream) {
     const int row_vecs = row_bytes / 16;
     const int64_t total = 2 * int64_t(B) * H_kv * T_new * row_vecs;
@@ -54,8 +54,8 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
     const int64_t want = (total + 255) / 256;
     const int64_t cap = int64_t(num_sms) * 8;
     const int grid = int(want < cap ? want : cap);
-    append_kernel<<<grid, 256, 0, stream>>>(K_layer, V_layer, k_new, v_new, cache_index, B, H_kv, T_new,
-                                            max_ctx, row_vecs, err);
+    append_kernel<<<grid, 256, 0, stream>>>(K_layer, V_layer, k_new, v_new, cache_index, index_offset, B, H_kv,
+                                            T_new, max_ctx, row_vecs, err);
     return cudaGetLastError();
 }
 

@@ -128,6 +128,9 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
         const int z = a.seg_base + seg;  // tensor-map segment coordinate
         const uint8_t *kseg = a.K + int64_t(seg) * kv_slab;
         const uint8_t *vseg = a.V + int64_t(seg) * kv_slab;
+        // In a fused step the segment's last row is this step's new row: it
+        // comes from k_new / v_new, never through a box over the stale cache.
+        const int new_row = a.k_new ? pc.n - 1 : -1;
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE) {
             const int nr = min(TILE, pc.hi - row0);
             if (round > 0) {
@@ -145,7 +148,8 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             const uint32_t vdst = kdst + C::TILE_BYTES;
-            const int q = nr >> 3, rem = nr & 7;  // 8-row groups, rows after them
+            const int nb = (new_row >= row0 && new_row < row0 + nr) ? new_row - row0 : nr;  // rows boxes may cover
+            const int q = nb >> 3, rem = nr - 8 * q;  // 8-row groups, rows after them
             if (lane == 0) {
                 // the stage's previous rows came through the generic proxy:
                 // order them before the TMA unit overwrites the stage
@@ -175,7 +179,10 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
                     const bool is_v = i >= per;
                     const int j = is_v ? i - per : i;
                     const int r = 8 * q + j / C::CHUNKS, c16 = j % C::CHUNKS;
-                    const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
+                    const uint8_t *src =
+                        row0 + r == new_row
+                            ? (is_v ? a.v_new : a.k_new) + int64_t(seg) * C::ROW_BYTES + c16 * 16
+                            : (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
                     dev::cp_async_16(C::swz(is_v ? vdst : kdst, r, c16 * 8), src);
                 }
                 dev::cp_async_arrive(full);
@@ -403,10 +410,24 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
     constexpr int HELP_MIN_OTHERS = MmaCfg<T, D, G>::HELP_MIN_OTHERS;
     uint32_t piece = 0;
     Piece pc;
+    constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
+    static_assert(2 * CHUNKS <= 32, "one 16-byte chunk of the new rows per lane");
+    const int64_t kv_slab = int64_t(a.max_ctx) * ROW_BYTES;
     while (walk.next(a, pc)) {
         Walker peek = walk;
         Piece next_pc;
         const bool final_piece = !peek.next(a, next_pc);
+        if (a.k_new && pc.hi == pc.n && lane < 2 * CHUNKS) {
+            // fused step: this CTA holds the segment's last row; store the
+            // new K and V rows into the cache (nobody in this launch reads
+            // them back from there)
+            const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
+            const bool is_v = lane >= CHUNKS;
+            const int c16 = is_v ? lane - CHUNKS : lane;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) + seg * ROW_BYTES) + c16);
+            uint8_t *cache = const_cast<uint8_t *>(is_v ? a.V : a.K);  // the caller's writable cache
+            reinterpret_cast<uint4 *>(cache + seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES)[c16] = v;
+        }
         bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
         ok = __all_sync(FULL, ok);
         if (!ok) {

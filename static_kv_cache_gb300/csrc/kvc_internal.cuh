@@ -58,6 +58,10 @@ struct DecodeArgs {
     const uint8_t *V;          // layer slab of the V cache
     const void *q;             // [B, H, D]
     void *out;                 // [B, H, D]
+    // Fused decode step (tensor-core kernel): the new rows [B, H_kv, D] that
+    // this launch appends at valid_len - 1 and attends with; null otherwise.
+    const uint8_t *k_new;
+    const uint8_t *v_new;
     const int32_t *valid_len;  // [B]
     float *part_ml;
     float *part_acc;
@@ -111,10 +115,10 @@ bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const 
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
                        CUtensorMap *v8);
 
-// Append launcher (kvc_append.cu).
+// Append launcher (kvc_append.cu): rows go to cache_index[b] + index_offset.
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
-                          const uint8_t *v_new, const int32_t *cache_index, int B,
-                          int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err,
+                          const uint8_t *v_new, const int32_t *cache_index, int index_offset,
+                          int B, int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err,
                           int num_sms, cudaStream_t stream);
 
 }  // namespace kvc

@@ -194,6 +194,8 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     a.V = static_cast<const uint8_t *>(v_base) + slab * layer;
     a.q = q;
     a.out = out;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
     a.valid_len = valid_len;
     a.part_ml = reinterpret_cast<float *>(ds->scratch + off_ml);
     a.part_acc = reinterpret_cast<float *>(ds->scratch + off_acc);

@@ -88,6 +88,13 @@ class Harness:
         st = self.kvc.kvc_decode_attn(self.h, layer, q, valid_len, hint, out, stream)
         return st, out
 
+    def step(self, layer, q, k_new, v_new, valid_len, hint=0, out=None, stream=None):
+        w = self.w
+        if out is None:
+            out = torch.empty((w.batch, w.n_heads, w.d_head), dtype=self.tdtype, device="cuda")
+        st = self.kvc.kvc_decode_step(self.h, layer, q, k_new, v_new, valid_len, hint, out, stream)
+        return st, out
+
     def error(self, stream=None):
         return self.kvc.kvc_get_error(self.h, stream)
 
