@@ -126,7 +126,7 @@ def kernel_source_hash() -> str:
 def recorded_traffic(workload: str):
     """DRAM bytes per launch of the decode kernel from a committed ncu
     summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
