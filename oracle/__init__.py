@@ -14,6 +14,10 @@ Contents
                          Optimization...", section #2, Before/After).
 * ``causal_attention``-- uncached full causal attention ("KV-Cache
                          Mechanics", Disabling the Cache).
+* ``prefill_attn``    -- chunked-prefill attention: each chunk query row
+                         attends over the rows up to its own position
+                         ("10.3", section 3; "KV-Cache Mechanics", AR
+                         Static KV-Cache).
 * ``kv_cache_bytes`` and friends -- the cache-size formula ("10.3",
                          section 2 boxed formula; section 4.4).
 """
@@ -28,8 +32,9 @@ from . import build as _build
 from .cache import ListAppendCache
 from .causal import causal_attention, widen
 from .formula import kv_bytes_per_token, kv_cache_bytes, mla_cache_bytes
+from .prefill import prefill_attn
 
-__all__ = ["decode_attn", "ListAppendCache", "causal_attention", "widen",
+__all__ = ["decode_attn", "prefill_attn", "ListAppendCache", "causal_attention", "widen",
            "kv_cache_bytes", "kv_bytes_per_token", "mla_cache_bytes",
            "load_library", "num_threads", "set_num_threads", "DTYPE_CODES"]
 
