@@ -215,6 +215,37 @@ kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q,
                            const int32_t *valid_len, int32_t max_valid_hint,
                            void *out, void *stream);
 
+/* ---- chunked prefill ------------------------------------------------------ */
+
+/* Causal attention of a chunk of T_new new tokens per sequence over the static
+ * cache ("KV-Cache Mechanics", AR Static KV-Cache: prefill fills the cache from
+ * cache_index, decoding continues from there; "10.3", section 3, prefill vs.
+ * decode).  The chunk's K and V rows must already be in the cache at rows
+ * [cache_index[b], cache_index[b] + T_new) (kvc_append with the same
+ * cache_index and T_new).  For every sequence b, query head i and chunk
+ * position t:
+ *   out[b, i, t, :] = softmax_j( q[b, i, t, :] . K_l[b, i / g, j, :] / sqrt(d_h) )
+ *                     . V_l[b, i / g, j, :]     over j <= cache_index[b] + t
+ * i.e. the decode attention of each chunk token over the rows up to and
+ * including its own (the pages leave the mask implicit; causal is the reading
+ * under which one pass, chunks and decode steps agree).  Rows past a token's
+ * own position are never read.  Arithmetic: fp32 products and accumulation,
+ * one round-to-nearest-even to the cache type.  Built for 16-bit caches with
+ * d_h of 64 or 128 (KVC_ERR_UNSUPPORTED otherwise).
+ *   layer        0 <= layer < n_layers
+ *   q            device, [B, H, T_new, d_h], 16-byte aligned
+ *   cache_index  device int32 [B]: row of each sequence's first chunk token.
+ *                A sequence with cache_index[b] < 0 or cache_index[b] + T_new
+ *                > max_context is skipped (output rows unwritten) and
+ *                KVC_ERR_DEVICE_INDEX is recorded.
+ *   T_new        chunk length, 0 <= T_new <= max_context (0: no-op)
+ *   out          device, [B, H, T_new, d_h]
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_CAPACITY, KVC_ERR_UNSUPPORTED,
+ * KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q,
+                            const int32_t *cache_index, int32_t T_new,
+                            void *out, void *stream);
+
 /* ---- decode without any device allocation ------------------------------- */
 
 /* Size of the library's built-in scratch array used by kvc_decode_attn_static:

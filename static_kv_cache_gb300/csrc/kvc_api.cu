@@ -25,6 +25,7 @@ struct kvc_cache {
     uint64_t ws_bytes;
     kvc::WorkspaceLayout wl;
     const kvc::DecodeKernelInfo *decode;
+    const kvc::PrefillKernelInfo *prefill;  // nullptr where chunked prefill is not built
     int n_stages;
     int smem_bytes;
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
@@ -62,6 +63,20 @@ const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
         default: break;
     }
 #undef KVC_PICK
+    return nullptr;
+}
+
+// Chunked-prefill kernel: 16-bit caches with d_h 64 or 128.
+const kvc::PrefillKernelInfo *find_prefill(const kvc_config *c) {
+    const int G = c->n_heads / c->n_kv_heads;
+    const int D = c->d_head;
+    if (c->dtype == KVC_BF16) {
+        if (D == 64) return kvc::prefill_kernel_bf16_64(G);
+        if (D == 128) return kvc::prefill_kernel_bf16_128(G);
+    } else if (c->dtype == KVC_FP16) {
+        if (D == 64) return kvc::prefill_kernel_f16_64(G);
+        if (D == 128) return kvc::prefill_kernel_f16_128(G);
+    }
     return nullptr;
 }
 
@@ -177,6 +192,8 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
     if (n_stages < info->consumer_warps + 1) return KVC_ERR_UNSUPPORTED;
     const int smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;
     if (info->set_max_smem(smem_bytes) != cudaSuccess) return KVC_ERR_CUDA;
+    const kvc::PrefillKernelInfo *pinfo = find_prefill(cfg);
+    if (pinfo && pinfo->set_max_smem(pinfo->smem) != cudaSuccess) return KVC_ERR_CUDA;
 
     // Zero the workspace: error word and per-segment counters start at 0.
     if (cudaMemsetAsync(workspace, 0, need, 0) != cudaSuccess) return KVC_ERR_CUDA;
@@ -197,9 +214,10 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
     h->ws_bytes = ws_bytes;
     h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads, h->group, cfg->d_head);
     h->decode = info;
+    h->prefill = pinfo;
     h->n_stages = n_stages;
     h->smem_bytes = smem_bytes;
-    if (info->tensor_maps &&
+    if ((info->tensor_maps || pinfo) &&
         !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
                                 int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
                                 &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
@@ -320,6 +338,43 @@ kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q, const voi
         static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return KVC_ERR_CUDA;
     return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
+}
+
+kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const int32_t *cache_index,
+                            int32_t T_new, void *out, void *stream) {
+    if (!h || layer < 0 || layer >= h->cfg.n_layers || !q || !cache_index || !out || T_new < 0)
+        return KVC_ERR_INVALID;
+    if (T_new == 0) return KVC_OK;
+    if (T_new > h->cfg.max_context) return KVC_ERR_CAPACITY;
+    if (!h->prefill) return KVC_ERR_UNSUPPORTED;
+    if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
+    const kvc_config &c = h->cfg;
+    const int64_t rows = int64_t(T_new) * h->group;
+    const int64_t q_blocks = (rows + h->prefill->q_rows - 1) / h->prefill->q_rows;
+    const int64_t grid = int64_t(c.batch) * c.n_kv_heads * q_blocks;
+    if (grid > 0x7fffffff) return KVC_ERR_UNSUPPORTED;
+    const uint64_t slab = layer_slab_bytes(h);
+    kvc::PrefillArgs a;
+    a.K = h->k_base + slab * layer;
+    a.V = h->v_base + slab * layer;
+    a.q = q;
+    a.out = out;
+    a.cache_index = cache_index;
+    a.err = reinterpret_cast<int32_t *>(h->ws);
+    a.B = c.batch;
+    a.H_kv = c.n_kv_heads;
+    a.max_ctx = c.max_context;
+    a.T_new = T_new;
+    a.q_blocks = int(q_blocks);
+    a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
+    a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    a.seg_base = layer * c.batch * c.n_kv_heads;
+    a.tm_k32 = h->tm_k32;
+    a.tm_k8 = h->tm_k8;
+    a.tm_v32 = h->tm_v32;
+    a.tm_v8 = h->tm_v8;
+    const cudaError_t e = h->prefill->launch(a, int(grid), h->prefill->smem, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
 kvc_status kvc_get_error(kvc_cache *h, void *stream) {

@@ -512,6 +512,10 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
 
     if (threadIdx.x == 0) {
+        dev::prefetch_tensormap(&a.tm_k32);
+        dev::prefetch_tensormap(&a.tm_v32);
+        dev::prefetch_tensormap(&a.tm_k8);
+        dev::prefetch_tensormap(&a.tm_v8);
         for (int s = 0; s < ns; ++s) {
             dev::mbar_init(bar0 + 8 * s, 1);
             dev::mbar_init(bar0 + 8 * (ns + s), 1);

@@ -108,6 +108,40 @@ KVC_DECLARE_DECODE_TABLE(f32, 128)
 KVC_DECLARE_DECODE_TABLE(f32, 256)
 #undef KVC_DECLARE_DECODE_TABLE
 
+// Arguments of the chunked-prefill kernel (grid constant).
+struct PrefillArgs {
+    const uint8_t *K;            // layer slab of the K cache, [B, H_kv, max_ctx, D]
+    const uint8_t *V;            // layer slab of the V cache
+    const void *q;               // [B, H, T_new, D]
+    void *out;                   // [B, H, T_new, D]
+    const int32_t *cache_index;  // [B]: row of each sequence's first chunk token
+    int32_t *err;
+    int32_t B, H_kv, max_ctx, T_new;
+    int32_t q_blocks;            // CTAs per (sequence, KV head): ceil(T_new * g / q_rows)
+    float scale_log2;            // log2(e) / sqrt(D)
+    unsigned long long timeout_ns;
+    int32_t seg_base;            // layer * B * H_kv (tensor-map segment of this layer)
+    CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;
+};
+
+// One compiled prefill kernel.
+struct PrefillKernelInfo {
+    int q_rows;  // query rows (chunk tokens x group heads) per CTA
+    int smem;    // dynamic shared memory per CTA
+    cudaError_t (*set_max_smem)(int bytes);
+    cudaError_t (*launch)(const PrefillArgs &a, int grid, int smem, cudaStream_t s);
+};
+
+// Registry of prefill kernels (16-bit caches, D = 64 or 128); nullptr for an
+// unsupported group size.
+#define KVC_DECLARE_PREFILL_TABLE(TAG, D) \
+    const PrefillKernelInfo *prefill_kernel_##TAG##_##D(int G);
+KVC_DECLARE_PREFILL_TABLE(bf16, 64)
+KVC_DECLARE_PREFILL_TABLE(bf16, 128)
+KVC_DECLARE_PREFILL_TABLE(f16, 64)
+KVC_DECLARE_PREFILL_TABLE(f16, 128)
+#undef KVC_DECLARE_PREFILL_TABLE
+
 // Tensor maps of a K and a V cache [n_segs][max_ctx][D] of 16-bit elements
 // (n_segs = L * B * H_kv): boxes of 64 columns x 32 rows and x 8 rows with the
 // 128-byte swizzle.  Host only; returns false if the driver refuses.
@@ -299,6 +333,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Bring a tensor map's descriptor close to the TMA unit before its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Order this thread's earlier generic-proxy shared-memory writes before

@@ -77,6 +77,8 @@ _lib.kvc_decode_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _vp, _vp]
 _lib.kvc_decode_attn.restype = _i32
 _lib.kvc_decode_step.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
 _lib.kvc_decode_step.restype = _i32
+_lib.kvc_prefill_attn.argtypes = [_vp, _i32, _vp, _vp, _i32, _vp, _vp]
+_lib.kvc_prefill_attn.restype = _i32
 _lib.kvc_decode_attn_static.argtypes = [_cfgp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
 _lib.kvc_decode_attn_static.restype = _i32
 _lib.kvc_get_error.argtypes = [_vp, _vp]
@@ -156,6 +158,11 @@ def kvc_decode_attn(h, layer: int, q, valid_len, max_valid_hint: int, out, strea
 def kvc_decode_step(h, layer: int, q, k_new, v_new, valid_len, max_valid_hint: int, out, stream=None) -> int:
     return _lib.kvc_decode_step(h, int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(valid_len),
                                 int(max_valid_hint), _ptr(out), _stream(stream))
+
+
+def kvc_prefill_attn(h, layer: int, q, cache_index, T_new: int, out, stream=None) -> int:
+    return _lib.kvc_prefill_attn(h, int(layer), _ptr(q), _ptr(cache_index), int(T_new), _ptr(out),
+                                 _stream(stream))
 
 
 def kvc_decode_attn_static(cfg: kvc_config, layer: int, k_base, v_base, q, valid_len,
