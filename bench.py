@@ -422,6 +422,8 @@ def bench_reference(args, rank, world, local):
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
+    if w.chunk:
+        return bench_reference_prefill(args, world, w)
     lengths = synth.live_lengths(w).numpy()
     host = cpu_host_inputs(w, lengths)
     for _ in range(args.warmup):
@@ -450,11 +452,244 @@ def bench_reference(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- chunked prefill
+PREFILL_METRIC = "chunked-prefill attention TFLOP/s"
+
+
+def prefill_work(w: synth.Workload, prefix) -> dict:
+    """Per layer: attention FLOPs (QK^T and PV, 2 FLOPs per multiply-add) of
+    the chunk's causal rows, and the algorithmic bytes (K/V rows up to the
+    chunk's end read once per KV head, q read, out written, the chunk's K/V
+    appended)."""
+    T, eb = w.chunk, synth.ELEM_BYTES[w.dtype]
+    rows = sum(T * int(c) + T * (T + 1) // 2 for c in prefix)      # (query, key) pairs per head
+    flops = 4 * w.d_head * w.n_heads * rows
+    kv = 2 * w.n_kv_heads * w.d_head * eb * sum(int(c) + T for c in prefix)
+    qo = 2 * w.batch * w.n_heads * T * w.d_head * eb
+    app = 4 * w.batch * w.n_kv_heads * T * w.d_head * eb
+    return {"flops": flops, "bytes": kv + qo + app}
+
+
+class PrefillState:
+    """Caches with the workload's live prefixes, and per layer one chunk of
+    T_new rows to append at the prefix end and attend with."""
+
+    def __init__(self, w: synth.Workload, device: int):
+        from static_kv_cache_gb300 import kvc
+        self.kvc, self.w = kvc, w
+        self.prefix = synth.live_lengths(w)
+        tdt = synth.DTYPES[w.dtype]
+        dev = torch.device("cuda", device)
+        L, B, T = w.n_layers, w.batch, w.chunk
+        shape = (L, B, w.n_kv_heads, w.max_context, w.d_head)
+        self.K = torch.empty(shape, dtype=tdt, device=dev)
+        self.V = torch.empty(shape, dtype=tdt, device=dev)
+        synth.poison_(self.K, w.dtype)
+        synth.poison_(self.V, w.dtype)
+        for layer in range(L):
+            for b in range(B):
+                n = int(self.prefix[b])
+                if n:
+                    shp = (w.n_kv_heads, n, w.d_head)
+                    self.K[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pk", layer, b), dev)
+                    self.V[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pv", layer, b), dev)
+        self.q = synth.normal((L, B, w.n_heads, T, w.d_head), w.dtype, synth.sub_seed(w.seed, "q"), dev)
+        self.k_new = synth.normal((L, B, w.n_kv_heads, T, w.d_head), w.dtype, synth.sub_seed(w.seed, "kn"), dev)
+        self.v_new = synth.normal((L, B, w.n_kv_heads, T, w.d_head), w.dtype, synth.sub_seed(w.seed, "vn"), dev)
+        self.out = torch.empty((L, B, w.n_heads, T, w.d_head), dtype=tdt, device=dev)
+        self.cache_index = self.prefix.to(dev)
+        self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
+        self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
+        st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
+        kvc.check(st, "kvc_alloc")
+        torch.cuda.synchronize(dev)
+
+    def step(self, stream, events=None, q=None, k_new=None, v_new=None, ci=None, out=None) -> int:
+        """The chunk of every layer: append at the prefix end, then the
+        prefill attention; returns the number of kernel launches."""
+        kvc, w = self.kvc, self.w
+        q = self.q if q is None else q
+        k_new = self.k_new if k_new is None else k_new
+        v_new = self.v_new if v_new is None else v_new
+        ci = self.cache_index if ci is None else ci
+        out = self.out if out is None else out
+        sp = stream.cuda_stream
+        for layer in range(w.n_layers):
+            kvc.check(kvc.kvc_append(self.h, layer, k_new[layer], v_new[layer], ci, w.chunk, sp), "kvc_append")
+            if events is not None:
+                events[layer][0].record(stream)
+            kvc.check(kvc.kvc_prefill_attn(self.h, layer, q[layer], ci, w.chunk, out[layer], sp), "kvc_prefill_attn")
+            if events is not None:
+                events[layer][1].record(stream)
+        return 2 * w.n_layers
+
+    def close(self):
+        self.kvc.kvc_free(self.h)
+
+
+def cpu_prefill_sample(w: synth.Workload, seconds: float):
+    """Time the fp64 oracle on a bounded sample of the prefill workload: each
+    sample is 8 chunk rows of one sequence of layer 0 (all heads, causal over
+    that sequence's prefix and chunk), cycling over the sequences."""
+    import oracle
+    prefix = synth.live_lengths(w)
+    T, rows_per_sample = w.chunk, 8
+    host = []
+    for b in range(w.batch):
+        c = int(prefix[b])
+        ctx = c + T
+        K = synth.normal((1, w.n_kv_heads, ctx, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu-k", b))
+        V = synth.normal((1, w.n_kv_heads, ctx, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu-v", b))
+        q = synth.normal((1, w.n_heads, rows_per_sample, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu-q", b))
+        host.append((c, synth.to_bits(q), synth.to_bits(K), synth.to_bits(V)))
+    flops, n, t0 = 0, 0, time.perf_counter()
+    while True:
+        c, q, K, V = host[n % len(host)]
+        t = T - rows_per_sample    # the last rows of the chunk: the most keys
+        oracle.prefill_attn(q, K, V, [c + t], rows_per_sample, w.dtype)
+        flops += 4 * w.d_head * w.n_heads * sum(c + t + i + 1 for i in range(rows_per_sample))
+        n += 1
+        spent = time.perf_counter() - t0
+        if spent >= seconds:
+            break
+    return flops / spent / 1e12, n, spent, oracle.num_threads()
+
+
+def bench_prefill(args, rank, world, local):
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
+    state = PrefillState(w, local)
+    work = prefill_work(w, state.prefix.numpy())
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            state.step(stream)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(w.n_layers)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = None if args.no_clocks else ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    launches = 0
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s_ in range(args.steps):
+            launches += state.step(stream, evs[s_])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    elapsed = reduce_max(t_start.elapsed_time(t_end) / 1e3, world, device=torch.device("cuda", local))
+    launch_ms = [evs[s_][l][0].elapsed_time(evs[s_][l][1]) for s_ in range(args.steps) for l in range(w.n_layers)]
+    err = state.kvc.kvc_get_error(state.h, stream.cuda_stream)
+    if err:
+        raise state.kvc.KvcError(err, "device error word after the timed region")
+    step_flops = work["flops"] * w.n_layers
+    value = world * step_flops * args.steps / elapsed / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        hq, hk, hv, hci = pin(state.q), pin(state.k_new), pin(state.v_new), pin(state.cache_index)
+        hout = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
+        dq, dk, dv, dci = (torch.empty_like(x) for x in (state.q, state.k_new, state.v_new, state.cache_index))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hci))
+        d2h = hout.numel() * hout.element_size()
+        e2e_steps = max(3, min(args.steps, 50))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(e2e_steps):
+                for d, hsrc in ((dq, hq), (dk, hk), (dv, hv), (dci, hci)):
+                    d.copy_(hsrc, non_blocking=True)
+                state.step(stream, q=dq, k_new=dk, v_new=dv, ci=dci)
+                hout.copy_(state.out, non_blocking=True)
+                stream.synchronize()
+        e2e_s = reduce_max(time.perf_counter() - t0, world, device=torch.device("cuda", local))
+        e2e = {"value": round(world * step_flops * e2e_steps / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        tf, n, spent, threads = cpu_prefill_sample(w, args.cpu_seconds)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle prefill attention of layer 0, the last 8 chunk rows of one sequence "
+                         f"(all {w.n_heads} heads) per sample, cycling over the batch: {n} samples in {spent:.1f} s"}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_src = float(pk["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained)"
+    except (OSError, KeyError, ValueError):
+        peak, peak_src = 1700.0, "fallback 1.7 PFLOP/s sustained bf16"
+    mean_launch_s = float(np.mean(launch_ms)) / 1e3
+    achieved = work["flops"] / mean_launch_s / 1e12
+    if rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.n_layers} layers, B={w.batch}, H={w.n_heads}, H_kv={w.n_kv_heads}, "
+                                   f"d_h={w.d_head}, chunk T_new={w.chunk} after live prefixes U{w.ragged}, {w.dtype} cache",
+                       "prefix_rows": [int(x) for x in state.prefix], "chunk": w.chunk,
+                       "parallelism": f"replicas x{world}"},
+            "prefill_tokens_per_s": round(world * w.batch * w.chunk / (elapsed / args.steps), 1),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel",
+                         "peak_source": peak_src, "flops_per_launch": work["flops"],
+                         "bytes_per_launch": work["bytes"],
+                         "mean_launch_us": round(mean_launch_s * 1e6, 3)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    state.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_reference_prefill(args, world, w):
+    """The oracle's prefill attention on the host cores: each step one
+    bounded sample (see cpu_prefill_sample) of about a second."""
+    import oracle
+    for _ in range(args.warmup):
+        cpu_prefill_sample(w, 0.0)
+    total_flops, total_s, samples = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        tf, n, spent, _ = cpu_prefill_sample(w, 1.0)
+        total_flops += tf * 1e12 * spent
+        total_s += spent
+        samples += n
+    value = total_flops / total_s / 1e12
+    sample = (f"fp64 oracle prefill attention of layer 0, the last 8 chunk rows of one sequence "
+              f"(all {w.n_heads} heads) per sample, cycling over the batch; {samples} samples in {total_s:.1f} s")
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_s / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "chunk": w.chunk},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         bench_reference(args, rank, world, local)
+    elif synth.WORKLOADS[args.workload].chunk:
+        bench_prefill(args, rank, world, local)
     else:
         bench_kvc(args, rank, world, local)
 

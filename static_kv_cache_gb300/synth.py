@@ -49,6 +49,7 @@ class Workload:
     ragged: tuple[int, int] | None = None
     first_append: int = 0
     seed: int = 1000
+    chunk: int = 0          # chunked prefill: T_new of the chunk appended after the live rows
 
     @property
     def group(self) -> int:
@@ -82,6 +83,10 @@ WORKLOADS = {
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1014),
+    # Chunked prefill on the Llama-3-8B-shaped cache: 4 sequences with live
+    # prefixes U{0..4096}, a 512-token chunk each (appended, then attended).
+    "llama3_8b_prefill": Workload("llama3_8b_prefill", 32, 4, 32, 8, 128, 8192, "bf16", steps=1,
+                                  ragged=(0, 4096), seed=1020, chunk=512),
 }
 
 
