@@ -14,6 +14,9 @@ Contents
                          Optimization...", section #2, Before/After).
 * ``causal_attention``-- uncached full causal attention ("KV-Cache
                          Mechanics", Disabling the Cache).
+* ``quantize_rows``   -- the int8 cache: symmetric per-row codes and fp32
+                         scales ("10.3", section 4.4), and the dequantised
+                         rows the attention reads.
 * ``prefill_attn``    -- chunked-prefill attention: each chunk query row
                          attends over the rows up to its own position
                          ("10.3", section 3; "KV-Cache Mechanics", AR
@@ -33,13 +36,15 @@ from .cache import ListAppendCache
 from .causal import causal_attention, widen
 from .formula import kv_bytes_per_token, kv_cache_bytes, mla_cache_bytes
 from .prefill import prefill_attn
+from .quant import dequantize_rows, quantize_rows
 
-__all__ = ["decode_attn", "prefill_attn", "ListAppendCache", "causal_attention", "widen",
+__all__ = ["decode_attn", "prefill_attn", "quantize_rows", "dequantize_rows", "ListAppendCache",
+           "causal_attention", "widen",
            "kv_cache_bytes", "kv_bytes_per_token", "mla_cache_bytes",
            "load_library", "num_threads", "set_num_threads", "DTYPE_CODES"]
 
-DTYPE_CODES = {"bf16": 0, "fp32": 1, "fp16": 2}
-_STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32}
+DTYPE_CODES = {"bf16": 0, "fp32": 1, "fp16": 2, "fp64": 3}
+_STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32, "fp64": np.float64}
 
 _lib = None
 

@@ -25,7 +25,8 @@
  *   the KV heads produces).
  *
  * Evaluation: every stored element is widened exactly to double (bf16,
- * fp16 and fp32 are all exact in double).  For each (b, h):
+ * fp16 and fp32 are all exact in double; fp64 inputs -- the dequantised rows
+ * of an int8 cache, code * scale, exact in double -- are taken as they are).  For each (b, h):
  *     s_j = (sum_d q[b,h,d] * K[b,k,j,d]) / sqrt(d_h)      for j < valid_b
  *     m   = max_j s_j
  *     w_j = exp(s_j - m)
@@ -51,7 +52,7 @@
 #include <omp.h>
 #endif
 
-enum { KVO_BF16 = 0, KVO_FP32 = 1, KVO_FP16 = 2 };
+enum { KVO_BF16 = 0, KVO_FP32 = 1, KVO_FP16 = 2, KVO_FP64 = 3 };
 
 enum {
     KVO_OK = 0,
@@ -91,6 +92,7 @@ static double load_elem(const void *base, int64_t idx, int dtype)
     switch (dtype) {
     case KVO_BF16: return bf16_to_double(((const uint16_t *)base)[idx]);
     case KVO_FP16: return fp16_to_double(((const uint16_t *)base)[idx]);
+    case KVO_FP64: return ((const double *)base)[idx];
     default:       return (double)((const float *)base)[idx];
     }
 }
@@ -134,7 +136,7 @@ int kvo_decode_attn(const void *q, const void *K, const void *V,
     if (!q || !K || !V || !valid_len || !out) return KVO_ERR_ARG;
     if (B < 1 || H < 1 || H_kv < 1 || d_h < 1 || ctx_stride < 1) return KVO_ERR_ARG;
     if (H % H_kv != 0) return KVO_ERR_ARG;
-    if (dtype != KVO_BF16 && dtype != KVO_FP32 && dtype != KVO_FP16) return KVO_ERR_ARG;
+    if (dtype != KVO_BF16 && dtype != KVO_FP32 && dtype != KVO_FP16 && dtype != KVO_FP64) return KVO_ERR_ARG;
     for (int32_t b = 0; b < B; ++b)
         if (valid_len[b] < 1 || valid_len[b] > ctx_stride) return KVO_ERR_LENGTH;
 
