@@ -49,6 +49,8 @@ def decode_kernel_name(w: synth.Workload) -> str:
     """The decode kernel the library picks for a workload: the tensor-core
     kernel for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128,
     the CUDA-core kernel otherwise."""
+    if w.dtype == "int8":
+        return "decode_q8_kernel"
     if w.dtype in ("bf16", "fp16") and 2 <= w.group <= 8 and w.d_head in (64, 128):
         return "decode_mma_kernel"
     return "decode_split_kernel"
@@ -194,11 +196,15 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- workload
 def step_bytes(w: synth.Workload, lengths) -> dict:
-    """Algorithmic bytes of one layer's decode step (per launch)."""
+    """Algorithmic bytes of one layer's decode step (per launch).  An int8
+    cache adds its 4-byte row scales to the rows read and written; its q,
+    out and new rows are bf16."""
     eb = synth.ELEM_BYTES[w.dtype]
+    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
+    sb = 4 if w.dtype == "int8" else 0                          # scale bytes per cache row
     live = int(np.asarray(lengths, dtype=np.int64).sum())
-    attn = 2 * w.n_kv_heads * w.d_head * eb * live + 2 * w.batch * w.n_heads * w.d_head * eb
-    append = 4 * w.batch * w.n_kv_heads * w.d_head * eb          # read k/v_new, write the rows
+    attn = 2 * w.n_kv_heads * (w.d_head * eb + sb) * live + 2 * w.batch * w.n_heads * w.d_head * ab
+    append = 2 * w.batch * w.n_kv_heads * (w.d_head * ab + w.d_head * eb + sb)  # read k/v_new, write the rows
     return {"attn": attn, "append": append}
 
 
@@ -211,32 +217,52 @@ class DeviceState:
         self.w = w
         self.lengths = synth.live_lengths(w)
         self.maxlen = int(self.lengths.max())
-        tdt = synth.DTYPES[w.dtype]
+        act = synth.ACT_DTYPE[w.dtype]
+        tdt, adt = synth.DTYPES[w.dtype], synth.DTYPES[act]
         dev = torch.device("cuda", device)
         shape = (w.n_layers, w.batch, w.n_kv_heads, w.max_context, w.d_head)
         self.K = torch.empty(shape, dtype=tdt, device=dev)
         self.V = torch.empty(shape, dtype=tdt, device=dev)
-        synth.poison_(self.K, w.dtype)
-        synth.poison_(self.V, w.dtype)
+        self.KS = self.VS = None
         pre = (self.lengths - 1).tolist()
-        for layer in range(w.n_layers):
-            for b in range(w.batch):
-                n = pre[b]
-                if n:
-                    shp = (w.n_kv_heads, n, w.d_head)
-                    self.K[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pk", layer, b), dev)
-                    self.V[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pv", layer, b), dev)
+        if w.dtype == "int8":
+            # codes uniform on [-127, 127], scales positive: synthetic rows as the
+            # quantising append would leave them; scales past the live rows NaN
+            self.KS = torch.full(shape[:-1], float("nan"), dtype=torch.float32, device=dev)
+            self.VS = torch.full(shape[:-1], float("nan"), dtype=torch.float32, device=dev)
+            g = synth.generator(synth.sub_seed(w.seed, "codes"), device=dev)
+            self.K.copy_(torch.randint(-127, 128, shape, generator=g, device=dev, dtype=torch.int8))
+            self.V.copy_(torch.randint(-127, 128, shape, generator=g, device=dev, dtype=torch.int8))
+            for layer in range(w.n_layers):
+                for b in range(w.batch):
+                    n = pre[b]
+                    if n:
+                        self.KS[layer, b, :, :n] = torch.rand((w.n_kv_heads, n), generator=g, device=dev) * 0.03 + 0.002
+                        self.VS[layer, b, :, :n] = torch.rand((w.n_kv_heads, n), generator=g, device=dev) * 0.03 + 0.002
+        else:
+            synth.poison_(self.K, w.dtype)
+            synth.poison_(self.V, w.dtype)
+            for layer in range(w.n_layers):
+                for b in range(w.batch):
+                    n = pre[b]
+                    if n:
+                        shp = (w.n_kv_heads, n, w.d_head)
+                        self.K[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pk", layer, b), dev)
+                        self.V[layer, b, :, :n] = synth.normal(shp, w.dtype, synth.sub_seed(w.seed, "pv", layer, b), dev)
         L, B = w.n_layers, w.batch
-        self.q = synth.normal((L, B, w.n_heads, w.d_head), w.dtype, synth.sub_seed(w.seed, "q"), dev)
-        self.k_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "kn"), dev)
-        self.v_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), w.dtype, synth.sub_seed(w.seed, "vn"), dev)
-        self.out = torch.empty((L, B, w.n_heads, w.d_head), dtype=tdt, device=dev)
+        self.q = synth.normal((L, B, w.n_heads, w.d_head), act, synth.sub_seed(w.seed, "q"), dev)
+        self.k_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), act, synth.sub_seed(w.seed, "kn"), dev)
+        self.v_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), act, synth.sub_seed(w.seed, "vn"), dev)
+        self.out = torch.empty((L, B, w.n_heads, w.d_head), dtype=adt, device=dev)
         self.valid_len = self.lengths.to(dev)
         # the step is one fused launch on the tensor-core kernel, else append + attention
         self.launches_per_layer = 1 if decode_kernel_name(w) == "decode_mma_kernel" else 2
         self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
         self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
-        st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
+        if w.dtype == "int8":
+            st, self.h = kvc.kvc_alloc_scaled(self.cfg, self.K, self.V, self.KS, self.VS, self.ws, self.ws.numel())
+        else:
+            st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
         kvc.check(st, "kvc_alloc")
         torch.cuda.synchronize(dev)
 
@@ -276,26 +302,43 @@ def cpu_oracle_sample(w: synth.Workload, seconds: float, host=None):
     if host is None:
         host = cpu_host_inputs(w, lengths)
     Kh, Vh, qh = host
-    eb = synth.ELEM_BYTES[w.dtype]
+    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     done_bytes, spent, n = 0, 0.0, 0
     while spent < seconds or n == 0:
         b = n % w.batch
         t0 = time.perf_counter()
-        oracle.decode_attn(qh[b:b + 1], Kh[b:b + 1], Vh[b:b + 1], lengths[b:b + 1], w.dtype)
+        oracle.decode_attn(qh[b:b + 1], Kh[b:b + 1], Vh[b:b + 1], lengths[b:b + 1], oracle_dtype(w))
         spent += time.perf_counter() - t0
-        done_bytes += 2 * w.n_kv_heads * w.d_head * eb * int(lengths[b]) + 2 * w.n_heads * w.d_head * eb
+        done_bytes += 2 * w.n_kv_heads * cache_row_bytes(w) * int(lengths[b]) + 2 * w.n_heads * w.d_head * ab
         n += 1
     return done_bytes / spent / 1e9, n, spent, oracle.num_threads()
 
 
 def cpu_host_inputs(w: synth.Workload, lengths):
-    """Layer-0 inputs drawn on the host (same distribution and shapes)."""
+    """Layer-0 inputs drawn on the host (same distribution and shapes).  For
+    an int8 cache: rows quantised by the oracle and handed to it
+    dequantised (fp64), q widened to fp64."""
     maxlen = int(np.max(lengths))
     shape = (w.batch, w.n_kv_heads, maxlen, w.d_head)
-    Kh = synth.to_bits(synth.normal(shape, w.dtype, synth.sub_seed(w.seed, "cpu_k"))).copy()
-    Vh = synth.to_bits(synth.normal(shape, w.dtype, synth.sub_seed(w.seed, "cpu_v"))).copy()
-    qh = synth.to_bits(synth.normal((w.batch, w.n_heads, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu_q")))
+    act = synth.ACT_DTYPE[w.dtype]
+    Kh = synth.to_bits(synth.normal(shape, act, synth.sub_seed(w.seed, "cpu_k"))).copy()
+    Vh = synth.to_bits(synth.normal(shape, act, synth.sub_seed(w.seed, "cpu_v"))).copy()
+    qh = synth.to_bits(synth.normal((w.batch, w.n_heads, w.d_head), act, synth.sub_seed(w.seed, "cpu_q")))
+    if w.dtype == "int8":
+        import oracle
+        Kh = oracle.dequantize_rows(*oracle.quantize_rows(Kh, act))
+        Vh = oracle.dequantize_rows(*oracle.quantize_rows(Vh, act))
+        qh = oracle.widen(qh, act)
     return Kh, Vh, qh
+
+
+def oracle_dtype(w: synth.Workload) -> str:
+    return "fp64" if w.dtype == "int8" else w.dtype
+
+
+def cache_row_bytes(w: synth.Workload) -> int:
+    """Bytes of one cache row as stored (codes plus the scale for int8)."""
+    return w.d_head * synth.ELEM_BYTES[w.dtype] + (4 if w.dtype == "int8" else 0)
 
 
 def workload_config(w: synth.Workload, lengths, world: int) -> dict:
@@ -430,13 +473,13 @@ def bench_reference(args, rank, world, local):
         cpu_oracle_sample(w, 0.0, host)
     import oracle
     total_bytes, total_s, samples = 0.0, 0.0, 0
-    eb = synth.ELEM_BYTES[w.dtype]
+    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     for s in range(args.steps):
         b = s % w.batch
         t0 = time.perf_counter()
-        oracle.decode_attn(host[2][b:b + 1], host[0][b:b + 1], host[1][b:b + 1], lengths[b:b + 1], w.dtype)
+        oracle.decode_attn(host[2][b:b + 1], host[0][b:b + 1], host[1][b:b + 1], lengths[b:b + 1], oracle_dtype(w))
         total_s += time.perf_counter() - t0
-        total_bytes += 2 * w.n_kv_heads * w.d_head * eb * int(lengths[b]) + 2 * w.n_heads * w.d_head * eb
+        total_bytes += 2 * w.n_kv_heads * cache_row_bytes(w) * int(lengths[b]) + 2 * w.n_heads * w.d_head * ab
         samples += 1
     value = total_bytes / total_s / 1e9
     sample = (f"fp64 oracle decode attention of layer 0, one sequence (all {w.n_heads} heads) per step, "

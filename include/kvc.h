@@ -74,7 +74,15 @@ typedef enum {
 
 /* Element type of the cache, of q / k_new / v_new, and of the output.
  * Bytes per element p: bf16 2, fp32 4, fp16 2 ("10.3", section 2). */
-typedef enum { KVC_BF16 = 0, KVC_FP32 = 1, KVC_FP16 = 2 } kvc_dtype;
+/* KVC_INT8: an int8 cache ("10.3", section 4.4: the cache stored as int8,
+ * p = 1 byte per element) with one fp32 scale per cache row (one token of
+ * one KV head), held in two caller-owned scale arrays bound by
+ * kvc_alloc_scaled.  A row of d_h values x is stored as
+ * code = rint(x * (127 / absmax)) in [-127, 127] with scale = absmax / 127
+ * (fp32 arithmetic, round half to even; scale 0 for a row of zeros), and the
+ * attention reads code * scale.  The activations of such a cache -- q, out,
+ * k_new, v_new -- are bf16.  Built for d_h = 128. */
+typedef enum { KVC_BF16 = 0, KVC_FP32 = 1, KVC_FP16 = 2, KVC_INT8 = 3 } kvc_dtype;
 
 /* Model shape of one static cache.
  *   n_layers     L, number of per-layer caches held in one allocation
@@ -126,6 +134,12 @@ uint64_t kvc_bytes_per_token(const kvc_config *cfg);
  * 0 if cfg is invalid. */
 uint64_t kvc_workspace_bytes(const kvc_config *cfg);
 
+/* Bytes of ONE of the two scale arrays of an int8 cache: one fp32 per row,
+ * n_layers * batch * n_kv_heads * max_context * 4, laid out [L, B, H_kv,
+ * T_max].  0 for other cache types or an invalid cfg.  (The cache-size
+ * formula, kvc_cache_bytes, counts the codes only, as the pages do.) */
+uint64_t kvc_scale_bytes(const kvc_config *cfg);
+
 /* ---- handle -------------------------------------------------------------- */
 
 /* Bind caller-owned device buffers to a new handle.
@@ -139,6 +153,15 @@ uint64_t kvc_workspace_bytes(const kvc_config *cfg);
  *   out             host; receives the handle on KVC_OK, untouched otherwise.
  * Uses the current CUDA device; later calls must run with it current.
  * Returns KVC_ERR_INVALID / _UNSUPPORTED / _ALIGNMENT / _WORKSPACE / _CUDA. */
+/* kvc_alloc for int8 caches (cfg->dtype == KVC_INT8): k_base and v_base
+ * hold the codes (one byte per element, same layout as above) and k_scale,
+ * v_scale (device, kvc_scale_bytes(cfg) each, 16-byte aligned) the per-row
+ * fp32 scales.  The other arguments, and the errors, are kvc_alloc's;
+ * KVC_ERR_INVALID for another dtype or a missing scale array.  kvc_alloc
+ * itself refuses KVC_INT8 (KVC_ERR_INVALID). */
+kvc_status kvc_alloc_scaled(const kvc_config *cfg, void *k_base, void *v_base, void *k_scale,
+                            void *v_scale, void *workspace, uint64_t ws_bytes, kvc_cache **out);
+
 kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base,
                      void *workspace, uint64_t ws_bytes, kvc_cache **out);
 
@@ -165,6 +188,8 @@ kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n);
  *                cache_index[b] < 0 or cache_index[b] + T_new > max_context is
  *                skipped and KVC_ERR_DEVICE_INDEX is recorded.
  *   T_new        rows per sequence, 0 <= T_new <= max_context (0: no-op)
+ * For an int8 cache k_new / v_new are bf16 and each row is quantised as it
+ * is written (codes and the row's scale; see KVC_INT8).
  * Host errors: KVC_ERR_INVALID, KVC_ERR_CAPACITY (T_new > max_context),
  * KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
 kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new,

@@ -44,6 +44,7 @@ def _units():
         for d in HEAD_DIMS:
             obj = os.path.join(BUILD, f"kvc_decode_{tag}_{d}.o")
             units.append((inst, obj, [f"-DKVC_INST_TYPE={code}", f"-DKVC_INST_D={d}"]))
+    units.append((os.path.join(CSRC, "kvc_decode_q8_inst.cu"), os.path.join(BUILD, "kvc_decode_q8_128.o"), []))
     pre = os.path.join(CSRC, "kvc_prefill_inst.cu")
     for code, tag in ((0, "bf16"), (1, "f16")):
         for d in (64, 128):

@@ -21,6 +21,8 @@ struct kvc_cache {
     int num_splits;          // 0: automatic
     uint8_t *k_base;
     uint8_t *v_base;
+    uint8_t *k_scale;        // int8 caches: per-row fp32 scales [L, B, H_kv, T_max]; else null
+    uint8_t *v_scale;
     uint8_t *ws;
     uint64_t ws_bytes;
     kvc::WorkspaceLayout wl;
@@ -38,6 +40,7 @@ int elem_bytes_of(int32_t dtype) {
         case KVC_BF16: return 2;
         case KVC_FP16: return 2;
         case KVC_FP32: return 4;
+        case KVC_INT8: return 1;
         default: return 0;
     }
 }
@@ -60,6 +63,8 @@ const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
             KVC_PICK(f16, 32) KVC_PICK(f16, 64) KVC_PICK(f16, 128) KVC_PICK(f16, 256) break;
         case KVC_FP32:
             KVC_PICK(f32, 32) KVC_PICK(f32, 64) KVC_PICK(f32, 128) KVC_PICK(f32, 256) break;
+        case KVC_INT8:
+            KVC_PICK(q8, 128) break;
         default: break;
     }
 #undef KVC_PICK
@@ -81,6 +86,11 @@ const kvc::PrefillKernelInfo *find_prefill(const kvc_config *c) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t layer_scale_bytes(const kvc_cache *h) {
+    const kvc_config &c = h->cfg;
+    return uint64_t(c.batch) * c.n_kv_heads * uint64_t(c.max_context) * 4;
+}
 
 uint64_t layer_slab_bytes(const kvc_cache *h) {
     const kvc_config &c = h->cfg;
@@ -108,15 +118,20 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
                             CUtensorMap *v8) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
-    const CUtensorMapDataType dt =
-        dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // 16-bit caches: boxes of 64 elements (128 bytes) per row; int8 codes:
+    // 128 elements (128 bytes).
+    const bool q8 = dtype == KVC_INT8;
+    const int eb = q8 ? 1 : 2;
+    const CUtensorMapDataType dt = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
-    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(max_ctx) * D * 2};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
     const cuuint32_t elem[3] = {1, 1, 1};
     struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
     const Job jobs[4] = {{k_base, 32, k32}, {k_base, 8, k8}, {v_base, 32, v32}, {v_base, 8, v8}};
     for (const Job &j : jobs) {
-        const cuuint32_t box[3] = {64, j.rows, 1};
+        const cuuint32_t box[3] = {cuuint32_t(128 / eb), j.rows, 1};
         if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -167,9 +182,19 @@ uint64_t kvc_workspace_bytes(const kvc_config *c) {
     return kvc::workspace_layout(c->batch, c->n_kv_heads, c->n_heads / c->n_kv_heads, c->d_head).total;
 }
 
-kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *workspace,
-                     uint64_t ws_bytes, kvc_cache **out) {
+uint64_t kvc_scale_bytes(const kvc_config *c) {
+    if (!shape_ok(c) || c->dtype != KVC_INT8) return 0;
+    return uint64_t(c->n_layers) * uint64_t(c->batch) * uint64_t(c->n_kv_heads) * uint64_t(c->max_context) * 4;
+}
+
+}  // extern "C"
+
+namespace {
+
+kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k_scale, void *v_scale,
+                      void *workspace, uint64_t ws_bytes, kvc_cache **out) {
     if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
+    if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
     const kvc::DecodeKernelInfo *info = find_decode(cfg);
     if (!info) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
@@ -210,6 +235,8 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
     h->num_splits = 0;
     h->k_base = static_cast<uint8_t *>(k_base);
     h->v_base = static_cast<uint8_t *>(v_base);
+    h->k_scale = static_cast<uint8_t *>(k_scale);
+    h->v_scale = static_cast<uint8_t *>(v_scale);
     h->ws = static_cast<uint8_t *>(workspace);
     h->ws_bytes = ws_bytes;
     h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads, h->group, cfg->d_head);
@@ -228,6 +255,22 @@ kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *wo
     return KVC_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base, void *workspace,
+                     uint64_t ws_bytes, kvc_cache **out) {
+    if (cfg && cfg->dtype == KVC_INT8) return KVC_ERR_INVALID;  // needs its scale arrays
+    return alloc_impl(cfg, k_base, v_base, nullptr, nullptr, workspace, ws_bytes, out);
+}
+
+kvc_status kvc_alloc_scaled(const kvc_config *cfg, void *k_base, void *v_base, void *k_scale, void *v_scale,
+                            void *workspace, uint64_t ws_bytes, kvc_cache **out) {
+    if (!cfg || cfg->dtype != KVC_INT8 || !k_scale || !v_scale) return KVC_ERR_INVALID;
+    return alloc_impl(cfg, k_base, v_base, k_scale, v_scale, workspace, ws_bytes, out);
+}
+
 void kvc_free(kvc_cache *h) { delete h; }
 
 kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n) {
@@ -244,6 +287,16 @@ kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void
     if (T_new > h->cfg.max_context) return KVC_ERR_CAPACITY;
     if (!aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
     const uint64_t slab = layer_slab_bytes(h);
+    if (h->cfg.dtype == KVC_INT8) {
+        const uint64_t ss = layer_scale_bytes(h);
+        const cudaError_t e = kvc::launch_append_q8(
+            h->k_base + slab * layer, h->v_base + slab * layer, reinterpret_cast<float *>(h->k_scale + ss * layer),
+            reinterpret_cast<float *>(h->v_scale + ss * layer), static_cast<const uint8_t *>(k_new),
+            static_cast<const uint8_t *>(v_new), cache_index, 0, h->cfg.batch, h->cfg.n_kv_heads, T_new,
+            h->cfg.max_context, h->cfg.d_head, reinterpret_cast<int32_t *>(h->ws), h->num_sms,
+            static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+    }
     const cudaError_t e = kvc::launch_append(
         h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
         static_cast<const uint8_t *>(v_new), cache_index, 0, h->cfg.batch, h->cfg.n_kv_heads, T_new,
@@ -285,6 +338,8 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
     a.out = out;
     a.k_new = static_cast<const uint8_t *>(k_new);
     a.v_new = static_cast<const uint8_t *>(v_new);
+    a.k_scale = h->k_scale ? reinterpret_cast<const float *>(h->k_scale + layer_scale_bytes(h) * layer) : nullptr;
+    a.v_scale = h->v_scale ? reinterpret_cast<const float *>(h->v_scale + layer_scale_bytes(h) * layer) : nullptr;
     a.valid_len = valid_len;
     a.part_ml = reinterpret_cast<float *>(h->ws + h->wl.part_ml);
     a.part_acc = reinterpret_cast<float *>(h->ws + h->wl.part_acc);
@@ -327,10 +382,21 @@ kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q, const voi
         return KVC_ERR_INVALID;
     if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
+    const uint64_t slab = layer_slab_bytes(h);
+    if (h->cfg.dtype == KVC_INT8) {  // the quantising append, then the attention
+        const uint64_t ss = layer_scale_bytes(h);
+        const cudaError_t e = kvc::launch_append_q8(
+            h->k_base + slab * layer, h->v_base + slab * layer, reinterpret_cast<float *>(h->k_scale + ss * layer),
+            reinterpret_cast<float *>(h->v_scale + ss * layer), static_cast<const uint8_t *>(k_new),
+            static_cast<const uint8_t *>(v_new), valid_len, -1, h->cfg.batch, h->cfg.n_kv_heads, 1,
+            h->cfg.max_context, h->cfg.d_head, reinterpret_cast<int32_t *>(h->ws), h->num_sms,
+            static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return KVC_ERR_CUDA;
+        return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
+    }
     if (h->decode->tensor_maps)  // one launch: the kernel appends as it streams
         return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, k_new, v_new);
     // the CUDA-core kernel: the append, then the attention, on the same stream
-    const uint64_t slab = layer_slab_bytes(h);
     const cudaError_t e = kvc::launch_append(
         h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
         static_cast<const uint8_t *>(v_new), valid_len, -1, h->cfg.batch, h->cfg.n_kv_heads, 1,

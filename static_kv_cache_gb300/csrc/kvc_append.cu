@@ -12,6 +12,8 @@
 // a set of contiguous copies.  One thread moves one 16-byte vector;
 // consecutive threads move consecutive vectors of a run (coalesced on both
 // sides).  K and V are handled by the same launch.
+#include <cuda_bf16.h>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -42,6 +44,84 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
                      (seg * max_ctx + ci) * int64_t(row_vecs) + off;
         *dst = __ldg(src);
     }
+}
+
+// int8 cache ("10.3", section 4.4: the cache stored as int8, p = 1): each
+// appended row of d_h bf16 elements is quantised symmetrically with one fp32
+// scale, scale = absmax / 127 and code = rint(x * (127 / absmax)) in fp32
+// (IEEE division and product, round half to even); a row of zeros gets
+// scale 0.  One warp per (row, K or V): lane l holds elements
+// [l * D/32, (l + 1) * D/32).
+template <int D>
+__global__ void __launch_bounds__(256) append_q8_kernel(uint8_t *__restrict__ K, uint8_t *__restrict__ V,
+                                                        float *__restrict__ ks, float *__restrict__ vs,
+                                                        const uint8_t *__restrict__ k_new,
+                                                        const uint8_t *__restrict__ v_new,
+                                                        const int32_t *__restrict__ cache_index,
+                                                        int index_offset, int B, int H_kv, int T_new, int max_ctx,
+                                                        int32_t *err) {
+    constexpr int EPL = D / 32;  // bf16 elements per lane (2 or 4)
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = int64_t(B) * H_kv * T_new;       // rows per tensor
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t wi = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); wi < 2 * rows; wi += warps) {
+        const bool is_v = wi >= rows;
+        const int64_t r = is_v ? wi - rows : wi;              // (b * H_kv + j) * T_new + t
+        const int64_t seg = r / T_new;
+        const int t = int(r - seg * T_new);
+        const int b = int(seg / H_kv);
+        const int ci = __ldg(cache_index + b) + index_offset;
+        if (ci < 0 || ci > max_ctx - T_new) {
+            if (lane == 0 && t == 0 && seg % H_kv == 0 && !is_v) atomicCAS(err, 0, ERR_DEVICE_INDEX);
+            continue;
+        }
+        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(is_v ? v_new : k_new) + r * D + lane * EPL;
+        float x[EPL];
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            x[e] = __bfloat162float(src[e]);
+            am = fmaxf(am, fabsf(x[e]));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float scale = am / 127.0f;
+        const float inv = am > 0.f ? 127.0f / am : 0.f;
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            int c = __float2int_rn(x[e] * inv);
+            c = c > 127 ? 127 : (c < -127 ? -127 : c);
+            packed |= (uint32_t(c) & 0xffu) << (8 * e);
+        }
+        const int64_t row = seg * max_ctx + ci + t;          // cache row within the layer
+        uint8_t *dst = (is_v ? V : K) + row * D + lane * EPL;
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint32_t *>(dst) = packed;
+        else
+            *reinterpret_cast<uint16_t *>(dst) = uint16_t(packed);
+        if (lane == 0) (is_v ? vs : ks)[row] = scale;
+    }
+}
+
+cudaError_t launch_append_q8(uint8_t *K_layer, uint8_t *V_layer, float *ks_layer, float *vs_layer,
+                             const uint8_t *k_new, const uint8_t *v_new, const int32_t *cache_index,
+                             int index_offset, int B, int H_kv, int T_new, int max_ctx, int D, int32_t *err,
+                             int num_sms, cudaStream_t stream) {
+    const int64_t warps = 2 * int64_t(B) * H_kv * T_new;
+    if (warps == 0) return cudaSuccess;
+    const int64_t want = (warps + 7) / 8;                   // 8 warps per 256-thread block
+    const int64_t cap = int64_t(num_sms) * 8;
+    const int grid = int(want < cap ? want : cap);
+    if (D == 128)
+        append_q8_kernel<128><<<grid, 256, 0, stream>>>(K_layer, V_layer, ks_layer, vs_layer, k_new, v_new,
+                                                        cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
+    else if (D == 64)
+        append_q8_kernel<64><<<grid, 256, 0, stream>>>(K_layer, V_layer, ks_layer, vs_layer, k_new, v_new,
+                                                       cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,

@@ -62,6 +62,9 @@ struct DecodeArgs {
     // this launch appends at valid_len - 1 and attends with; null otherwise.
     const uint8_t *k_new;
     const uint8_t *v_new;
+    // int8 caches: one fp32 scale per cache row, [B, H_kv, max_ctx] per layer
+    const float *k_scale;
+    const float *v_scale;
     const int32_t *valid_len;  // [B]
     float *part_ml;
     float *part_acc;
@@ -106,6 +109,7 @@ KVC_DECLARE_DECODE_TABLE(f32, 32)
 KVC_DECLARE_DECODE_TABLE(f32, 64)
 KVC_DECLARE_DECODE_TABLE(f32, 128)
 KVC_DECLARE_DECODE_TABLE(f32, 256)
+KVC_DECLARE_DECODE_TABLE(q8, 128)
 #undef KVC_DECLARE_DECODE_TABLE
 
 // Arguments of the chunked-prefill kernel (grid constant).
@@ -148,6 +152,13 @@ KVC_DECLARE_PREFILL_TABLE(f16, 128)
 bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
                        CUtensorMap *v8);
+
+// Quantising append for int8 caches (kvc_append.cu): bf16 rows -> one fp32
+// scale per row and int8 codes, written at cache_index[b] + index_offset.
+cudaError_t launch_append_q8(uint8_t *K_layer, uint8_t *V_layer, float *ks_layer, float *vs_layer,
+                             const uint8_t *k_new, const uint8_t *v_new, const int32_t *cache_index,
+                             int index_offset, int B, int H_kv, int T_new, int max_ctx, int D, int32_t *err,
+                             int num_sms, cudaStream_t stream);
 
 // Append launcher (kvc_append.cu): rows go to cache_index[b] + index_offset.
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
@@ -223,6 +234,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // issuing thread's cp.async group.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // Arrive on `bar` once this thread's earlier cp.async copies have landed; the

@@ -123,6 +123,7 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
                                              const int32_t *valid_len, int32_t max_valid_hint,
                                              void *out, void *stream) {
     if (!cfg || !k_base || !v_base || !q || !valid_len || !out) return KVC_ERR_INVALID;
+    if (cfg->dtype == KVC_INT8) return KVC_ERR_UNSUPPORTED;  // no scale arrays on this call
     const int eb = elem_bytes(cfg->dtype);
     if (eb == 0 || cfg->n_layers <= 0 || cfg->batch <= 0 || cfg->n_heads <= 0 || cfg->n_kv_heads <= 0 ||
         cfg->d_head <= 0 || cfg->max_context <= 0 || cfg->n_heads % cfg->n_kv_heads != 0)

@@ -28,7 +28,8 @@ KVC_ERR_ALIGNMENT = 8
 KVC_BF16 = 0
 KVC_FP32 = 1
 KVC_FP16 = 2
-DTYPE_CODES = {"bf16": KVC_BF16, "fp32": KVC_FP32, "fp16": KVC_FP16}
+KVC_INT8 = 3
+DTYPE_CODES = {"bf16": KVC_BF16, "fp32": KVC_FP32, "fp16": KVC_FP16, "int8": KVC_INT8}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -62,11 +63,13 @@ _lib.kvc_status_str.argtypes = [_i32]
 _lib.kvc_status_str.restype = ctypes.c_char_p
 _lib.kvc_check_config.argtypes = [_cfgp]
 _lib.kvc_check_config.restype = _i32
-for _n in ("kvc_cache_bytes", "kvc_bytes_per_token", "kvc_workspace_bytes"):
+for _n in ("kvc_cache_bytes", "kvc_bytes_per_token", "kvc_workspace_bytes", "kvc_scale_bytes"):
     getattr(_lib, _n).argtypes = [_cfgp]
     getattr(_lib, _n).restype = _u64
 _lib.kvc_alloc.argtypes = [_cfgp, _vp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
 _lib.kvc_alloc.restype = _i32
+_lib.kvc_alloc_scaled.argtypes = [_cfgp, _vp, _vp, _vp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
+_lib.kvc_alloc_scaled.restype = _i32
 _lib.kvc_free.argtypes = [_vp]
 _lib.kvc_free.restype = None
 _lib.kvc_set_num_splits.argtypes = [_vp, _i32]
@@ -134,6 +137,17 @@ def kvc_alloc(cfg: kvc_config, k_base, v_base, workspace, ws_bytes: int):
     h = _vp()
     st = _lib.kvc_alloc(ctypes.byref(cfg), _ptr(k_base), _ptr(v_base), _ptr(workspace),
                         int(ws_bytes), ctypes.byref(h))
+    return st, (h.value if st == KVC_OK else None)
+
+
+def kvc_scale_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_scale_bytes(ctypes.byref(cfg))
+
+
+def kvc_alloc_scaled(cfg: kvc_config, k_base, v_base, k_scale, v_scale, workspace, ws_bytes: int):
+    h = _vp()
+    st = _lib.kvc_alloc_scaled(ctypes.byref(cfg), _ptr(k_base), _ptr(v_base), _ptr(k_scale), _ptr(v_scale),
+                               _ptr(workspace), int(ws_bytes), ctypes.byref(h))
     return st, (h.value if st == KVC_OK else None)
 
 

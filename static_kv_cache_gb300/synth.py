@@ -18,8 +18,10 @@ import hashlib
 
 import torch
 
-DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
-ELEM_BYTES = {"bf16": 2, "fp16": 2, "fp32": 4}
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32, "int8": torch.int8}
+ELEM_BYTES = {"bf16": 2, "fp16": 2, "fp32": 4, "int8": 1}
+# activations (q, out, new rows) of a cache type: int8 caches take bf16 ones
+ACT_DTYPE = {"bf16": "bf16", "fp16": "fp16", "fp32": "fp32", "int8": "bf16"}
 
 # Quiet-NaN bit patterns with a recognisable payload.
 POISON_BITS = {"bf16": 0x7FA5, "fp16": 0x7E5A, "fp32": 0x7FA5A5A5}
@@ -79,6 +81,9 @@ WORKLOADS = {
     "qwen2_5_1_5b_bf16": Workload("qwen2_5_1_5b_bf16", 28, 64, 12, 2, 128, 4096, "bf16",
                                   steps=1, prefill=4095, seed=1013),
     # One Llama-2-70B-shaped layer (MHA 64 heads) at 32k context, B=1 and B=4.
+    # The Llama-3-8B-shaped layer with an int8 cache (one fp32 scale per row).
+    "llama3_8b_int8": Workload("llama3_8b_int8", 32, 16, 32, 8, 128, 8192, "int8", steps=1,
+                               ragged=(1024, 8192), seed=1002),
     "llama2_70b_b1": Workload("llama2_70b_b1", 1, 1, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",
