@@ -5,7 +5,7 @@
 // x_hat = code * scale; q and the output are bf16.
 //
 // Same decomposition, stage ring, merge warp and split combine as
-// decode_mma_kernel; the tiles hold int8 codes (32 rows of d_h bytes, TMA
+// decode_mma_kernel; the tiles hold int8 codes (64 rows of d_h bytes, TMA
 // boxes with the 128-byte swizzle) and the row scales arrive by 4-byte
 // cp.async beside them.  The per-row scale factors out of both products
 // exactly:
@@ -39,7 +39,12 @@ namespace kvc {
 template <int D, int G>
 struct Q8Cfg {
     static constexpr int ROW_BYTES = D;                 // one int8 code per element
-    static constexpr int TILE = 32;
+    // 64 keys per tile: a stage (K and V codes) is 16 KB.  The stage ring
+    // moves a bounded number of tiles per microsecond, so tiles as small as
+    // 32 int8 rows would halve the bytes in flight per tile and cap the
+    // stream well below the memory's rate.
+    static constexpr int TILE = 64;
+    static constexpr int MT = TILE / 16;                 // 16-key m-tiles of S^T = k-steps of P.V
     static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K codes, V codes
     static constexpr int CHUNKS = ROW_BYTES / 16;
@@ -50,7 +55,7 @@ struct Q8Cfg {
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
     static constexpr int VL_CACHE = 256;
     static constexpr int N_FLAGS = 8;
-    // per stage besides the codes: 32 K scales + 32 V scales (in their own array)
+    // per stage besides the codes: TILE K scales + TILE V scales (in their own array)
     static constexpr int SCALE_BYTES = 2 * TILE * 4;
     static constexpr int FIXED_SMEM =
         1024 + 16 + 4 * (SCR_ACC_FLOATS + SCR_ML_FLOATS) + 4 * N_FLAGS + 4 * VL_CACHE;
@@ -123,24 +128,28 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
             const uint32_t sdst = scale0 + uint32_t(stage) * C::SCALE_BYTES;
-            const int q = nr >> 3, rem = nr & 7;
+            const int q = nr >> 3, rem = nr & 7;  // 8-row groups (boxes), rows after them
             if (lane == 0) {
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
-                if (q == 4) {
-                    dev::tma_load_3d(kdst, &a.tm_k32, 0, row0, z, full);
-                    dev::tma_load_3d(vdst, &a.tm_v32, 0, row0, z, full);
-                } else {
-                    for (int j = 0; j < q; ++j) {
-                        dev::tma_load_3d(kdst + j * 8 * 128, &a.tm_k8, 0, row0 + 8 * j, z, full);
-                        dev::tma_load_3d(vdst + j * 8 * 128, &a.tm_v8, 0, row0 + 8 * j, z, full);
-                    }
+                const int q32 = q >> 2;  // whole 32-row boxes, then 8-row boxes
+                for (int j = 0; j < q32; ++j) {
+                    dev::tma_load_3d(kdst + j * 32 * 128, &a.tm_k32, 0, row0 + 32 * j, z, full);
+                    dev::tma_load_3d(vdst + j * 32 * 128, &a.tm_v32, 0, row0 + 32 * j, z, full);
+                }
+                for (int j = 4 * q32; j < q; ++j) {
+                    dev::tma_load_3d(kdst + j * 8 * 128, &a.tm_k8, 0, row0 + 8 * j, z, full);
+                    dev::tma_load_3d(vdst + j * 8 * 128, &a.tm_v8, 0, row0 + 8 * j, z, full);
                 }
             }
-            // row scales: lane l takes rows l (K) and l (V)
-            if (lane < nr) {
-                dev::cp_async_4(sdst + 4 * lane, kss + row0 + lane);
-                dev::cp_async_4(sdst + 4 * (TILE + lane), vss + row0 + lane);
+            // row scales: lane l takes rows l and l + 32 of K and of V
+#pragma unroll
+            for (int h = 0; h < TILE / 32; ++h) {
+                const int r = lane + 32 * h;
+                if (r < nr) {
+                    dev::cp_async_4(sdst + 4 * r, kss + row0 + r);
+                    dev::cp_async_4(sdst + 4 * (TILE + r), vss + row0 + r);
+                }
             }
             if (rem) {
                 const int per = rem * C::CHUNKS;
@@ -172,7 +181,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(const __grid_constant__ DecodeArgs a) {
     using C = Q8Cfg<D, G>;
     using T = __nv_bfloat16;  // q and output
-    constexpr int NW = C::NW, TILE = C::TILE, CPAIRS = C::CPAIRS;
+    constexpr int NW = C::NW, TILE = C::TILE, CPAIRS = C::CPAIRS, MT = C::MT;
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -323,11 +332,11 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             const float *ksc = scales + cur_stage * 2 * TILE, *vsc = ksc + TILE;
 
             // ---- S^T = K . Q^T on the codes, then the K row scales
-            float s[2][4];
+            float s[MT][4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+            for (int mt = 0; mt < MT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int cp = 0; cp < CPAIRS; ++cp) {
                     uint32_t r[4];
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
                     dev::mma_16816_f16(s[mt], hi, qb[cp][2], qb[cp][3]);
                 }
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
                 const int k = 16 * mt + gq;
                 const float sa = ksc[k], sb = ksc[k + 8];   // rows past nr hold stale scales
                 s[mt][0] = k < nr ? s[mt][0] * sa : -INFINITY;
@@ -353,8 +362,12 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             }
 
             // ---- online softmax per head column
-            float x0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-            float x1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+            float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                x0 = fmaxf(x0, fmaxf(s[mt][0], s[mt][2]));
+                x1 = fmaxf(x1, fmaxf(s[mt][1], s[mt][3]));
+            }
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
@@ -364,16 +377,19 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             const float corr0 = exp2f(m0 - mn0), corr1 = exp2f(m1 - mn1);
             m0 = mn0;
             m1 = mn1;
-            float p[2][4];
+            float p[MT][4];
+            float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
                 p[mt][0] = exp2f(fmaf(s[mt][0], a.scale_log2, -mn0));
                 p[mt][1] = exp2f(fmaf(s[mt][1], a.scale_log2, -mn1));
                 p[mt][2] = exp2f(fmaf(s[mt][2], a.scale_log2, -mn0));
                 p[mt][3] = exp2f(fmaf(s[mt][3], a.scale_log2, -mn1));
+                ps0 += p[mt][0] + p[mt][2];
+                ps1 += p[mt][1] + p[mt][3];
             }
-            l0 = fmaf(l0, corr0, (p[0][0] + p[0][2]) + (p[1][0] + p[1][2]));
-            l1 = fmaf(l1, corr1, (p[0][1] + p[0][3]) + (p[1][1] + p[1][3]));
+            l0 = fmaf(l0, corr0, ps0);
+            l1 = fmaf(l1, corr1, ps1);
             if (__any_sync(FULL, (corr0 != 1.f) || (corr1 != 1.f))) {
 #pragma unroll
                 for (int cp = 0; cp < CPAIRS; ++cp)
@@ -386,9 +402,9 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
                     }
             }
             // ---- scaled probabilities P'[key][head] = p * scale_v[key] -> B fragments
-            uint32_t pb[2][2];
+            uint32_t pb[MT][2];
 #pragma unroll
-            for (int kst = 0; kst < 2; ++kst) {
+            for (int kst = 0; kst < MT; ++kst) {
                 const int k = 16 * kst + gq;
                 const float va = k < nr ? vsc[k] : 0.f, vb = k + 8 < nr ? vsc[k + 8] : 0.f;
                 pb[kst][0] = dev::movmatrix_trans(q8::pack_f16(p[kst][0] * va, p[kst][1] * va));
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             }
             // ---- O^T += V^T . P'^T on the codes
 #pragma unroll
-            for (int kst = 0; kst < 2; ++kst)
+            for (int kst = 0; kst < MT; ++kst)
 #pragma unroll
                 for (int cp = 0; cp < CPAIRS; ++cp) {
                     uint32_t r[4];
