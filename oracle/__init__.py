@@ -17,6 +17,8 @@ Contents
 * ``quantize_rows``   -- the int8 cache: symmetric per-row codes and fp32
                          scales ("10.3", section 4.4), and the dequantised
                          rows the attention reads.
+* ``paged.gather``    -- the logical rows of a paged cache through its block
+                         table ("10.3", section 7, PagedAttention).
 * ``prefill_attn``    -- chunked-prefill attention: each chunk query row
                          attends over the rows up to its own position
                          ("10.3", section 3; "KV-Cache Mechanics", AR
@@ -37,6 +39,7 @@ from .causal import causal_attention, widen
 from .formula import kv_bytes_per_token, kv_cache_bytes, mla_cache_bytes
 from .prefill import prefill_attn
 from .quant import dequantize_rows, quantize_rows
+from . import paged
 
 __all__ = ["decode_attn", "prefill_attn", "quantize_rows", "dequantize_rows", "ListAppendCache",
            "causal_attention", "widen",
