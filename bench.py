@@ -198,13 +198,16 @@ class ClockSampler:
 def step_bytes(w: synth.Workload, lengths) -> dict:
     """Algorithmic bytes of one layer's decode step (per launch).  An int8
     cache adds its 4-byte row scales to the rows read and written; its q,
-    out and new rows are bf16."""
+    out and new rows are bf16.  A paged cache adds the 4-byte block-table
+    entries of the live rows."""
     eb = synth.ELEM_BYTES[w.dtype]
     ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     sb = 4 if w.dtype == "int8" else 0                          # scale bytes per cache row
     live = int(np.asarray(lengths, dtype=np.int64).sum())
     attn = 2 * w.n_kv_heads * (w.d_head * eb + sb) * live + 2 * w.batch * w.n_heads * w.d_head * ab
     append = 2 * w.batch * w.n_kv_heads * (w.d_head * ab + w.d_head * eb + sb)  # read k/v_new, write the rows
+    if w.paged:   # the block table entries of the live rows, read once
+        attn += 4 * int(((np.asarray(lengths, dtype=np.int64) + synth.BLOCK_ROWS - 1) // synth.BLOCK_ROWS).sum())
     return {"attn": attn, "append": append}
 
 
@@ -221,11 +224,34 @@ class DeviceState:
         tdt, adt = synth.DTYPES[w.dtype], synth.DTYPES[act]
         dev = torch.device("cuda", device)
         shape = (w.n_layers, w.batch, w.n_kv_heads, w.max_context, w.d_head)
+        self.table = None
+        if w.paged:
+            table, self.num_blocks = synth.block_table(self.lengths.numpy(), w.max_context,
+                                                       synth.sub_seed(w.seed, "table"))
+            self.table = torch.from_numpy(table).to(dev)
+            shape = (w.n_layers, self.num_blocks, w.n_kv_heads, synth.BLOCK_ROWS, w.d_head)
         self.K = torch.empty(shape, dtype=tdt, device=dev)
         self.V = torch.empty(shape, dtype=tdt, device=dev)
         self.KS = self.VS = None
         pre = (self.lengths - 1).tolist()
-        if w.dtype == "int8":
+        if w.paged:
+            synth.poison_(self.K, w.dtype)
+            synth.poison_(self.V, w.dtype)
+            R = synth.BLOCK_ROWS
+            for layer in range(w.n_layers):
+                for b in range(w.batch):
+                    n = pre[b]
+                    if n == 0:
+                        continue
+                    nb = (n + R - 1) // R
+                    idx = self.table[b, :nb].long()
+                    for pool, tag in ((self.K, "pk"), (self.V, "pv")):
+                        rows = torch.empty((w.n_kv_heads, nb * R, w.d_head), dtype=tdt, device=dev)
+                        synth.poison_(rows, w.dtype)
+                        rows[:, :n] = synth.normal((w.n_kv_heads, n, w.d_head), w.dtype,
+                                                   synth.sub_seed(w.seed, tag, layer, b), dev)
+                        pool[layer].index_copy_(0, idx, rows.view(w.n_kv_heads, nb, R, w.d_head).transpose(0, 1))
+        elif w.dtype == "int8":
             # codes uniform on [-127, 127], scales positive: synthetic rows as the
             # quantising append would leave them; scales past the live rows NaN
             self.KS = torch.full(shape[:-1], float("nan"), dtype=torch.float32, device=dev)
@@ -259,7 +285,10 @@ class DeviceState:
         self.launches_per_layer = 1 if decode_kernel_name(w) == "decode_mma_kernel" else 2
         self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
         self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
-        if w.dtype == "int8":
+        if w.paged:
+            st, self.h = kvc.kvc_alloc_paged(self.cfg, self.K, self.V, self.num_blocks, self.table, self.ws,
+                                             self.ws.numel())
+        elif w.dtype == "int8":
             st, self.h = kvc.kvc_alloc_scaled(self.cfg, self.K, self.V, self.KS, self.VS, self.ws, self.ws.numel())
         else:
             st, self.h = kvc.kvc_alloc(self.cfg, self.K, self.V, self.ws, self.ws.numel())
@@ -301,17 +330,37 @@ def cpu_oracle_sample(w: synth.Workload, seconds: float, host=None):
     lengths = synth.live_lengths(w).numpy()
     if host is None:
         host = cpu_host_inputs(w, lengths)
-    Kh, Vh, qh = host
-    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     done_bytes, spent, n = 0, 0.0, 0
     while spent < seconds or n == 0:
         b = n % w.batch
         t0 = time.perf_counter()
-        oracle.decode_attn(qh[b:b + 1], Kh[b:b + 1], Vh[b:b + 1], lengths[b:b + 1], oracle_dtype(w))
+        oracle_one(w, host, b, lengths)
         spent += time.perf_counter() - t0
-        done_bytes += 2 * w.n_kv_heads * cache_row_bytes(w) * int(lengths[b]) + 2 * w.n_heads * w.d_head * ab
+        done_bytes += sample_bytes(w, lengths, b)
         n += 1
     return done_bytes / spent / 1e9, n, spent, oracle.num_threads()
+
+
+def oracle_one(w: synth.Workload, host, b: int, lengths):
+    """The oracle's decode attention of sequence b (layer 0); a paged cache
+    is first gathered through its block table."""
+    import oracle
+    Kh, Vh, qh, table = host
+    n = lengths[b:b + 1]
+    if table is not None:
+        K = oracle.paged.gather(Kh, table[b:b + 1], int(n[0]))
+        V = oracle.paged.gather(Vh, table[b:b + 1], int(n[0]))
+    else:
+        K, V = Kh[b:b + 1], Vh[b:b + 1]
+    return oracle.decode_attn(qh[b:b + 1], K, V, n, oracle_dtype(w))
+
+
+def sample_bytes(w: synth.Workload, lengths, b: int) -> int:
+    """Algorithmic bytes of one oracle sample (one sequence, all heads)."""
+    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
+    n = int(lengths[b])
+    table = 4 * ((n + synth.BLOCK_ROWS - 1) // synth.BLOCK_ROWS) if w.paged else 0
+    return 2 * w.n_kv_heads * cache_row_bytes(w) * n + 2 * w.n_heads * w.d_head * ab + table
 
 
 def cpu_host_inputs(w: synth.Workload, lengths):
@@ -329,7 +378,21 @@ def cpu_host_inputs(w: synth.Workload, lengths):
         Kh = oracle.dequantize_rows(*oracle.quantize_rows(Kh, act))
         Vh = oracle.dequantize_rows(*oracle.quantize_rows(Vh, act))
         qh = oracle.widen(qh, act)
-    return Kh, Vh, qh
+    table = None
+    if w.paged:   # the same rows scattered into 16-row blocks of a pool
+        table, nb = synth.block_table(lengths, w.max_context, synth.sub_seed(w.seed, "cpu_table"))
+        R = synth.BLOCK_ROWS
+        pools = []
+        for dense in (Kh, Vh):
+            pool = np.zeros((nb, w.n_kv_heads, R, w.d_head), dtype=dense.dtype)
+            for b in range(w.batch):
+                n = int(lengths[b])
+                for j in range((n + R - 1) // R):
+                    m = min(R, n - j * R)
+                    pool[table[b, j], :, :m] = dense[b, :, j * R:j * R + m]
+            pools.append(pool)
+        Kh, Vh = pools
+    return Kh, Vh, qh, table
 
 
 def oracle_dtype(w: synth.Workload) -> str:
@@ -349,6 +412,8 @@ def workload_config(w: synth.Workload, lengths, world: int) -> dict:
             "d_head": w.d_head, "max_context": w.max_context, "cache_dtype": w.dtype,
             "live_rows_per_kv_head": int(np.asarray(lengths).sum()),
             "valid_len": "ragged U{%d..%d}" % w.ragged if w.ragged else "uniform %d" % int(lengths[0]),
+            "layout": ("paged: 16-row blocks at random places in a pool of exactly the blocks the live rows need, "
+                       "one int32 block table [B, max_context/16]") if w.paged else "contiguous [L, B, H_kv, max_context, d_h]",
             "l2": "inputs larger than L2: each layer's live K/V exceeds the 129 MB L2 and the layers are cycled",
             "parallelism": f"replicas x{world} (independent batches, no collective on the data path)"}
 
@@ -428,7 +493,7 @@ def bench_kvc(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         gbs, n, spent, threads = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"fp64 oracle decode attention of layer 0, one sequence (all {w.n_heads} heads) "
+               "sample": f"fp64 oracle {'gather through the block table and ' if w.paged else ''}decode attention of layer 0, one sequence (all {w.n_heads} heads) "
                          f"per sample, cycling over the batch: {n} samples in {spent:.1f} s"}
 
     value = job_throughput(bytes_step, world, elapsed_max, args.steps)
@@ -473,16 +538,16 @@ def bench_reference(args, rank, world, local):
         cpu_oracle_sample(w, 0.0, host)
     import oracle
     total_bytes, total_s, samples = 0.0, 0.0, 0
-    ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     for s in range(args.steps):
         b = s % w.batch
         t0 = time.perf_counter()
-        oracle.decode_attn(host[2][b:b + 1], host[0][b:b + 1], host[1][b:b + 1], lengths[b:b + 1], oracle_dtype(w))
+        oracle_one(w, host, b, lengths)
         total_s += time.perf_counter() - t0
-        total_bytes += 2 * w.n_kv_heads * cache_row_bytes(w) * int(lengths[b]) + 2 * w.n_heads * w.d_head * ab
+        total_bytes += sample_bytes(w, lengths, b)
         samples += 1
     value = total_bytes / total_s / 1e9
-    sample = (f"fp64 oracle decode attention of layer 0, one sequence (all {w.n_heads} heads) per step, "
+    sample = (f"fp64 oracle {'gather through the block table and ' if w.paged else ''}decode attention of layer 0, "
+              f"one sequence (all {w.n_heads} heads) per step, "
               f"cycling over the batch; {samples} steps in {total_s:.1f} s")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / samples * 1e3, 3),

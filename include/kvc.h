@@ -162,6 +162,35 @@ uint64_t kvc_scale_bytes(const kvc_config *cfg);
 kvc_status kvc_alloc_scaled(const kvc_config *cfg, void *k_base, void *v_base, void *k_scale,
                             void *v_scale, void *workspace, uint64_t ws_bytes, kvc_cache **out);
 
+/* ---- paged caches ----------------------------------------------------------- */
+
+/* Bytes of ONE pool of a paged cache with num_blocks physical blocks per
+ * layer: n_layers * num_blocks * n_kv_heads * 16 * d_head elements.  0 for an
+ * invalid cfg or num_blocks <= 0 (and for int8 caches, which are not paged). */
+uint64_t kvc_pool_bytes(const kvc_config *cfg, int32_t num_blocks);
+
+/* A paged cache ("10.3", section 7, PagedAttention: the cache allocated in
+ * fixed-size blocks of 16 tokens, made logically contiguous by a block
+ * table).  Per layer, K and V each live in a pool of num_blocks physical
+ * blocks, laid out [L, num_blocks, H_kv, 16, d_h] (layer l's pool starts at
+ * element l * num_blocks * H_kv * 16 * d_h); block_table (device, int32
+ * [B, max_context / 16], caller-owned, shared by the layers) maps logical
+ * block j of sequence b to a physical block, so token p of sequence b lives in
+ * block block_table[b, p / 16] at slot p % 16.  The caller may change the
+ * table between calls (it is read at every launch; blocks may be shared
+ * read-only between sequences).  kvc_append and kvc_decode_step write through
+ * the table, kvc_decode_attn and kvc_decode_step read through it; rows past a
+ * sequence's live length are never read.  A table entry outside
+ * [0, num_blocks) is recorded as KVC_ERR_DEVICE_INDEX and its rows are
+ * neither read nor written.  cfg->max_context must be a multiple of 16.
+ * Built for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128
+ * (KVC_ERR_UNSUPPORTED otherwise); kvc_prefill_attn returns
+ * KVC_ERR_UNSUPPORTED on a paged handle.  Other arguments and errors as for
+ * kvc_alloc. */
+kvc_status kvc_alloc_paged(const kvc_config *cfg, void *k_pool, void *v_pool, int32_t num_blocks,
+                           const int32_t *block_table, void *workspace, uint64_t ws_bytes,
+                           kvc_cache **out);
+
 kvc_status kvc_alloc(const kvc_config *cfg, void *k_base, void *v_base,
                      void *workspace, uint64_t ws_bytes, kvc_cache **out);
 

@@ -23,6 +23,8 @@ struct kvc_cache {
     uint8_t *v_base;
     uint8_t *k_scale;        // int8 caches: per-row fp32 scales [L, B, H_kv, T_max]; else null
     uint8_t *v_scale;
+    const int32_t *block_table;  // paged caches: [B, max_blocks]; else null
+    int32_t num_blocks;          // paged: physical blocks per layer pool
     uint8_t *ws;
     uint64_t ws_bytes;
     kvc::WorkspaceLayout wl;
@@ -94,6 +96,8 @@ uint64_t layer_scale_bytes(const kvc_cache *h) {
 
 uint64_t layer_slab_bytes(const kvc_cache *h) {
     const kvc_config &c = h->cfg;
+    if (h->block_table)  // paged: one pool of num_blocks blocks of 16 rows per KV head
+        return uint64_t(h->num_blocks) * c.n_kv_heads * 16ull * c.d_head * h->elem_bytes;
     return uint64_t(c.batch) * c.n_kv_heads * uint64_t(c.max_context) * c.d_head * h->elem_bytes;
 }
 
@@ -134,6 +138,26 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
         const cuuint32_t box[3] = {cuuint32_t(128 / eb), j.rows, 1};
         if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+bool kvc::encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
+                           CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16)) return false;
+    const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {cuuint64_t(D), 16, cuuint64_t(n_blocks_total)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, 16ull * D * 2};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
+    const Job jobs[4] = {{k_pool, 16, k16}, {k_pool, 8, k8}, {v_pool, 16, v16}, {v_pool, 8, v8}};
+    for (const Job &j : jobs) {
+        const cuuint32_t box[3] = {64, j.rows, 1};
+        if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
@@ -192,7 +216,8 @@ uint64_t kvc_scale_bytes(const kvc_config *c) {
 namespace {
 
 kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k_scale, void *v_scale,
-                      void *workspace, uint64_t ws_bytes, kvc_cache **out) {
+                      void *workspace, uint64_t ws_bytes, kvc_cache **out, const int32_t *block_table = nullptr,
+                      int32_t num_blocks = 0) {
     if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
     if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
     const kvc::DecodeKernelInfo *info = find_decode(cfg);
@@ -237,6 +262,8 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     h->v_base = static_cast<uint8_t *>(v_base);
     h->k_scale = static_cast<uint8_t *>(k_scale);
     h->v_scale = static_cast<uint8_t *>(v_scale);
+    h->block_table = block_table;
+    h->num_blocks = num_blocks;
     h->ws = static_cast<uint8_t *>(workspace);
     h->ws_bytes = ws_bytes;
     h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads, h->group, cfg->d_head);
@@ -244,7 +271,14 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     h->prefill = pinfo;
     h->n_stages = n_stages;
     h->smem_bytes = smem_bytes;
-    if ((info->tensor_maps || pinfo) &&
+    if (block_table) {
+        h->prefill = nullptr;  // chunked prefill reads contiguous caches only
+        if (!kvc::encode_pool_maps(cfg->dtype, cfg->d_head, int64_t(cfg->n_layers) * num_blocks * cfg->n_kv_heads,
+                                   k_base, v_base, &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
+    } else if ((info->tensor_maps || pinfo) &&
         !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
                                 int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
                                 &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
@@ -269,6 +303,22 @@ kvc_status kvc_alloc_scaled(const kvc_config *cfg, void *k_base, void *v_base, v
                             void *workspace, uint64_t ws_bytes, kvc_cache **out) {
     if (!cfg || cfg->dtype != KVC_INT8 || !k_scale || !v_scale) return KVC_ERR_INVALID;
     return alloc_impl(cfg, k_base, v_base, k_scale, v_scale, workspace, ws_bytes, out);
+}
+
+uint64_t kvc_pool_bytes(const kvc_config *cfg, int32_t num_blocks) {
+    if (!shape_ok(cfg) || num_blocks <= 0 || cfg->dtype == KVC_INT8) return 0;
+    return uint64_t(cfg->n_layers) * uint64_t(num_blocks) * uint64_t(cfg->n_kv_heads) * 16ull *
+           uint64_t(cfg->d_head) * uint64_t(elem_bytes_of(cfg->dtype));
+}
+
+kvc_status kvc_alloc_paged(const kvc_config *cfg, void *k_pool, void *v_pool, int32_t num_blocks,
+                           const int32_t *block_table, void *workspace, uint64_t ws_bytes, kvc_cache **out) {
+    if (!cfg || !block_table || num_blocks <= 0 || cfg->max_context % 16 != 0) return KVC_ERR_INVALID;
+    if (cfg->dtype == KVC_INT8) return KVC_ERR_UNSUPPORTED;
+    const kvc::DecodeKernelInfo *info = shape_ok(cfg) ? find_decode(cfg) : nullptr;
+    if (info && !info->tensor_maps) return KVC_ERR_UNSUPPORTED;  // the paged producer is the TMA kernel's
+    if (!aligned16(block_table)) return KVC_ERR_ALIGNMENT;
+    return alloc_impl(cfg, k_pool, v_pool, nullptr, nullptr, workspace, ws_bytes, out, block_table, num_blocks);
 }
 
 void kvc_free(kvc_cache *h) { delete h; }
@@ -301,7 +351,7 @@ kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void
         h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
         static_cast<const uint8_t *>(v_new), cache_index, 0, h->cfg.batch, h->cfg.n_kv_heads, T_new,
         h->cfg.max_context, h->cfg.d_head * h->elem_bytes, reinterpret_cast<int32_t *>(h->ws),
-        h->num_sms, static_cast<cudaStream_t>(stream));
+        h->num_sms, static_cast<cudaStream_t>(stream), h->block_table, h->cfg.max_context / 16, h->num_blocks);
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
@@ -353,6 +403,11 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.seg_base = layer * c.batch * c.n_kv_heads;
+    a.block_table = h->block_table;
+    a.max_blocks = c.max_context / 16;
+    a.num_blocks = h->num_blocks;
+    a.gran = h->block_table ? 16 : 1;
+    if (h->block_table) a.seg_base = layer * h->num_blocks * c.n_kv_heads;
     if (h->decode->tensor_maps) {
         a.tm_k32 = h->tm_k32;
         a.tm_k8 = h->tm_k8;

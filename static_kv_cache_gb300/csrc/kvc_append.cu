@@ -23,7 +23,8 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
                                                      const uint8_t *__restrict__ v_new,
                                                      const int32_t *__restrict__ cache_index, int index_offset,
                                                      int B, int H_kv, int T_new, int max_ctx, int row_vecs,
-                                                     int32_t *err) {
+                                                     const int32_t *__restrict__ table, int max_blocks,
+                                                     int num_blocks, int32_t *err) {
     const int64_t run = int64_t(T_new) * row_vecs;   // vectors per (b, j)
     const int64_t per_tensor = int64_t(B) * H_kv * run;
     const int64_t total = 2 * per_tensor;
@@ -40,8 +41,19 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
             continue;
         }
         const uint4 *src = reinterpret_cast<const uint4 *>(is_v ? v_new : k_new) + seg * run + off;
-        uint4 *dst = reinterpret_cast<uint4 *>(is_v ? V : K) +
-                     (seg * max_ctx + ci) * int64_t(row_vecs) + off;
+        int64_t row;  // destination row, in rows of the layer's cache or pool
+        if (table) {  // paged: the position's slot in its physical block of 16 rows
+            const int pos = ci + int(off / row_vecs);
+            const int phys = __ldg(table + int64_t(b) * max_blocks + pos / 16);
+            if (phys < 0 || phys >= num_blocks) {
+                atomicCAS(err, 0, ERR_DEVICE_INDEX);
+                continue;
+            }
+            row = (int64_t(phys) * H_kv + seg % H_kv) * 16 + pos % 16;
+        } else {
+            row = seg * max_ctx + ci + off / row_vecs;
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(is_v ? V : K) + row * row_vecs + off % row_vecs;
         *dst = __ldg(src);
     }
 }
@@ -127,7 +139,7 @@ cudaError_t launch_append_q8(uint8_t *K_layer, uint8_t *V_layer, float *ks_layer
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
                           const uint8_t *v_new, const int32_t *cache_index, int index_offset, int B,
                           int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err, int num_sms,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const int32_t *table, int max_blocks, int num_blocks) {
     const int row_vecs = row_bytes / 16;
     const int64_t total = 2 * int64_t(B) * H_kv * T_new * row_vecs;
     if (total == 0) return cudaSuccess;
@@ -135,7 +147,7 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
     const int64_t cap = int64_t(num_sms) * 8;
     const int grid = int(want < cap ? want : cap);
     append_kernel<<<grid, 256, 0, stream>>>(K_layer, V_layer, k_new, v_new, cache_index, index_offset, B, H_kv,
-                                            T_new, max_ctx, row_vecs, err);
+                                            T_new, max_ctx, row_vecs, table, max_blocks, num_blocks, err);
     return cudaGetLastError();
 }
 

@@ -173,6 +173,10 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
     return v;
 }
 
+// A segment's rows in the flattened split space: its live rows rounded up to
+// the granularity.
+__device__ __forceinline__ int round_len(const DecodeArgs &a, int n) { return (n + a.gran - 1) / a.gran * a.gran; }
+
 __device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl, int lane) {
     Plan p;
     int64_t total = 0;
@@ -183,10 +187,11 @@ __device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl
             n = live_len(a, vl, b);
             if (n == 0 && blockIdx.x == 0 && threadIdx.x < 32) dev::record_error(a.err, ERR_DEVICE_INDEX);
         }
-        total += warp_sum_i64(n);
+        total += warp_sum_i64(round_len(a, n));
     }
     const int64_t R = total * a.H_kv;
     p.chunk = (R + gridDim.x - 1) / gridDim.x;
+    p.chunk = (p.chunk + a.gran - 1) / a.gran * a.gran;  // split points fall on multiples of gran
     p.r0 = min(R, int64_t(blockIdx.x) * p.chunk);
     p.r1 = min(R, p.r0 + p.chunk);
     p.b = a.B;
@@ -197,7 +202,7 @@ __device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
         const int n = (b < a.B) ? live_len(a, vl, b) : 0;
-        const int64_t w = int64_t(n) * a.H_kv;
+        const int64_t w = int64_t(round_len(a, n)) * a.H_kv;
         int64_t incl = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -219,9 +224,10 @@ __device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl
     return p;
 }
 
-// One maximal run of rows of one segment inside the CTA's range.
+// One maximal run of rows of one segment inside the CTA's range: live rows
+// [lo, hi) of the segment; len is the segment's length in the split space.
 struct Piece {
-    int b, kv, lo, hi, n;
+    int b, kv, lo, hi, n, len;
     int64_t seg_start;
 };
 
@@ -230,20 +236,23 @@ struct Walker {
     int b, kv, n;
     int64_t seg_start, r, r1;
 
+    int len;  // round_len of n
+
     __device__ __forceinline__ void init(const DecodeArgs &a, const Plan &p, const int32_t *lengths) {
         vl = lengths;
         b = p.b;
         n = p.n;
+        len = round_len(a, n);
         r = p.r0;
         r1 = p.r1;
-        kv = (n > 0) ? int((p.r0 - p.pb) / n) : 0;
-        seg_start = p.pb + int64_t(kv) * n;
+        kv = (len > 0) ? int((p.r0 - p.pb) / len) : 0;
+        seg_start = p.pb + int64_t(kv) * len;
     }
 
     __device__ __forceinline__ bool next(const DecodeArgs &a, Piece &pc) {
         if (r >= r1 || b >= a.B) return false;
-        while (r >= seg_start + n) {
-            seg_start += n;
+        while (r >= seg_start + len) {
+            seg_start += len;
             if (++kv == a.H_kv) {
                 kv = 0;
                 do {
@@ -251,15 +260,18 @@ struct Walker {
                     n = (b < a.B) ? live_len(a, vl, b) : 0;
                 } while (b < a.B && n == 0);
                 if (b >= a.B) return false;
+                len = round_len(a, n);
             }
         }
         pc.b = b;
         pc.kv = kv;
         pc.n = n;
+        pc.len = len;
         pc.seg_start = seg_start;
         pc.lo = int(r - seg_start);
-        pc.hi = int(min(int64_t(n), r1 - seg_start));
-        r = seg_start + pc.hi;
+        const int end = int(min(int64_t(len), r1 - seg_start));
+        pc.hi = min(end, n);  // rounding rows hold no data
+        r = seg_start + end;
         return true;
     }
 };
@@ -330,7 +342,7 @@ __device__ __forceinline__ void merge_piece(const DecodeArgs &a, const Plan &pla
 
     const int seg = pc.b * a.H_kv + pc.kv;
     const int c0 = int(pc.seg_start / plan.chunk);
-    const int c1 = int((pc.seg_start + pc.n - 1) / plan.chunk);
+    const int c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
     const bool whole = (c0 == c1);
     T *ob = reinterpret_cast<T *>(a.out) + (int64_t(pc.b) * H + pc.kv * G) * D;
     const bool aborted = flags[0] != 0;

@@ -202,6 +202,123 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
     return issued;
 }
 
+// The producer for a paged cache: a tile of 32 rows starts on a block
+// boundary (the split space is rounded to 16 rows per segment), so it is the
+// first 16 rows of two logical blocks.  Their physical blocks come from the
+// block table, 32 entries at a time (one per lane, shared by shuffles); a
+// full block arrives as one 16-row box per 64-column block of K and of V, a
+// partial one as an 8-row box and 16-byte cp.async copies.  A table entry
+// outside [0, num_blocks) is recorded as a device-index error and its block
+// is not copied.
+template <typename C>
+__device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Walker walk, uint32_t stage0,
+                                                        uint32_t bar0, int ns, volatile int *flags, int lane) {
+    constexpr int TILE = C::TILE, CB = C::ROW_BYTES / 128, BS = 16;
+    static_assert(TILE == 2 * BS, "a tile is two blocks");
+    constexpr unsigned FULL = 0xffffffffu;
+    const int64_t block_bytes = int64_t(BS) * C::ROW_BYTES;  // one KV head's rows of a block
+    uint32_t issued = 0, generic_written = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    Piece pc;
+    while (ok && walk.next(a, pc)) {
+        const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
+        const int new_row = a.k_new ? pc.n - 1 : -1;
+        int cached_base = -1 << 30;
+        int32_t cached = -1;  // lane l: physical block of logical block cached_base + l
+        for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE) {
+            const int nr = min(TILE, pc.hi - row0);
+            if (round > 0) {
+                const bool w =
+                    dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns);
+                if (!__all_sync(FULL, w)) {
+                    if (lane == 0) {
+                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                        flags[0] = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+            }
+            const int blk0 = row0 / BS;
+            if (blk0 + 1 >= cached_base + 32) {
+                cached_base = blk0;
+                cached = blk0 + lane < a.max_blocks ? __ldg(trow + blk0 + lane) : -1;
+            }
+            int phys[2], rows[2], boxed[2];
+            uint32_t tx_rows = 0;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                phys[jj] = __shfl_sync(FULL, cached, blk0 + jj - cached_base);
+                rows[jj] = max(0, min(BS, nr - BS * jj));
+                const int first = row0 + BS * jj;
+                const int nb = (new_row >= first && new_row < first + rows[jj]) ? new_row - first : rows[jj];
+                boxed[jj] = nb == BS ? BS : (nb >= 8 ? 8 : 0);
+                if (rows[jj] > 0 && (phys[jj] < 0 || phys[jj] >= a.num_blocks)) {
+                    if (lane == 0) dev::record_error(a.err, ERR_DEVICE_INDEX);
+                    rows[jj] = boxed[jj] = 0;  // not copied: its rows stay stale
+                }
+                tx_rows += uint32_t(boxed[jj]);
+            }
+            const uint32_t full = bar0 + 8 * stage;
+            const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
+            const uint32_t vdst = kdst + C::TILE_BYTES;
+            if (lane == 0) {
+                if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
+                dev::mbar_expect_tx(full, 2u * tx_rows * C::ROW_BYTES);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    if (!boxed[jj]) continue;
+                    const int z = a.seg_base + phys[jj] * a.H_kv + pc.kv;
+                    const CUtensorMap *mk = boxed[jj] == BS ? &a.tm_k32 : &a.tm_k8;
+                    const CUtensorMap *mv = boxed[jj] == BS ? &a.tm_v32 : &a.tm_v8;
+#pragma unroll
+                    for (int cb = 0; cb < CB; ++cb) {
+                        const uint32_t off = cb * C::BLOCK_BYTES + jj * BS * 128;
+                        dev::tma_load_3d(kdst + off, mk, cb * 64, 0, z, full);
+                        dev::tma_load_3d(vdst + off, mv, cb * 64, 0, z, full);
+                    }
+                }
+            }
+            bool generic = false;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int rem = rows[jj] - boxed[jj];
+                if (rem <= 0) continue;
+                generic = true;
+                const int64_t blk_off = (int64_t(phys[jj]) * a.H_kv + pc.kv) * block_bytes;
+                const int per = rem * C::CHUNKS;
+                for (int i = lane; i < 2 * per; i += 32) {
+                    const bool is_v = i >= per;
+                    const int j = is_v ? i - per : i;
+                    const int r = boxed[jj] + j / C::CHUNKS, c16 = j % C::CHUNKS;  // row within the block
+                    const int logical = row0 + BS * jj + r;
+                    const uint8_t *src =
+                        logical == new_row
+                            ? (is_v ? a.v_new : a.k_new) + (int64_t(pc.b) * a.H_kv + pc.kv) * C::ROW_BYTES + c16 * 16
+                            : (is_v ? a.V : a.K) + blk_off + int64_t(r) * C::ROW_BYTES + c16 * 16;
+                    dev::cp_async_16(C::swz(is_v ? vdst : kdst, BS * jj + r, c16 * 8), src);
+                }
+            }
+            if (generic) {
+                dev::cp_async_arrive(full);
+                generic_written |= 1u << stage;
+            } else {
+                generic_written &= ~(1u << stage);
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(full);
+            ++issued;
+            if (++stage == ns) {
+                stage = 0;
+                ++round;
+            }
+        }
+    }
+    return issued;
+}
+
 // Zero the halves of a 32-bit pair of keys (k, k + 1) that are not live.
 __device__ __forceinline__ uint32_t live_pair(uint32_t r, int k, int nr) {
     return r & ((k < nr ? 0x0000ffffu : 0u) | (k + 1 < nr ? 0xffff0000u : 0u));
@@ -426,7 +543,15 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
             const int c16 = is_v ? lane - CHUNKS : lane;
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) + seg * ROW_BYTES) + c16);
             uint8_t *cache = const_cast<uint8_t *>(is_v ? a.V : a.K);  // the caller's writable cache
-            reinterpret_cast<uint4 *>(cache + seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES)[c16] = v;
+            int64_t row_off = seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES;
+            if (a.block_table) {  // paged: the row's slot in its physical block
+                const int p = pc.n - 1;
+                const int phys = __ldg(a.block_table + int64_t(pc.b) * a.max_blocks + p / 16);
+                row_off = phys >= 0 && phys < a.num_blocks
+                              ? ((int64_t(phys) * a.H_kv + pc.kv) * 16 + p % 16) * ROW_BYTES
+                              : -1;  // reported by the producer
+            }
+            if (row_off >= 0) reinterpret_cast<uint4 *>(cache + row_off)[c16] = v;
         }
         bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
         ok = __all_sync(FULL, ok);
@@ -444,7 +569,7 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
 
         const int seg = pc.b * a.H_kv + pc.kv;
         const int c0 = int(pc.seg_start / plan.chunk);
-        const int c1 = int((pc.seg_start + pc.n - 1) / plan.chunk);
+        const int c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
         const int me = int(blockIdx.x);
         if (c0 != c1) {
             int ticket = 0;
@@ -536,7 +661,9 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
-        const uint32_t issued = produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
+        const uint32_t issued = a.block_table
+                                    ? produce_tiles_paged<C>(a, walk, stage0, bar0, ns, flags, lane)
+                                    : produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
         dev::named_barrier_sync(2, C::THREADS);  // every warp is done
         if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);

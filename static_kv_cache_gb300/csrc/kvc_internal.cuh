@@ -65,6 +65,14 @@ struct DecodeArgs {
     // int8 caches: one fp32 scale per cache row, [B, H_kv, max_ctx] per layer
     const float *k_scale;
     const float *v_scale;
+    // Paged caches (tensor-core kernel): K and V are this layer's pools
+    // [num_blocks, H_kv, 16, D], block_table [B, max_blocks] maps a sequence's
+    // logical block to a physical one; null for contiguous caches.
+    const int32_t *block_table;
+    int32_t max_blocks, num_blocks;
+    // Rows of the flattened split space per segment are rounded up to a
+    // multiple of gran (16 for paged caches, so every tile starts on a block).
+    int32_t gran;
     const int32_t *valid_len;  // [B]
     float *part_ml;
     float *part_acc;
@@ -160,11 +168,20 @@ cudaError_t launch_append_q8(uint8_t *K_layer, uint8_t *V_layer, float *ks_layer
                              int index_offset, int B, int H_kv, int T_new, int max_ctx, int D, int32_t *err,
                              int num_sms, cudaStream_t stream);
 
-// Append launcher (kvc_append.cu): rows go to cache_index[b] + index_offset.
+// Append launcher (kvc_append.cu): rows go to cache_index[b] + index_offset;
+// with a block table, K_layer / V_layer are the layer's pools [num_blocks,
+// H_kv, 16, D] and the rows go to their slots in the mapped blocks.
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
                           const uint8_t *v_new, const int32_t *cache_index, int index_offset,
                           int B, int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err,
-                          int num_sms, cudaStream_t stream);
+                          int num_sms, cudaStream_t stream, const int32_t *table = nullptr,
+                          int max_blocks = 0, int num_blocks = 0);
+
+// Tensor maps of paged pools [n_blocks_total][16][D] (n_blocks_total = L *
+// num_blocks * H_kv): boxes of 64 columns x 16 rows (in the *32 slots) and x 8
+// rows, 128-byte swizzle.  Host only.
+bool encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
+                      CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8);
 
 }  // namespace kvc
 

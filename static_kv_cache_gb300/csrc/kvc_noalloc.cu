@@ -210,6 +210,9 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.seg_base = layer * cfg->batch * cfg->n_kv_heads;
+    a.block_table = nullptr;
+    a.max_blocks = a.num_blocks = 0;
+    a.gran = 1;
     if (info->tensor_maps) {
         a.tm_k32 = maps[0];
         a.tm_k8 = maps[1];

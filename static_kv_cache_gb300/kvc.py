@@ -70,6 +70,10 @@ _lib.kvc_alloc.argtypes = [_cfgp, _vp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
 _lib.kvc_alloc.restype = _i32
 _lib.kvc_alloc_scaled.argtypes = [_cfgp, _vp, _vp, _vp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
 _lib.kvc_alloc_scaled.restype = _i32
+_lib.kvc_alloc_paged.argtypes = [_cfgp, _vp, _vp, _i32, _vp, _vp, _u64, ctypes.POINTER(_vp)]
+_lib.kvc_alloc_paged.restype = _i32
+_lib.kvc_pool_bytes.argtypes = [_cfgp, _i32]
+_lib.kvc_pool_bytes.restype = _u64
 _lib.kvc_free.argtypes = [_vp]
 _lib.kvc_free.restype = None
 _lib.kvc_set_num_splits.argtypes = [_vp, _i32]
@@ -148,6 +152,17 @@ def kvc_alloc_scaled(cfg: kvc_config, k_base, v_base, k_scale, v_scale, workspac
     h = _vp()
     st = _lib.kvc_alloc_scaled(ctypes.byref(cfg), _ptr(k_base), _ptr(v_base), _ptr(k_scale), _ptr(v_scale),
                                _ptr(workspace), int(ws_bytes), ctypes.byref(h))
+    return st, (h.value if st == KVC_OK else None)
+
+
+def kvc_pool_bytes(cfg: kvc_config, num_blocks: int) -> int:
+    return _lib.kvc_pool_bytes(ctypes.byref(cfg), int(num_blocks))
+
+
+def kvc_alloc_paged(cfg: kvc_config, k_pool, v_pool, num_blocks: int, block_table, workspace, ws_bytes: int):
+    h = _vp()
+    st = _lib.kvc_alloc_paged(ctypes.byref(cfg), _ptr(k_pool), _ptr(v_pool), int(num_blocks), _ptr(block_table),
+                              _ptr(workspace), int(ws_bytes), ctypes.byref(h))
     return st, (h.value if st == KVC_OK else None)
 
 

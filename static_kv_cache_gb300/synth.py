@@ -16,6 +16,7 @@ from __future__ import annotations
 import dataclasses
 import hashlib
 
+import numpy as np
 import torch
 
 DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32, "int8": torch.int8}
@@ -52,6 +53,7 @@ class Workload:
     first_append: int = 0
     seed: int = 1000
     chunk: int = 0          # chunked prefill: T_new of the chunk appended after the live rows
+    paged: bool = False     # cache in 16-row blocks of a pool, addressed through a block table
 
     @property
     def group(self) -> int:
@@ -84,6 +86,10 @@ WORKLOADS = {
     # The Llama-3-8B-shaped layer with an int8 cache (one fp32 scale per row).
     "llama3_8b_int8": Workload("llama3_8b_int8", 32, 16, 32, 8, 128, 8192, "int8", steps=1,
                                ragged=(1024, 8192), seed=1002),
+    # The same cache paged: each sequence's live rows (and its next row) in
+    # 16-row blocks placed at random in a pool of exactly those blocks.
+    "llama3_8b_paged": Workload("llama3_8b_paged", 32, 16, 32, 8, 128, 8192, "bf16", steps=1,
+                                ragged=(1024, 8192), seed=1002, paged=True),
     "llama2_70b_b1": Workload("llama2_70b_b1", 1, 1, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",
@@ -126,6 +132,27 @@ def live_lengths(w: Workload) -> torch.Tensor:
     if w.ragged is not None:
         return ragged_lengths(w.batch, w.ragged[0], w.ragged[1], sub_seed(w.seed, "len"))
     return torch.full((w.batch,), (w.prefill or 0) + w.first_append + 1, dtype=torch.int32)
+
+
+BLOCK_ROWS = 16
+
+
+def block_table(lengths, max_context: int, seed: int) -> tuple[np.ndarray, int]:
+    """A random block table for a paged cache: sequence b gets the
+    ceil(lengths[b] / 16) blocks its rows [0, lengths[b]) occupy, drawn without
+    replacement from a pool of exactly the blocks all sequences need; the
+    entries past those are 0 (never read).  Returns (table [B, max_context/16]
+    int32, num_blocks)."""
+    lengths = np.asarray(lengths, dtype=np.int64)
+    need = (lengths + BLOCK_ROWS - 1) // BLOCK_ROWS
+    num_blocks = max(1, int(need.sum()))
+    perm = np.random.default_rng(seed).permutation(num_blocks).astype(np.int32)
+    table = np.zeros((len(lengths), max_context // BLOCK_ROWS), dtype=np.int32)
+    at = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    return table, num_blocks
 
 
 def poison_(t: torch.Tensor, dtype: str) -> torch.Tensor:
