@@ -23,6 +23,9 @@ Contents
                          attends over the rows up to its own position
                          ("10.3", section 3; "KV-Cache Mechanics", AR
                          Static KV-Cache).
+* ``mla_decode_attn`` -- MLA decode: K and V rebuilt per head from the
+                         cached latents by the up-projections, then the
+                         single-query attention ("10.3", section 4.3).
 * ``kv_cache_bytes`` and friends -- the cache-size formula ("10.3",
                          section 2 boxed formula; section 4.4).
 """
@@ -38,10 +41,11 @@ from .cache import ListAppendCache
 from .causal import causal_attention, widen
 from .formula import kv_bytes_per_token, kv_cache_bytes, mla_cache_bytes
 from .prefill import prefill_attn
+from .mla import mla_decode_attn
 from .quant import dequantize_rows, quantize_rows
 from . import paged
 
-__all__ = ["decode_attn", "prefill_attn", "quantize_rows", "dequantize_rows", "ListAppendCache",
+__all__ = ["decode_attn", "prefill_attn", "mla_decode_attn", "quantize_rows", "dequantize_rows", "ListAppendCache",
            "causal_attention", "widen",
            "kv_cache_bytes", "kv_bytes_per_token", "mla_cache_bytes",
            "load_library", "num_threads", "set_num_threads", "DTYPE_CODES"]
