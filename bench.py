@@ -49,6 +49,8 @@ def decode_kernel_name(w: synth.Workload) -> str:
     """The decode kernel the library picks for a workload: the tensor-core
     kernel for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128,
     the CUDA-core kernel otherwise."""
+    if w.d_latent:
+        return "mla_decode_kernel"
     if w.dtype == "int8":
         return "decode_q8_kernel"
     if w.dtype in ("bf16", "fp16") and 2 <= w.group <= 8 and w.d_head in (64, 128):
@@ -199,9 +201,15 @@ def step_bytes(w: synth.Workload, lengths) -> dict:
     """Algorithmic bytes of one layer's decode step (per launch).  An int8
     cache adds its 4-byte row scales to the rows read and written; its q,
     out and new rows are bf16.  A paged cache adds the 4-byte block-table
-    entries of the live rows."""
+    entries of the live rows.  An MLA cache reads each latent row once for all
+    heads, plus the two up-projections of the layer."""
     eb = synth.ELEM_BYTES[w.dtype]
     ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
+    if w.d_latent:   # MLA: the latent rows once, q and out, both up-projections, the step's latent row
+        live = int(np.asarray(lengths, dtype=np.int64).sum())
+        attn = (live * w.d_latent * eb + 2 * w.batch * w.n_heads * w.d_head * ab
+                + 2 * w.n_heads * w.d_head * w.d_latent * eb)
+        return {"attn": attn, "append": 2 * w.batch * w.d_latent * eb}
     sb = 4 if w.dtype == "int8" else 0                          # scale bytes per cache row
     live = int(np.asarray(lengths, dtype=np.int64).sum())
     attn = 2 * w.n_kv_heads * (w.d_head * eb + sb) * live + 2 * w.batch * w.n_heads * w.d_head * ab
@@ -213,6 +221,9 @@ def step_bytes(w: synth.Workload, lengths) -> dict:
 
 class DeviceState:
     """Caches, workspace, handle and the per-layer step inputs on one GPU."""
+
+    # per-step inputs (attribute, keyword of step())
+    STEP_INPUTS = (("q", "q"), ("k_new", "k_new"), ("v_new", "v_new"), ("valid_len", "vl"))
 
     def __init__(self, w: synth.Workload, device: int):
         from static_kv_cache_gb300 import kvc
@@ -317,8 +328,76 @@ class DeviceState:
                 events[layer][1].record(stream)
         return self.launches_per_layer * w.n_layers
 
+    def error(self, stream) -> int:
+        return self.kvc.kvc_get_error(self.h, stream.cuda_stream)
+
     def close(self):
         self.kvc.kvc_free(self.h)
+
+
+class MlaState:
+    """The MLA latent cache [L, B, max_context, d_latent], per-layer
+    up-projections [L, H, d_h, d_latent] (entries N(0, 1/d_latent), so the
+    rebuilt rows have unit variance), workspace, handle and step inputs."""
+
+    STEP_INPUTS = (("q", "q"), ("c_new", "c_new"), ("valid_len", "vl"))
+
+    def __init__(self, w: synth.Workload, device: int):
+        from static_kv_cache_gb300 import kvc
+        self.kvc = kvc
+        self.w = w
+        self.lengths = synth.live_lengths(w)
+        self.maxlen = int(self.lengths.max())
+        tdt = synth.DTYPES[w.dtype]
+        dev = torch.device("cuda", device)
+        L, B, H = w.n_layers, w.batch, w.n_heads
+        self.C = torch.empty((L, B, w.max_context, w.d_latent), dtype=tdt, device=dev)
+        synth.poison_(self.C, w.dtype)
+        pre = (self.lengths - 1).tolist()
+        for layer in range(L):
+            for b in range(B):
+                if pre[b]:
+                    self.C[layer, b, :pre[b]] = synth.normal((pre[b], w.d_latent), w.dtype,
+                                                             synth.sub_seed(w.seed, "pc", layer, b), dev)
+        shape_w = (L, H, w.d_head, w.d_latent)
+        self.wk = (synth.normal(shape_w, "fp32", synth.sub_seed(w.seed, "wk"), dev) / w.d_latent ** 0.5).to(tdt)
+        self.wv = (synth.normal(shape_w, "fp32", synth.sub_seed(w.seed, "wv"), dev) / w.d_latent ** 0.5).to(tdt)
+        self.q = synth.normal((L, B, H, w.d_head), w.dtype, synth.sub_seed(w.seed, "q"), dev)
+        self.c_new = synth.normal((L, B, w.d_latent), w.dtype, synth.sub_seed(w.seed, "cn"), dev)
+        self.out = torch.empty((L, B, H, w.d_head), dtype=tdt, device=dev)
+        self.valid_len = self.lengths.to(dev)
+        self.launches_per_layer = 3   # absorb (+ append), attention over the latents, combine + up-projection
+        self.cfg = kvc.make_mla_config(L, B, H, w.d_head, w.d_latent, w.max_context, w.dtype)
+        self.ws = torch.zeros(kvc.kvc_mla_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
+        st, self.h = kvc.kvc_mla_alloc(self.cfg, self.C, self.ws, self.ws.numel())
+        kvc.check(st, "kvc_mla_alloc")
+        torch.cuda.synchronize(dev)
+
+    def step(self, stream, events=None, q=None, c_new=None, vl=None, out=None) -> int:
+        """One MLA decode step over all layers: kvc_mla_decode_step per layer
+        (append the latent row at valid_len - 1, attend, up-project)."""
+        kvc, w = self.kvc, self.w
+        q = self.q if q is None else q
+        c_new = self.c_new if c_new is None else c_new
+        vl = self.valid_len if vl is None else vl
+        out = self.out if out is None else out
+        sp = stream.cuda_stream
+        for layer in range(w.n_layers):
+            if events is not None:
+                events[layer][0].record(stream)
+            st = kvc.kvc_mla_decode_step(self.h, layer, q[layer], c_new[layer], self.wk[layer], self.wv[layer], vl,
+                                         self.maxlen, out[layer], sp)
+            if st:
+                raise kvc.KvcError(st, "kvc_mla_decode_step")
+            if events is not None:
+                events[layer][1].record(stream)
+        return self.launches_per_layer * w.n_layers
+
+    def error(self, stream) -> int:
+        return self.kvc.kvc_mla_get_error(self.h, stream.cuda_stream)
+
+    def close(self):
+        self.kvc.kvc_mla_free(self.h)
 
 
 # --------------------------------------------------------------------------- CPU oracle sample
@@ -343,10 +422,14 @@ def cpu_oracle_sample(w: synth.Workload, seconds: float, host=None):
 
 def oracle_one(w: synth.Workload, host, b: int, lengths):
     """The oracle's decode attention of sequence b (layer 0); a paged cache
-    is first gathered through its block table."""
+    is first gathered through its block table; an MLA cache goes through the
+    MLA oracle (keys and values rebuilt from the latents)."""
     import oracle
-    Kh, Vh, qh, table = host
     n = lengths[b:b + 1]
+    if w.d_latent:
+        Ch, wk, wv, qh = host
+        return oracle.mla_decode_attn(qh[b:b + 1], Ch[b:b + 1, :int(n[0])], wk, wv, n, w.dtype)
+    Kh, Vh, qh, table = host
     if table is not None:
         K = oracle.paged.gather(Kh, table[b:b + 1], int(n[0]))
         V = oracle.paged.gather(Vh, table[b:b + 1], int(n[0]))
@@ -359,6 +442,8 @@ def sample_bytes(w: synth.Workload, lengths, b: int) -> int:
     """Algorithmic bytes of one oracle sample (one sequence, all heads)."""
     ab = synth.ELEM_BYTES[synth.ACT_DTYPE[w.dtype]]
     n = int(lengths[b])
+    if w.d_latent:
+        return n * w.d_latent * synth.ELEM_BYTES[w.dtype] + 2 * w.n_heads * w.d_head * ab
     table = 4 * ((n + synth.BLOCK_ROWS - 1) // synth.BLOCK_ROWS) if w.paged else 0
     return 2 * w.n_kv_heads * cache_row_bytes(w) * n + 2 * w.n_heads * w.d_head * ab + table
 
@@ -368,8 +453,17 @@ def cpu_host_inputs(w: synth.Workload, lengths):
     an int8 cache: rows quantised by the oracle and handed to it
     dequantised (fp64), q widened to fp64."""
     maxlen = int(np.max(lengths))
-    shape = (w.batch, w.n_kv_heads, maxlen, w.d_head)
     act = synth.ACT_DTYPE[w.dtype]
+    if w.d_latent:
+        Ch = synth.to_bits(synth.normal((w.batch, maxlen, w.d_latent), w.dtype, synth.sub_seed(w.seed, "cpu_c"))).copy()
+        wsh = (w.n_heads, w.d_head, w.d_latent)
+        wk = synth.to_bits((synth.normal(wsh, "fp32", synth.sub_seed(w.seed, "cpu_wk")) / w.d_latent ** 0.5)
+                           .to(synth.DTYPES[w.dtype]))
+        wv = synth.to_bits((synth.normal(wsh, "fp32", synth.sub_seed(w.seed, "cpu_wv")) / w.d_latent ** 0.5)
+                           .to(synth.DTYPES[w.dtype]))
+        qh = synth.to_bits(synth.normal((w.batch, w.n_heads, w.d_head), w.dtype, synth.sub_seed(w.seed, "cpu_q")))
+        return Ch, wk, wv, qh
+    shape = (w.batch, w.n_kv_heads, maxlen, w.d_head)
     Kh = synth.to_bits(synth.normal(shape, act, synth.sub_seed(w.seed, "cpu_k"))).copy()
     Vh = synth.to_bits(synth.normal(shape, act, synth.sub_seed(w.seed, "cpu_v"))).copy()
     qh = synth.to_bits(synth.normal((w.batch, w.n_heads, w.d_head), act, synth.sub_seed(w.seed, "cpu_q")))
@@ -395,6 +489,12 @@ def cpu_host_inputs(w: synth.Workload, lengths):
     return Kh, Vh, qh, table
 
 
+def oracle_what(w: synth.Workload) -> str:
+    if w.d_latent:
+        return "MLA decode attention (keys and values rebuilt from the latents)"
+    return ("gather through the block table and " if w.paged else "") + "decode attention"
+
+
 def oracle_dtype(w: synth.Workload) -> str:
     return "fp64" if w.dtype == "int8" else w.dtype
 
@@ -405,6 +505,15 @@ def cache_row_bytes(w: synth.Workload) -> int:
 
 
 def workload_config(w: synth.Workload, lengths, world: int) -> dict:
+    if w.d_latent:
+        return {"workload": f"{w.name}: MLA latent cache, {w.n_layers} layers, B={w.batch}, H={w.n_heads}, "
+                            f"d_h={w.d_head}, d_latent={w.d_latent}, max_context={w.max_context}, {w.dtype} cache",
+                "n_layers": w.n_layers, "batch": w.batch, "n_heads": w.n_heads, "d_head": w.d_head,
+                "d_latent": w.d_latent, "max_context": w.max_context, "cache_dtype": w.dtype,
+                "live_rows": int(np.asarray(lengths).sum()),
+                "valid_len": "ragged U{%d..%d}" % w.ragged if w.ragged else "uniform %d" % int(lengths[0]),
+                "l2": "inputs larger than L2: each layer's live latents exceed the 129 MB L2 and the layers are cycled",
+                "parallelism": f"replicas x{world} (independent batches, no collective on the data path)"}
     return {"workload": f"{w.name}: {w.n_layers} layers, B={w.batch}, H={w.n_heads}, "
                         f"H_kv={w.n_kv_heads}, d_h={w.d_head}, max_context={w.max_context}, "
                         f"{w.dtype} cache",
@@ -425,7 +534,7 @@ def bench_kvc(args, rank, world, local):
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = w.with_(n_layers=args.layers)
-    state = DeviceState(w, local)
+    state = MlaState(w, local) if w.d_latent else DeviceState(w, local)
     lengths = state.lengths.numpy()
     per_layer = step_bytes(w, lengths)
     bytes_step = (per_layer["attn"] + per_layer["append"]) * w.n_layers
@@ -457,7 +566,7 @@ def bench_kvc(args, rank, world, local):
     elapsed = t_start.elapsed_time(t_end) / 1e3
     elapsed_max = reduce_max(elapsed, world, device=torch.device("cuda", local))
     decode_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(w.n_layers)]
-    err = state.kvc.kvc_get_error(state.h, stream.cuda_stream)
+    err = state.error(stream)
     if err:
         raise state.kvc.KvcError(err, "device error word after the timed region")
 
@@ -465,12 +574,11 @@ def bench_kvc(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        hq, hk, hv = pin(state.q), pin(state.k_new), pin(state.v_new)
-        hvl = pin(state.valid_len)
+        host = {name: pin(getattr(state, name)) for name, _ in state.STEP_INPUTS}
+        devin = {name: torch.empty_like(getattr(state, name)) for name, _ in state.STEP_INPUTS}
+        kw = {arg: devin[name] for name, arg in state.STEP_INPUTS}
         hout = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
-        dq, dk, dv = torch.empty_like(state.q), torch.empty_like(state.k_new), torch.empty_like(state.v_new)
-        dvl = torch.empty_like(state.valid_len)
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hvl))
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = hout.numel() * hout.element_size()
         e2e_steps = max(3, min(args.steps, 200))
         barrier(world)
@@ -478,9 +586,9 @@ def bench_kvc(args, rank, world, local):
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for _ in range(e2e_steps):
-                for d, hsrc in ((dq, hq), (dk, hk), (dv, hv), (dvl, hvl)):
-                    d.copy_(hsrc, non_blocking=True)
-                state.step(stream, q=dq, k_new=dk, v_new=dv, vl=dvl)
+                for name, _ in state.STEP_INPUTS:
+                    devin[name].copy_(host[name], non_blocking=True)
+                state.step(stream, **kw)
                 hout.copy_(state.out, non_blocking=True)
                 stream.synchronize()
         e2e_s = reduce_max(time.perf_counter() - t0, world, device=torch.device("cuda", local))
@@ -493,7 +601,7 @@ def bench_kvc(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         gbs, n, spent, threads = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"fp64 oracle {'gather through the block table and ' if w.paged else ''}decode attention of layer 0, one sequence (all {w.n_heads} heads) "
+               "sample": f"fp64 oracle {oracle_what(w)} of layer 0, one sequence (all {w.n_heads} heads) "
                          f"per sample, cycling over the batch: {n} samples in {spent:.1f} s"}
 
     value = job_throughput(bytes_step, world, elapsed_max, args.steps)
@@ -539,6 +647,8 @@ def bench_reference(args, rank, world, local):
     import oracle
     total_bytes, total_s, samples = 0.0, 0.0, 0
     for s in range(args.steps):
+        if total_s > 12 * args.cpu_seconds:   # keep the whole run to a few minutes
+            break
         b = s % w.batch
         t0 = time.perf_counter()
         oracle_one(w, host, b, lengths)
@@ -546,7 +656,7 @@ def bench_reference(args, rank, world, local):
         total_bytes += sample_bytes(w, lengths, b)
         samples += 1
     value = total_bytes / total_s / 1e9
-    sample = (f"fp64 oracle {'gather through the block table and ' if w.paged else ''}decode attention of layer 0, "
+    sample = (f"fp64 oracle {oracle_what(w)} of layer 0, "
               f"one sequence (all {w.n_heads} heads) per step, "
               f"cycling over the batch; {samples} steps in {total_s:.1f} s")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
@@ -631,6 +741,9 @@ class PrefillState:
                 events[layer][1].record(stream)
         return 2 * w.n_layers
 
+    def error(self, stream) -> int:
+        return self.kvc.kvc_get_error(self.h, stream.cuda_stream)
+
     def close(self):
         self.kvc.kvc_free(self.h)
 
@@ -696,7 +809,7 @@ def bench_prefill(args, rank, world, local):
     clocks = sampler.stop() if sampler else None
     elapsed = reduce_max(t_start.elapsed_time(t_end) / 1e3, world, device=torch.device("cuda", local))
     launch_ms = [evs[s_][l][0].elapsed_time(evs[s_][l][1]) for s_ in range(args.steps) for l in range(w.n_layers)]
-    err = state.kvc.kvc_get_error(state.h, stream.cuda_stream)
+    err = state.error(stream)
     if err:
         raise state.kvc.KvcError(err, "device error word after the timed region")
     step_flops = work["flops"] * w.n_layers

@@ -346,6 +346,99 @@ kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t layer,
  * KVC_ERR_CUDA if the synchronisation or the copy fails. */
 kvc_status kvc_get_error(kvc_cache *h, void *stream);
 
+/* ---- MLA latent cache --------------------------------------------------- */
+
+/* "10.3 -- KV cache implementation details", section 4.3 (Multi-head Latent
+ * Attention): the cache holds one latent vector c of width d_latent per token
+ * -- a single tensor, no separate K and V -- and head h rebuilds its key and
+ * value rows from it by up-projections, k = W_UK[h] c and v = W_UV[h] c with
+ * W_UK[h], W_UV[h] of shape [d_head, d_latent].  Decode attention is
+ *   out[b, h] = sum_t softmax_t(q[b, h] . k_t / sqrt(d_head)) v_t
+ * over the live rows t < valid_len[b].  The library evaluates it in the
+ * absorbed order -- q~ = W_UK[h]^T q (rounded once to the cache type),
+ * attention of q~ over the latents, W_UV[h] applied to the attended latent
+ * (kept in fp32) -- reading every latent row once for all heads.
+ * Size: n_layers * d_latent * max_context * batch * p bytes ("10.3" §4.3).
+ *
+ * Shapes the kernels take: KVC_BF16 or KVC_FP16, n_heads 8 or 16, d_latent
+ * 128, 256 or 512, d_head 16..256 in multiples of 8; others are
+ * KVC_ERR_UNSUPPORTED.  Conventions (ownership, streams, device error word)
+ * as for the calls above. */
+typedef struct {
+    int32_t n_layers;
+    int32_t batch;
+    int32_t n_heads;
+    int32_t d_head;       /* width of the rebuilt key and value rows, and of q and out */
+    int32_t d_latent;     /* d_c */
+    int32_t max_context;
+    int32_t dtype;        /* kvc_dtype */
+} kvc_mla_config;
+
+typedef struct kvc_mla_cache kvc_mla_cache; /* opaque handle */
+
+/* Bytes of the latent cache [n_layers, batch, max_context, d_latent]; 0 for an
+ * invalid configuration. */
+uint64_t kvc_mla_cache_bytes(const kvc_mla_config *cfg);
+
+/* Workspace bytes kvc_mla_alloc needs: the error word, the absorbed queries
+ * [B, H, d_latent] and the split partials of up to 256 + B splits. */
+uint64_t kvc_mla_workspace_bytes(const kvc_mla_config *cfg);
+
+/* Bind a caller-owned latent cache and workspace to a new handle.
+ *   cfg        host
+ *   c_base     device, kvc_mla_cache_bytes(cfg) bytes, 16-byte aligned; the
+ *              latents of layer l start at l * B * max_context * d_latent
+ *              elements
+ *   workspace  device, >= kvc_mla_workspace_bytes(cfg), 256-byte aligned;
+ *              kvc_mla_alloc zeroes its error word (synchronously); it must
+ *              not be used for anything else while the handle lives
+ *   out        host; receives the handle
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_UNSUPPORTED, KVC_ERR_ALIGNMENT,
+ * KVC_ERR_WORKSPACE, KVC_ERR_CUDA. */
+kvc_status kvc_mla_alloc(const kvc_mla_config *cfg, void *c_base, void *workspace,
+                         uint64_t ws_bytes, kvc_mla_cache **out);
+
+void kvc_mla_free(kvc_mla_cache *h);
+
+/* Number of splits (CTAs) of the attention launch: 0 automatic, else
+ * 1..256. */
+kvc_status kvc_mla_set_num_splits(kvc_mla_cache *h, int32_t n);
+
+/* Write T_new latent rows per sequence at cache_index[b].
+ *   c_new        device, [B, T_new, d_latent], 16-byte aligned
+ *   cache_index  device int32 [B]; a sequence whose rows would leave
+ *                [0, max_context) is skipped and KVC_ERR_DEVICE_INDEX recorded
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_CAPACITY, KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_mla_append(kvc_mla_cache *h, int32_t layer, const void *c_new,
+                          const int32_t *cache_index, int32_t T_new, void *stream);
+
+/* MLA decode attention of one layer.
+ *   q          device, [B, n_heads, d_head], 16-byte aligned
+ *   w_uk, w_uv device, [n_heads, d_head, d_latent] each, 16-byte aligned
+ *   valid_len  device int32 [B]: live latent rows of each sequence; a value
+ *              outside [1, max_context] skips the sequence (out unwritten) and
+ *              records KVC_ERR_DEVICE_INDEX
+ *   max_valid_hint  host upper bound of valid_len (sizes the grid), 0 = max_context
+ *   out        device, [B, n_heads, d_head]
+ * Three launches on the stream: absorb, attention over the latents, combine
+ * with the up-projection.
+ * Host errors: KVC_ERR_INVALID, KVC_ERR_ALIGNMENT, KVC_ERR_CUDA. */
+kvc_status kvc_mla_decode_attn(kvc_mla_cache *h, int32_t layer, const void *q,
+                               const void *w_uk, const void *w_uv,
+                               const int32_t *valid_len, int32_t max_valid_hint,
+                               void *out, void *stream);
+
+/* The decode step of one layer: write c_new [B, d_latent] (device, 16-byte
+ * aligned) at row valid_len[b] - 1, then kvc_mla_decode_attn.  The append
+ * rides in the absorb launch (three launches in all). */
+kvc_status kvc_mla_decode_step(kvc_mla_cache *h, int32_t layer, const void *q,
+                               const void *c_new, const void *w_uk, const void *w_uv,
+                               const int32_t *valid_len, int32_t max_valid_hint,
+                               void *out, void *stream);
+
+/* As kvc_get_error, for an MLA handle. */
+kvc_status kvc_mla_get_error(kvc_mla_cache *h, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,7 +37,7 @@ def nvcc() -> str:
 
 def _units():
     units = []
-    for src in ("kvc_api.cu", "kvc_append.cu", "kvc_noalloc.cu"):
+    for src in ("kvc_api.cu", "kvc_append.cu", "kvc_noalloc.cu", "kvc_mla_api.cu"):
         units.append((os.path.join(CSRC, src), os.path.join(BUILD, src.replace(".cu", ".o")), []))
     inst = os.path.join(CSRC, "kvc_decode_inst.cu")
     for tag, code in ELEM_TYPES.items():
@@ -50,6 +50,9 @@ def _units():
         for d in (64, 128):
             obj = os.path.join(BUILD, f"kvc_prefill_{tag}_{d}.o")
             units.append((pre, obj, [f"-DKVC_INST_TYPE={code}", f"-DKVC_INST_D={d}"]))
+    mla = os.path.join(CSRC, "kvc_mla_inst.cu")
+    for code, tag in ((0, "bf16"), (1, "f16")):
+        units.append((mla, os.path.join(BUILD, f"kvc_mla_{tag}.o"), [f"-DKVC_INST_TYPE={code}"]))
     return units
 
 

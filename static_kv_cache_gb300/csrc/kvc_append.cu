@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
                                                      int num_blocks, int32_t *err) {
     const int64_t run = int64_t(T_new) * row_vecs;   // vectors per (b, j)
     const int64_t per_tensor = int64_t(B) * H_kv * run;
-    const int64_t total = 2 * per_tensor;
+    const int64_t total = V ? 2 * per_tensor : per_tensor;   // V null: one tensor (a latent cache)
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const bool is_v = i >= per_tensor;
@@ -141,7 +141,7 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
                           int H_kv, int T_new, int max_ctx, int row_bytes, int32_t *err, int num_sms,
                           cudaStream_t stream, const int32_t *table, int max_blocks, int num_blocks) {
     const int row_vecs = row_bytes / 16;
-    const int64_t total = 2 * int64_t(B) * H_kv * T_new * row_vecs;
+    const int64_t total = (V_layer ? 2 : 1) * int64_t(B) * H_kv * T_new * row_vecs;
     if (total == 0) return cudaSuccess;
     const int64_t want = (total + 255) / 256;
     const int64_t cap = int64_t(num_sms) * 8;

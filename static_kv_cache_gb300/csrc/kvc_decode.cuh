@@ -162,7 +162,8 @@ struct Plan {
 
 // Live rows of sequence b, 0 for an out-of-range length.  `vl` is the
 // valid_len array or a shared-memory copy of it.
-__device__ __forceinline__ int live_len(const DecodeArgs &a, const int32_t *vl, int b) {
+template <class A>
+__device__ __forceinline__ int live_len(const A &a, const int32_t *vl, int b) {
     const int v = vl[b];
     return (v >= 1 && v <= a.max_ctx) ? v : 0;
 }
@@ -175,9 +176,11 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
 
 // A segment's rows in the flattened split space: its live rows rounded up to
 // the granularity.
-__device__ __forceinline__ int round_len(const DecodeArgs &a, int n) { return (n + a.gran - 1) / a.gran * a.gran; }
+template <class A>
+__device__ __forceinline__ int round_len(const A &a, int n) { return (n + a.gran - 1) / a.gran * a.gran; }
 
-__device__ __forceinline__ Plan make_plan(const DecodeArgs &a, const int32_t *vl, int lane) {
+template <class A>
+__device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lane) {
     Plan p;
     int64_t total = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -238,7 +241,8 @@ struct Walker {
 
     int len;  // round_len of n
 
-    __device__ __forceinline__ void init(const DecodeArgs &a, const Plan &p, const int32_t *lengths) {
+    template <class A>
+    __device__ __forceinline__ void init(const A &a, const Plan &p, const int32_t *lengths) {
         vl = lengths;
         b = p.b;
         n = p.n;
@@ -249,7 +253,8 @@ struct Walker {
         seg_start = p.pb + int64_t(kv) * len;
     }
 
-    __device__ __forceinline__ bool next(const DecodeArgs &a, Piece &pc) {
+    template <class A>
+    __device__ __forceinline__ bool next(const A &a, Piece &pc) {
         if (r >= r1 || b >= a.B) return false;
         while (r >= seg_start + len) {
             seg_start += len;

@@ -209,3 +209,77 @@ def check(status: int, what: str = "") -> None:
     """Raise KvcError unless status is KVC_OK."""
     if status != KVC_OK:
         raise KvcError(status, what)
+
+
+# ---- MLA latent cache
+class kvc_mla_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("d_head", ctypes.c_int32),
+                ("d_latent", ctypes.c_int32), ("max_context", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_mcfgp = ctypes.POINTER(kvc_mla_config)
+for _n in ("kvc_mla_cache_bytes", "kvc_mla_workspace_bytes"):
+    getattr(_lib, _n).argtypes = [_mcfgp]
+    getattr(_lib, _n).restype = _u64
+_lib.kvc_mla_alloc.argtypes = [_mcfgp, _vp, _vp, _u64, ctypes.POINTER(_vp)]
+_lib.kvc_mla_alloc.restype = _i32
+_lib.kvc_mla_free.argtypes = [_vp]
+_lib.kvc_mla_free.restype = None
+_lib.kvc_mla_set_num_splits.argtypes = [_vp, _i32]
+_lib.kvc_mla_set_num_splits.restype = _i32
+_lib.kvc_mla_append.argtypes = [_vp, _i32, _vp, _vp, _i32, _vp]
+_lib.kvc_mla_append.restype = _i32
+_lib.kvc_mla_decode_attn.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+_lib.kvc_mla_decode_attn.restype = _i32
+_lib.kvc_mla_decode_step.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+_lib.kvc_mla_decode_step.restype = _i32
+_lib.kvc_mla_get_error.argtypes = [_vp, _vp]
+_lib.kvc_mla_get_error.restype = _i32
+
+
+def make_mla_config(n_layers, batch, n_heads, d_head, d_latent, max_context, dtype) -> kvc_mla_config:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return kvc_mla_config(n_layers, batch, n_heads, d_head, d_latent, max_context, code)
+
+
+def kvc_mla_cache_bytes(cfg: kvc_mla_config) -> int:
+    return _lib.kvc_mla_cache_bytes(ctypes.byref(cfg))
+
+
+def kvc_mla_workspace_bytes(cfg: kvc_mla_config) -> int:
+    return _lib.kvc_mla_workspace_bytes(ctypes.byref(cfg))
+
+
+def kvc_mla_alloc(cfg: kvc_mla_config, c_base, workspace, ws_bytes: int):
+    h = _vp()
+    st = _lib.kvc_mla_alloc(ctypes.byref(cfg), _ptr(c_base), _ptr(workspace), int(ws_bytes), ctypes.byref(h))
+    return st, (h.value if st == KVC_OK else None)
+
+
+def kvc_mla_free(h) -> None:
+    _lib.kvc_mla_free(h)
+
+
+def kvc_mla_set_num_splits(h, n: int) -> int:
+    return _lib.kvc_mla_set_num_splits(h, int(n))
+
+
+def kvc_mla_append(h, layer: int, c_new, cache_index, T_new: int, stream=None) -> int:
+    return _lib.kvc_mla_append(h, int(layer), _ptr(c_new), _ptr(cache_index), int(T_new), _stream(stream))
+
+
+def kvc_mla_decode_attn(h, layer: int, q, w_uk, w_uv, valid_len, max_valid_hint: int, out, stream=None) -> int:
+    return _lib.kvc_mla_decode_attn(h, int(layer), _ptr(q), _ptr(w_uk), _ptr(w_uv), _ptr(valid_len),
+                                    int(max_valid_hint), _ptr(out), _stream(stream))
+
+
+def kvc_mla_decode_step(h, layer: int, q, c_new, w_uk, w_uv, valid_len, max_valid_hint: int, out,
+                        stream=None) -> int:
+    return _lib.kvc_mla_decode_step(h, int(layer), _ptr(q), _ptr(c_new), _ptr(w_uk), _ptr(w_uv),
+                                    _ptr(valid_len), int(max_valid_hint), _ptr(out), _stream(stream))
+
+
+def kvc_mla_get_error(h, stream=None) -> int:
+    return _lib.kvc_mla_get_error(h, _stream(stream))

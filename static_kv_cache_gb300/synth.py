@@ -54,6 +54,7 @@ class Workload:
     seed: int = 1000
     chunk: int = 0          # chunked prefill: T_new of the chunk appended after the live rows
     paged: bool = False     # cache in 16-row blocks of a pool, addressed through a block table
+    d_latent: int = 0       # MLA: width of the cached latent (one row per token, no K/V heads)
 
     @property
     def group(self) -> int:
@@ -90,6 +91,10 @@ WORKLOADS = {
     # 16-row blocks placed at random in a pool of exactly those blocks.
     "llama3_8b_paged": Workload("llama3_8b_paged", 32, 16, 32, 8, 128, 8192, "bf16", steps=1,
                                 ragged=(1024, 8192), seed=1002, paged=True),
+    # MLA latent cache with the DeepSeek-V2 widths the pages give (d_c = 512
+    # against 16 heads x 128), B=64, ragged live lengths U{1024..8192}.
+    "mla_dsv2": Workload("mla_dsv2", 32, 64, 16, 1, 128, 8192, "bf16", steps=1,
+                         ragged=(1024, 8192), seed=1030, d_latent=512),
     "llama2_70b_b1": Workload("llama2_70b_b1", 1, 1, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",

@@ -90,5 +90,27 @@ def test_handle_calls_reject_null(kvc_library_path):
 def test_all_configs_of_the_workloads_are_supported(kvc_library_path):
     from static_kv_cache_gb300 import kvc, synth
     for w in synth.WORKLOADS.values():
+        if w.d_latent:
+            continue   # MLA caches: test_mla_host_config
         cfg = kvc.make_config(w.n_layers, w.batch, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
         assert kvc.kvc_check_config(cfg) == kvc.KVC_OK, w.name
+
+
+def test_mla_host_config(kvc_library_path):
+    """The MLA cache size is the pages' one-tensor formula ("10.3", 4.3:
+    n_layers * d_c * n_ctx * B * p), equal to the oracle's; unsupported and
+    invalid shapes are refused on the host before any CUDA call."""
+    import oracle
+    from static_kv_cache_gb300 import kvc, synth
+    w = synth.WORKLOADS["mla_dsv2"]
+    cfg = kvc.make_mla_config(w.n_layers, w.batch, w.n_heads, w.d_head, w.d_latent, w.max_context, w.dtype)
+    assert kvc.kvc_mla_cache_bytes(cfg) == oracle.mla_cache_bytes(w.n_layers, w.d_latent, w.max_context, w.batch, 2)
+    assert kvc.kvc_mla_workspace_bytes(cfg) > 0
+    assert kvc.kvc_mla_alloc(kvc.make_mla_config(1, 2, 16, 128, 96, 64, "bf16"), 16, 256, 1 << 30)[0] \
+        == kvc.KVC_ERR_UNSUPPORTED
+    assert kvc.kvc_mla_alloc(kvc.make_mla_config(1, 0, 16, 128, 512, 64, "bf16"), 16, 256, 1 << 30)[0] \
+        == kvc.KVC_ERR_INVALID
+    assert kvc.kvc_mla_cache_bytes(kvc.make_mla_config(1, 2, 16, 128, 512, 0, "bf16")) == 0
+    assert kvc.kvc_mla_decode_attn(None, 0, 16, 16, 16, 16, 0, 16) == kvc.KVC_ERR_INVALID
+    assert kvc.kvc_mla_get_error(None) == kvc.KVC_ERR_INVALID
+    kvc.kvc_mla_free(None)
