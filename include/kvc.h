@@ -357,11 +357,12 @@ kvc_status kvc_get_error(kvc_cache *h, void *stream);
  * over the live rows t < valid_len[b].  The library evaluates it in the
  * absorbed order -- q~ = W_UK[h]^T q (rounded once to the cache type),
  * attention of q~ over the latents, W_UV[h] applied to the attended latent
- * (kept in fp32) -- reading every latent row once for all heads.
+ * (folded over the splits in fp32, then rounded once to the cache type for
+ * the tensor-core product) -- reading every latent row once for all heads.
  * Size: n_layers * d_latent * max_context * batch * p bytes ("10.3" §4.3).
  *
  * Shapes the kernels take: KVC_BF16 or KVC_FP16, n_heads 8 or 16, d_latent
- * 128, 256 or 512, d_head 16..256 in multiples of 8; others are
+ * 128, 256 or 512, d_head 16..256 in multiples of 16; others are
  * KVC_ERR_UNSUPPORTED.  Conventions (ownership, streams, device error word)
  * as for the calls above. */
 typedef struct {

@@ -129,82 +129,93 @@ struct MlaCfg {
 // ---------------------------------------------------------------------------
 // Absorb: q~[b, h, j] = scale * sum_i q[b, h, i] W_UK[h, i, j], rounded once
 // to the cache type; with c_new, also the step's latent row into the cache.
-// Grid (H, DC / 128, ceil(B / 16)), 256 threads: block (h, y, z) computes
-// columns [128 y, 128 y + 128) for sequences [16 z, 16 z + 16); thread t takes
-// column t % 128 of 8 sequences.  The block's slice of W_UK[h] goes through
-// shared memory 64 rows at a time, each row slice read with one coalesced
-// sweep of 16-byte loads, so the reads are in flight together.
+// Per head this is a [B x d_h] . [d_h x d_c] product, taken on mma.sync with
+// fp32 accumulation.  Grid (H, DC / 64, ceil(B / 64)), 128 threads: block
+// (h, y, z) computes columns [64 y, 64 y + 64) for sequences
+// [64 z, 64 z + 64); warp w takes the 16 sequences 64 z + 16 w + [0, 16) and
+// all 8 column n-tiles.  q rows and the W_UK[h] slice reach shared memory
+// by cp.async (row strides padded by 16 bytes, so every ldmatrix is
+// conflict-free); the W slice is [d][j], read transposed into B fragments.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int DH_MAX>
+struct MlaAbsorbSmem {
+    static constexpr int QS = DH_MAX + 8;                 // q row stride, elements
+    static constexpr int WS = 64 + 8;                     // W slice row stride, elements
+    static constexpr int BYTES = 64 * QS * 2 + DH_MAX * WS * 2;
+};
+
 template <typename T, int DC>
-__global__ void __launch_bounds__(256) mla_absorb_kernel(const MlaAbsorbArgs a) {
+__global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaAbsorbArgs a) {
     using E = MlaElem<T>;
-    constexpr int DCH = 64;                  // W_UK rows per shared-memory pass
-    __shared__ __align__(16) T ws[DCH][128];
-    __shared__ float qs[16][257];
-    const int h = blockIdx.x;
-    const int j0 = blockIdx.y * 128;
-    const int b0 = blockIdx.z * 16;
-    const int t = threadIdx.x;
-    // q rows of the 16 sequences: 16-byte vectors (d_h is a multiple of 8), all
-    // issued before any is stored
-    {
-        const T *q = static_cast<const T *>(a.q);
-        const int vpr = a.d_h >> 3;                       // vectors per row
-        uint4 v[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int i = t + 256 * k, bb = i / vpr;
-            v[k] = (i < 16 * vpr && b0 + bb < a.B)
-                       ? __ldg(reinterpret_cast<const uint4 *>(q + (int64_t(b0 + bb) * a.H + h) * a.d_h) + (i - bb * vpr))
-                       : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int i = t + 256 * k, bb = i / vpr, c = (i - bb * vpr) * 8;
-            if (i < 16 * vpr) {
-                const T *e = reinterpret_cast<const T *>(&v[k]);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) qs[bb][c + x] = E::load(e[x]);
-            }
-        }
+    using S = MlaAbsorbSmem<256>;
+    extern __shared__ __align__(16) uint8_t abs_smem[];
+    T *qs = reinterpret_cast<T *>(abs_smem);                  // [64][QS]
+    T *wsl = qs + 64 * S::QS;                                 // [d_h][WS]
+    const int h = blockIdx.x, j0 = blockIdx.y * 64, b0 = blockIdx.z * 64;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int dh = a.d_h, vq = dh / 8;                        // 16-byte vectors per q row
+    const T *q = static_cast<const T *>(a.q);
+    const T *w = static_cast<const T *>(a.w_uk) + int64_t(h) * dh * DC + j0;
+    for (int v = t; v < 64 * vq; v += 128) {
+        const int r = v / vq, c = (v - r * vq) * 8;
+        const uint32_t dst = dev::smem_addr(qs + r * S::QS + c);
+        if (b0 + r < a.B) dev::cp_async_16(dst, q + (int64_t(b0 + r) * a.H + h) * dh + c);
+        else *reinterpret_cast<uint4 *>(qs + r * S::QS + c) = make_uint4(0u, 0u, 0u, 0u);
     }
-    const int j = t & 127, bh = t >> 7;      // column, half of the block's sequences
-    float acc[8];
+    for (int v = t; v < dh * 8; v += 128) {
+        const int r = v >> 3, c = (v & 7) * 8;
+        dev::cp_async_16(dev::smem_addr(wsl + r * S::WS + c), w + int64_t(r) * DC + c);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    cp_async_wait_all();
+    __syncthreads();
+
+    float acc[8][4];
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb) acc[bb] = 0.f;
-    const T *w = static_cast<const T *>(a.w_uk) + int64_t(h) * a.d_h * DC + j0;
-    for (int d0 = 0; d0 < a.d_h; d0 += DCH) {
-        const int rows = min(DCH, a.d_h - d0);
-        __syncthreads();                     // previous pass done with ws (and qs written)
+    for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int l7 = lane & 7, j8 = lane >> 3;
+    // A (q rows x d): lane supplies row 16 w + (j8 & 1) * 8 + l7, columns (j8 >> 1) * 8
+    const uint32_t a_addr = dev::smem_addr(qs + (16 * warp + (j8 & 1) * 8 + l7) * S::QS + (j8 >> 1) * 8);
+    // B (d x columns) from W rows via .trans: lane supplies d row (j8 & 1) * 8 + l7, columns (j8 >> 1) * 8
+    const uint32_t b_addr = dev::smem_addr(wsl + ((j8 & 1) * 8 + l7) * S::WS + (j8 >> 1) * 8);
+    for (int ks = 0; ks < dh / 16; ++ks) {
+        uint32_t af[4];
+        dev::ldsm_x4(a_addr + ks * 32, af);
 #pragma unroll
-        for (int k = 0; k < DCH * 16 / 256; ++k) {   // 16-byte vectors: 16 per 128-column row slice
-            const int v = t + 256 * k, r = v >> 4, c = (v & 15) * 8;
-            if (r < rows)
-                *reinterpret_cast<uint4 *>(&ws[r][c]) =
-                    __ldg(reinterpret_cast<const uint4 *>(w + int64_t(d0 + r) * DC + c));
-        }
-        __syncthreads();
-        for (int r = 0; r < rows; ++r) {
-            const float wv = E::load(ws[r][j]);
-#pragma unroll
-            for (int bb = 0; bb < 8; ++bb) acc[bb] = fmaf(qs[bh * 8 + bb][d0 + r], wv, acc[bb]);
+        for (int np = 0; np < 4; ++np) {     // pairs of n-tiles
+            uint32_t bf[4];
+            dev::ldsm_x4_trans(b_addr + (ks * 16 * S::WS + np * 16) * 2, bf);
+            E::mma(acc[2 * np], af, bf[0], bf[1]);
+            E::mma(acc[2 * np + 1], af, bf[2], bf[3]);
         }
     }
     T *qt = static_cast<T *>(a.qt);
+    const int rb = b0 + 16 * warp + (lane >> 2);
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb) {
-        const int b = b0 + bh * 8 + bb;
-        if (b < a.B) qt[(int64_t(b) * a.H + h) * DC + j0 + j] = E::store(acc[bb] * a.scale);
+    for (int nt = 0; nt < 8; ++nt) {
+        const int j = j0 + nt * 8 + 2 * (lane & 3);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int b = rb + 8 * hf;
+            if (b < a.B) {
+                T pair[2] = {E::store(acc[nt][2 * hf] * a.scale), E::store(acc[nt][2 * hf + 1] * a.scale)};
+                *reinterpret_cast<uint32_t *>(qt + (int64_t(b) * a.H + h) * DC + j) = *reinterpret_cast<uint32_t *>(pair);
+            }
+        }
     }
     if (a.c_new && h == 0) {
+        // the step's latent rows of the block's sequences and columns: 64 x 64
         const T *cn = static_cast<const T *>(a.c_new);
         T *cache = static_cast<T *>(a.cache);
-        for (int bb = 0; bb < 8; ++bb) {
-            const int b = b0 + bh * 8 + bb;
+        for (int i = t; i < 64 * 8; i += 128) {
+            const int bb = i >> 3, c = (i & 7) * 8, b = b0 + bb;
             if (b >= a.B) break;
             const int v = __ldg(a.valid_len + b);
             if (v >= 1 && v <= a.max_ctx)
-                cache[(int64_t(b) * a.max_ctx + v - 1) * DC + j0 + j] = cn[int64_t(b) * DC + j0 + j];
-            else if (j == 0 && blockIdx.y == 0)
+                *reinterpret_cast<uint4 *>(cache + (int64_t(b) * a.max_ctx + v - 1) * DC + j0 + c) =
+                    __ldg(reinterpret_cast<const uint4 *>(cn + int64_t(b) * DC + j0 + c));
+            else if (c == 0 && blockIdx.y == 0)
                 dev::record_error(a.err, ERR_DEVICE_INDEX);
         }
     }
@@ -546,70 +557,87 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
 // ---------------------------------------------------------------------------
 // Combine and up-project: for each sequence b and head h, fold the partials
 // of b's splits (slots [c0 + b, c1 + b], the CTAs whose ranges meet b's rows)
-// into o~ = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), then
-// out[b, h] = W_UV[h] o~, rounded once.  Grid (H, ceil(B / 8), ceil(d_h /
-// 32)), 256 threads: warp k folds sequence 8 y + k (its lanes over the
-// splits, then over the columns), then warp k applies rows 32 z + k + 8 u
-// (u < 4) of W_UV[h], loaded at the start, to all 8 sequences.  Each of the
-// d_h / 32 blocks of a (head, 8 sequences) pair folds the same partials.  A
-// sequence with an out-of-range length has no partials and keeps its out.
+// into o~ = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), round it once to
+// the cache type, then out[b, h] = W_UV[h] o~ on mma.sync (fp32
+// accumulation), rounded once.  Grid (H, ceil(B / 16), ceil(d_h / 32)), 512
+// threads.  The block's 32 rows of W_UV[h] start towards shared memory
+// (cp.async) first; meanwhile warp k folds sequence 16 y + k (its lanes over
+// the splits, then over the columns, every split's loads issued together);
+// then warps 0-3 each take one
+// 8-row n-tile of the block's rows against the 16 sequences over all of d_c.
+// The d_h / 32 blocks of a (head, 16 sequences) pair fold the same partials.
+// A sequence with an out-of-range length has no partials and keeps its out.
+template <int DC>
+struct MlaCombineSmem {
+    static constexpr int AS = DC + 8;                     // row stride of o~ and of W rows, elements
+    static constexpr int A = 16 * AS * 2;                 // o~ of 16 sequences
+    static constexpr int W = 32 * AS * 2;                 // 32 rows of W_UV[h]
+    static constexpr int WTS = 16 * MLA_MAX_CTAS * 4;     // split weights
+    static constexpr int BYTES = A + W + WTS + 128;
+};
+
 template <typename T, int DC>
-__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaCombineArgs a) {
+__global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a) {
     using E = MlaElem<T>;
-    __shared__ __align__(16) float os[8][DC];
-    __shared__ float wts[8][MLA_MAX_CTAS];
-    __shared__ int s_c0[8], s_c1[8];
+    using S = MlaCombineSmem<DC>;
+    extern __shared__ __align__(16) uint8_t cmb[];
+    T *os = reinterpret_cast<T *>(cmb);                               // [16][AS]
+    T *wrows = reinterpret_cast<T *>(cmb + S::A);                      // [32][AS]
+    float *wts = reinterpret_cast<float *>(cmb + S::A + S::W);        // [16][MLA_MAX_CTAS]
+    int *s_c0 = reinterpret_cast<int *>(cmb + S::A + S::W + S::WTS);   // [16]
+    int *s_c1 = s_c0 + 16;                                             // [16]
     const int h = blockIdx.x;
-    const int b0 = blockIdx.y * 8;
+    const int b0 = blockIdx.y * 16;
+    const int i0 = blockIdx.z * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr unsigned FULL = 0xffffffffu;
-    // this block's rows of W_UV[h]: i = 32 z + w + 8 u, loads issued now, used last
-    constexpr int R = DC / 128;               // 4-element chunks per lane per row
-    constexpr int RW = 4;                     // rows per warp
-    const T *w = static_cast<const T *>(a.w_uv) + int64_t(h) * a.d_h * DC;
-    const int i0 = blockIdx.z * 8 * RW + warp;
-    uint2 raw[RW][R];
-#pragma unroll
-    for (int u = 0; u < RW; ++u) {
-        const int i = i0 + 8 * u;
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            raw[u][r] = i < a.d_h ? __ldg(reinterpret_cast<const uint2 *>(w + int64_t(i) * DC + r * 128 + lane * 4))
-                                  : make_uint2(0u, 0u);
+    const int rows = min(32, a.d_h - i0);
+    {
+        const T *w = static_cast<const T *>(a.w_uv) + (int64_t(h) * a.d_h + i0) * DC;
+        for (int v = threadIdx.x; v < rows * (DC / 8); v += 512) {
+            const int r = v / (DC / 8), c = (v - r * (DC / 8)) * 8;
+            dev::cp_async_16(dev::smem_addr(wrows + r * S::AS + c), w + int64_t(r) * DC + c);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     if (warp == 0) {
         // the decode launch's plan: flattened offsets of the sequences and the split length
         int64_t base = 0, mine = 0;
         int my_n = 0;
-        for (int c0 = 0; c0 < a.B; c0 += 32) {
-            const int b = c0 + lane;
-            int n = 0;
-            if (b < a.B) {
-                const int v = a.valid_len[b];
-                n = (v >= 1 && v <= a.max_ctx) ? v : 0;
-            }
-            int64_t incl = n;
+        for (int c0 = 0; c0 < a.B; c0 += 64) {   // two loads per lane in flight together
+            int n2[2];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int64_t y = __shfl_up_sync(FULL, incl, o);
-                if (lane >= o) incl += y;
+            for (int e = 0; e < 2; ++e) {
+                const int b = c0 + 32 * e + lane;
+                const int v = b < a.B ? a.valid_len[b] : 0;
+                n2[e] = (v >= 1 && v <= a.max_ctx) ? v : 0;
             }
-            for (int k = 0; k < 8; ++k) {
-                const int want = b0 + k;
-                if (want >= c0 && want < c0 + 32) {
-                    const int src = want - c0;
-                    const int64_t ex = base + __shfl_sync(FULL, incl - n, src);
-                    const int nn = __shfl_sync(FULL, n, src);
-                    if (lane == k) {
-                        mine = ex;
-                        my_n = nn;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int n = n2[e], cb = c0 + 32 * e;
+                int64_t incl = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t y = __shfl_up_sync(FULL, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                for (int k = 0; k < 16; ++k) {
+                    const int want = b0 + k;
+                    if (want >= cb && want < cb + 32) {
+                        const int src = want - cb;
+                        const int64_t ex = base + __shfl_sync(FULL, incl - n, src);
+                        const int nn = __shfl_sync(FULL, n, src);
+                        if (lane == k) {
+                            mine = ex;
+                            my_n = nn;
+                        }
                     }
                 }
+                base += __shfl_sync(FULL, incl, 31);
             }
-            base += __shfl_sync(FULL, incl, 31);
         }
         const int64_t chunk = (base + a.grid - 1) / a.grid;
-        if (lane < 8) {
+        if (lane < 16) {
             const bool live = my_n > 0 && b0 + lane < a.B;
             s_c0[lane] = live ? int(mine / chunk) : 0;
             s_c1[lane] = live ? int((mine + my_n - 1) / chunk) : -1;
@@ -617,21 +645,33 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaCombineArgs a
     }
     __syncthreads();
     {
-        const int b = b0 + warp, c0 = s_c0[warp], ns = s_c1[warp] - c0 + 1;
-        if (b < a.B && ns > 0) {
+        // warp k folds sequence b0 + k
+        const int s16 = warp, b = b0 + s16, c0 = s_c0[s16], ns = s_c1[s16] - c0 + 1;
+        T *orow = os + s16 * S::AS;
+        if (b >= a.B || ns <= 0) {   // no live rows: a zero row (its output is not written)
+            for (int c = lane * 8; c < DC; c += 256) *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
             const float *ml = a.part_ml + ((int64_t(c0) + b) * a.H + h) * 2;
             const int64_t ml_stride = int64_t(a.H) * 2;       // next slot
-            float M = -INFINITY;
-            for (int k = lane; k < ns; k += 32)
-                if (ml[k * ml_stride + 1] > 0.f) M = fmaxf(M, ml[k * ml_stride]);
+            float *wk_s = wts + s16 * MLA_MAX_CTAS;
+            float M = -INFINITY, L = 0.f;
+            for (int k0 = 0; k0 < ns; k0 += 32) {             // one pass for up to 32 splits
+                const int k = k0 + lane;
+                const float2 v = k < ns ? *reinterpret_cast<const float2 *>(ml + k * ml_stride) : make_float2(-INFINITY, 0.f);
+                if (k < ns) wk_s[k] = v.x;                    // each split's running max, for now
+                if (v.y > 0.f) M = fmaxf(M, v.x);
+            }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-            float L = 0.f;
-            for (int k = lane; k < ns; k += 32) {
-                const float l = ml[k * ml_stride + 1];
-                const float wk = l > 0.f ? exp2f(ml[k * ml_stride] - M) : 0.f;
-                wts[warp][k] = wk;
-                L += l * wk;
+            __syncwarp();
+            for (int k0 = 0; k0 < ns; k0 += 32) {
+                const int k = k0 + lane;
+                if (k < ns) {
+                    const float l = ml[k * ml_stride + 1];
+                    const float wk = l > 0.f ? exp2f(wk_s[k] - M) : 0.f;
+                    wk_s[k] = wk;
+                    L += l * wk;
+                }
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(FULL, L, o);
@@ -640,23 +680,24 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaCombineArgs a
             const float *acc = a.part_acc + ((int64_t(c0) + b) * a.H + h) * DC + lane * 4;
             const int64_t acc_stride = int64_t(a.H) * DC;
             constexpr int R4 = DC / 128;      // float4 columns per lane
+            constexpr int KB = 4;             // splits whose loads are in flight together
             float4 sum[R4];
 #pragma unroll
             for (int r = 0; r < R4; ++r) sum[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int k0 = 0; k0 < ns; k0 += 4) {   // four splits' loads in flight together
-                float4 x[4][R4];
-                float wk[4];
+            for (int k0 = 0; k0 < ns; k0 += KB) {
+                float4 x[KB][R4];
+                float wk[KB];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < KB; ++kk) {
                     const int k = k0 + kk;
-                    wk[kk] = k < ns ? wts[warp][k] : 0.f;
+                    wk[kk] = k < ns ? wk_s[k] : 0.f;
 #pragma unroll
                     for (int r = 0; r < R4; ++r)
                         x[kk][r] = wk[kk] != 0.f ? __ldg(reinterpret_cast<const float4 *>(acc + k * acc_stride + r * 128))
                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < KB; ++kk)
 #pragma unroll
                     for (int r = 0; r < R4; ++r) {
                         sum[r].x = fmaf(wk[kk], x[kk][r].x, sum[r].x);
@@ -666,45 +707,42 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaCombineArgs a
                     }
             }
 #pragma unroll
-            for (int r = 0; r < R4; ++r)
-                *reinterpret_cast<float4 *>(&os[warp][r * 128 + lane * 4]) =
-                    make_float4(sum[r].x * inv, sum[r].y * inv, sum[r].z * inv, sum[r].w * inv);
-        }
-    }
-    __syncthreads();
-    // out[b, h, i] = W_UV[h, i, :] . o~[b, h] for the block's rows
-    T *out = static_cast<T *>(a.out);
-#pragma unroll
-    for (int u = 0; u < RW; ++u) {
-        const int i = i0 + 8 * u;
-        float acc[8];
-#pragma unroll
-        for (int bb = 0; bb < 8; ++bb) acc[bb] = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const T *wv = reinterpret_cast<const T *>(&raw[u][r]);
-            const float w0 = E::load(wv[0]), w1 = E::load(wv[1]), w2 = E::load(wv[2]), w3 = E::load(wv[3]);
-            const int c = r * 128 + lane * 4;
-#pragma unroll
-            for (int bb = 0; bb < 8; ++bb) {
-                const float4 x = *reinterpret_cast<const float4 *>(&os[bb][c]);
-                acc[bb] = fmaf(w0, x.x, fmaf(w1, x.y, fmaf(w2, x.z, fmaf(w3, x.w, acc[bb]))));
+            for (int r = 0; r < R4; ++r) {
+                T v4[4] = {E::store(sum[r].x * inv), E::store(sum[r].y * inv), E::store(sum[r].z * inv),
+                           E::store(sum[r].w * inv)};
+                *reinterpret_cast<uint2 *>(orow + r * 128 + lane * 4) = *reinterpret_cast<uint2 *>(v4);
             }
         }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // out[b0 + m, h, i0 + 8 warp + n] for warps 0-3: A = o~ [16 x d_c], B = W rows [8 x d_c]
+    if (warp < 4 && 8 * warp < rows) {
+        const int l7 = lane & 7, j8 = lane >> 3;
+        const uint32_t a_addr = dev::smem_addr(os + ((j8 & 1) * 8 + l7) * S::AS + (j8 >> 1) * 8);
+        const uint32_t b_addr = dev::smem_addr(wrows + (8 * warp + l7) * S::AS + (j8 & 1) * 8 + (j8 >> 1) * 16);
+        float c2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // two chains over k
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb) {
-            float v = acc[bb];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-            acc[bb] = v;
+        for (int ks = 0; ks < DC / 16; ks += 2) {
+            uint32_t af[4], bf[4];
+            dev::ldsm_x4(a_addr + ks * 32, af);
+            dev::ldsm_x4(b_addr + ks * 32, bf);          // lanes 16-31 supply the next k-step
+            E::mma(c2[0], af, bf[0], bf[1]);
+            uint32_t af2[4];
+            dev::ldsm_x4(a_addr + (ks + 1) * 32, af2);
+            E::mma(c2[1], af2, bf[2], bf[3]);
         }
-        if (lane < 8 && i < a.d_h) {
-            float mine = acc[0];
+        T *out = static_cast<T *>(a.out);
+        const int i = i0 + 8 * warp + 2 * (lane & 3);
 #pragma unroll
-            for (int bb = 1; bb < 8; ++bb)
-                if (lane == bb) mine = acc[bb];
-            const int b = b0 + lane;
-            if (b < a.B && s_c1[lane] >= s_c0[lane]) out[(int64_t(b) * a.H + h) * a.d_h + i] = E::store(mine);
+        for (int hf = 0; hf < 2; ++hf) {
+            const int m = (lane >> 2) + 8 * hf, b = b0 + m;
+            if (b < a.B && s_c1[m] >= s_c0[m]) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (i + e < i0 + rows)
+                        out[(int64_t(b) * a.H + h) * a.d_h + i + e] = E::store(c2[0][2 * hf + e] + c2[1][2 * hf + e]);
+            }
         }
     }
 }
@@ -714,7 +752,7 @@ struct MlaKernelInfo {
     int stage_bytes;
     int fixed_smem;       // besides the stages and their barriers
     int min_stages;
-    cudaError_t (*set_max_smem)(int bytes);
+    cudaError_t (*set_max_smem)(int bytes);   // the decode kernel's, and the combine kernel's fixed size
     cudaError_t (*launch)(const MlaArgs &a, int grid, int smem, cudaStream_t s);
     cudaError_t (*absorb)(const MlaAbsorbArgs &a, cudaStream_t s);
     cudaError_t (*combine)(const MlaCombineArgs &a, cudaStream_t s);
@@ -728,6 +766,12 @@ const MlaKernelInfo *mla_info() {
         C::FIXED_SMEM,
         2,
         [](int bytes) {
+            cudaError_t e = cudaFuncSetAttribute(mla_combine_kernel<T, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 MlaCombineSmem<DC>::BYTES);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(mla_absorb_kernel<T, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     MlaAbsorbSmem<256>::BYTES);
+            if (e != cudaSuccess) return e;
             return cudaFuncSetAttribute(mla_decode_kernel<T, DC, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         },
         [](const MlaArgs &a, int grid, int smem, cudaStream_t s) {
@@ -735,13 +779,13 @@ const MlaKernelInfo *mla_info() {
             return cudaGetLastError();
         },
         [](const MlaAbsorbArgs &a, cudaStream_t s) {
-            const dim3 grid(a.H, DC / 128, (a.B + 15) / 16);
-            mla_absorb_kernel<T, DC><<<grid, 256, 0, s>>>(a);
+            const dim3 grid(a.H, DC / 64, (a.B + 63) / 64);
+            mla_absorb_kernel<T, DC><<<grid, 128, MlaAbsorbSmem<256>::BYTES, s>>>(a);
             return cudaGetLastError();
         },
         [](const MlaCombineArgs &a, cudaStream_t s) {
-            const dim3 grid(a.H, (a.B + 7) / 8, (a.d_h + 31) / 32);
-            mla_combine_kernel<T, DC><<<grid, 256, 0, s>>>(a);
+            const dim3 grid(a.H, (a.B + 15) / 16, (a.d_h + 31) / 32);
+            mla_combine_kernel<T, DC><<<grid, 512, MlaCombineSmem<DC>::BYTES, s>>>(a);
             return cudaGetLastError();
         },
     };

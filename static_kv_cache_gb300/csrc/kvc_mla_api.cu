@@ -37,7 +37,7 @@ bool mla_shape_ok(const kvc_mla_config *c) {
 }
 
 const kvc::MlaKernelInfo *find_mla(const kvc_mla_config *c) {
-    if (c->d_head % 8 != 0 || c->d_head < 16 || c->d_head > 256) return nullptr;
+    if (c->d_head % 16 != 0 || c->d_head < 16 || c->d_head > 256) return nullptr;
     if (c->dtype == KVC_BF16) return kvc::mla_kernel_bf16(c->d_latent, c->n_heads);
     if (c->dtype == KVC_FP16) return kvc::mla_kernel_f16(c->d_latent, c->n_heads);
     return nullptr;

@@ -4,8 +4,9 @@
 per token, keys and values rebuilt per head by up-projections
 (oracle.mla_decode_attn writes that definition out).  The GPU takes the
 absorbed order; its only roundings beyond fp32 accumulation are the absorbed
-query (once, to the cache type) and the probabilities fed to the tensor-core
-product (bf16 / fp16, each in [0, 1]), and the output (once).
+query and the attended latent (once each, to the cache type, as tensor-core
+operands), the probabilities fed to the tensor-core product (bf16 / fp16,
+each in [0, 1]), and the output (once).
 
 Checked: decode over ragged lengths and several split counts for every
 compiled (d_c, H) with both 16-bit types; a step sequence whose cache bytes
