@@ -633,8 +633,6 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);
     int32_t *vl_cache = reinterpret_cast<int32_t *>(scr_ml + C::SCR_ML_FLOATS) + C::N_FLAGS;
     const int32_t *vl = a.B <= C::VL_CACHE ? vl_cache : a.valid_len;
-    if (a.B <= C::VL_CACHE)
-        for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&a.tm_k32);
@@ -650,6 +648,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         flags[0] = 0;
         dev::fence_mbar_init();
     }
+    // everything above overlaps the previous kernel on the stream; nothing
+    // below runs before it has completed
+    dev::grid_dependency_wait();
+    dev::allow_dependents();
+    if (a.B <= C::VL_CACHE)
+        for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
     __syncthreads();
 
     const Plan plan = make_plan(a, vl, lane);
@@ -922,8 +926,7 @@ cudaError_t set_mma_max_smem(int bytes) {
 
 template <typename T, int D, int G>
 cudaError_t launch_mma(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
-    decode_mma_kernel<T, D, G><<<grid, MmaCfg<T, D, G>::THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_mma_kernel<T, D, G>, dim3(grid), dim3(MmaCfg<T, D, G>::THREADS), smem, s, a);
 }
 
 template <typename T, int D, int G>

@@ -180,6 +180,26 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
 // Tensor maps of paged pools [n_blocks_total][16][D] (n_blocks_total = L *
 // num_blocks * H_kv): boxes of 64 columns x 16 rows (in the *32 slots) and x 8
 // rows, 128-byte swizzle.  Host only.
+// Launch `kernel` with programmatic stream serialization, so that its CTAs may
+// be scheduled while the previous kernel on the stream drains (the kernel
+// calls dev::grid_dependency_wait before touching global memory).
+#ifdef __CUDACC__
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStream_t s, const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
+
 bool encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
                       CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8);
 
@@ -386,6 +406,15 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 __device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
     atomicCAS(err, 0, code);
 }
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream drains;
+// grid_dependency_wait blocks until that kernel has completed and its memory
+// operations are visible (immediately when there is no such kernel), so it
+// comes before the first global-memory access.  allow_dependents lets the
+// next such kernel be scheduled once every CTA of this grid has issued it.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace dev
 }  // namespace kvc

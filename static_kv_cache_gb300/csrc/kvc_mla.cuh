@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaAbsorbArgs a) 
     const int h = blockIdx.x, j0 = blockIdx.y * 64, b0 = blockIdx.z * 64;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int dh = a.d_h, vq = dh / 8;                        // 16-byte vectors per q row
+    dev::grid_dependency_wait();   // the previous kernel on the stream has completed
+    dev::allow_dependents();
     const T *q = static_cast<const T *>(a.q);
     const T *w = static_cast<const T *>(a.w_uk) + int64_t(h) * dh * DC + j0;
     for (int v = t; v < 64 * vq; v += 128) {
@@ -255,6 +257,10 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
         dev::prefetch_tensormap(&a.tm64);
         dev::prefetch_tensormap(&a.tm16);
     }
+    // the set-up above overlaps the previous kernel on the stream (the absorb);
+    // nothing below runs before it has completed
+    dev::grid_dependency_wait();
+    dev::allow_dependents();
     __syncthreads();
 
     const Plan plan = make_plan(a, a.valid_len, lane);
@@ -592,6 +598,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr unsigned FULL = 0xffffffffu;
     const int rows = min(32, a.d_h - i0);
+    dev::grid_dependency_wait();   // the previous kernel on the stream (the attention) has completed
+    dev::allow_dependents();
     {
         const T *w = static_cast<const T *>(a.w_uv) + (int64_t(h) * a.d_h + i0) * DC;
         for (int v = threadIdx.x; v < rows * (DC / 8); v += 512) {
@@ -775,18 +783,15 @@ const MlaKernelInfo *mla_info() {
             return cudaFuncSetAttribute(mla_decode_kernel<T, DC, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         },
         [](const MlaArgs &a, int grid, int smem, cudaStream_t s) {
-            mla_decode_kernel<T, DC, H><<<grid, C::THREADS, smem, s>>>(a);
-            return cudaGetLastError();
+            return launch_pdl(mla_decode_kernel<T, DC, H>, dim3(grid), dim3(C::THREADS), smem, s, a);
         },
         [](const MlaAbsorbArgs &a, cudaStream_t s) {
             const dim3 grid(a.H, DC / 64, (a.B + 63) / 64);
-            mla_absorb_kernel<T, DC><<<grid, 128, MlaAbsorbSmem<256>::BYTES, s>>>(a);
-            return cudaGetLastError();
+            return launch_pdl(mla_absorb_kernel<T, DC>, grid, dim3(128), MlaAbsorbSmem<256>::BYTES, s, a);
         },
         [](const MlaCombineArgs &a, cudaStream_t s) {
             const dim3 grid(a.H, (a.B + 15) / 16, (a.d_h + 31) / 32);
-            mla_combine_kernel<T, DC><<<grid, 512, MlaCombineSmem<DC>::BYTES, s>>>(a);
-            return cudaGetLastError();
+            return launch_pdl(mla_combine_kernel<T, DC>, grid, dim3(512), MlaCombineSmem<DC>::BYTES, s, a);
         },
     };
     return &info;
