@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t *__restrict__ K, ui
                                                      int B, int H_kv, int T_new, int max_ctx, int row_vecs,
                                                      const int32_t *__restrict__ table, int max_blocks,
                                                      int num_blocks, int32_t *err) {
+    dev::grid_dependency_wait();   // the previous kernel on the stream has completed
+    dev::allow_dependents();
     const int64_t run = int64_t(T_new) * row_vecs;   // vectors per (b, j)
     const int64_t per_tensor = int64_t(B) * H_kv * run;
     const int64_t total = V ? 2 * per_tensor : per_tensor;   // V null: one tensor (a latent cache)
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(256) append_q8_kernel(uint8_t *__restrict__ K,
                                                         int index_offset, int B, int H_kv, int T_new, int max_ctx,
                                                         int32_t *err) {
     constexpr int EPL = D / 32;  // bf16 elements per lane (2 or 4)
+    dev::grid_dependency_wait();   // the previous kernel on the stream has completed
+    dev::allow_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t rows = int64_t(B) * H_kv * T_new;       // rows per tensor
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -126,14 +130,12 @@ cudaError_t launch_append_q8(uint8_t *K_layer, uint8_t *V_layer, float *ks_layer
     const int64_t cap = int64_t(num_sms) * 8;
     const int grid = int(want < cap ? want : cap);
     if (D == 128)
-        append_q8_kernel<128><<<grid, 256, 0, stream>>>(K_layer, V_layer, ks_layer, vs_layer, k_new, v_new,
-                                                        cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
-    else if (D == 64)
-        append_q8_kernel<64><<<grid, 256, 0, stream>>>(K_layer, V_layer, ks_layer, vs_layer, k_new, v_new,
-                                                       cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(append_q8_kernel<128>, dim3(grid), dim3(256), 0, stream, K_layer, V_layer, ks_layer, vs_layer,
+                          k_new, v_new, cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
+    if (D == 64)
+        return launch_pdl(append_q8_kernel<64>, dim3(grid), dim3(256), 0, stream, K_layer, V_layer, ks_layer, vs_layer,
+                          k_new, v_new, cache_index, index_offset, B, H_kv, T_new, max_ctx, err);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_new,
@@ -146,9 +148,8 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
     const int64_t want = (total + 255) / 256;
     const int64_t cap = int64_t(num_sms) * 8;
     const int grid = int(want < cap ? want : cap);
-    append_kernel<<<grid, 256, 0, stream>>>(K_layer, V_layer, k_new, v_new, cache_index, index_offset, B, H_kv,
-                                            T_new, max_ctx, row_vecs, table, max_blocks, num_blocks, err);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3(grid), dim3(256), 0, stream, K_layer, V_layer, k_new, v_new, cache_index,
+                      index_offset, B, H_kv, T_new, max_ctx, row_vecs, table, max_blocks, num_blocks, err);
 }
 
 }  // namespace kvc

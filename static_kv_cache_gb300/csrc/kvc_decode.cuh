@@ -439,6 +439,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::THREADS, 1)
         flags[1] = 0;
         dev::fence_mbar_init();
     }
+    // the set-up above overlaps the previous kernel on the stream; nothing
+    // below runs before it has completed
+    dev::grid_dependency_wait();
+    dev::allow_dependents();
     __syncthreads();
 
     const Plan plan = make_plan(a, a.valid_len, lane);
@@ -677,8 +681,7 @@ cudaError_t set_decode_max_smem(int bytes) {
 
 template <typename T, int D, int G>
 cudaError_t launch_decode(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
-    decode_split_kernel<T, D, G><<<grid, DecodeCfg<T, D, G>::THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_kernel<T, D, G>, dim3(grid), dim3(DecodeCfg<T, D, G>::THREADS), smem, s, a);
 }
 
 template <typename T, int D, int G>

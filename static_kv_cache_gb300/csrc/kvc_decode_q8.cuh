@@ -199,8 +199,6 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
     volatile int *flags = reinterpret_cast<volatile int *>(scr_ml + C::SCR_ML_FLOATS);
     int32_t *vl_cache = reinterpret_cast<int32_t *>(scr_ml + C::SCR_ML_FLOATS) + C::N_FLAGS;
     const int32_t *vl = a.B <= C::VL_CACHE ? vl_cache : a.valid_len;
-    if (a.B <= C::VL_CACHE)
-        for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&a.tm_k32);
@@ -214,6 +212,12 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
         flags[0] = 0;
         dev::fence_mbar_init();
     }
+    // the set-up above overlaps the previous kernel on the stream (the
+    // quantising append); nothing below runs before it has completed
+    dev::grid_dependency_wait();
+    dev::allow_dependents();
+    if (a.B <= C::VL_CACHE)
+        for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
     __syncthreads();
 
     const Plan plan = make_plan(a, vl, lane);
@@ -495,8 +499,7 @@ cudaError_t set_q8_max_smem(int bytes) {
 
 template <int D, int G>
 cudaError_t launch_q8(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
-    decode_q8_kernel<D, G><<<grid, Q8Cfg<D, G>::THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_q8_kernel<D, G>, dim3(grid), dim3(Q8Cfg<D, G>::THREADS), smem, s, a);
 }
 
 template <int D, int G>

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(PrefillCfg<T, D, G>::THREADS, 2)
     const int seg = int(blockIdx.x) / a.q_blocks;       // b * H_kv + kv
     const int qb = int(blockIdx.x) % a.q_blocks;
     const int b = seg / a.H_kv, kv = seg % a.H_kv;
+    dev::grid_dependency_wait();   // the previous kernel on the stream (the chunk's append) has completed
+    dev::allow_dependents();
     const int c = __ldg(a.cache_index + b);
     if (c < 0 || c > a.max_ctx - a.T_new) {             // uniform over the CTA
         if (threadIdx.x == 0 && qb == 0 && kv == 0) dev::record_error(a.err, ERR_DEVICE_INDEX);
@@ -337,8 +339,7 @@ cudaError_t set_prefill_max_smem(int bytes) {
 
 template <typename T, int D, int G>
 cudaError_t launch_prefill(const PrefillArgs &a, int grid, int smem, cudaStream_t s) {
-    prefill_kernel<T, D, G><<<grid, PrefillCfg<T, D, G>::THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel<T, D, G>, dim3(grid), dim3(PrefillCfg<T, D, G>::THREADS), smem, s, a);
 }
 
 template <typename T, int D, int G>
