@@ -41,6 +41,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_mma.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_decode_q8.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_mla.cuh",
                   "static_kv_cache_gb300/csrc/kvc_internal.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_inst.cu")
 
