@@ -73,6 +73,22 @@ const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
     return nullptr;
 }
 
+// Kernel for a paged pool: the tensor-core kernel (16-bit, 2 to 8 query heads
+// per KV head); for d_h = 128 the variant whose consumers read the half-row
+// tile layout the paged producer writes, for d_h = 64 the contiguous cache's
+// kernel (the layouts coincide).  Null otherwise.
+const kvc::DecodeKernelInfo *find_decode_paged(const kvc_config *c) {
+    const int G = c->n_heads / c->n_kv_heads;
+    if (G < 2 || G > 8) return nullptr;
+    if (c->d_head == 128) {
+        if (c->dtype == KVC_BF16) return kvc::decode_kernel_paged_bf16_128(G);
+        if (c->dtype == KVC_FP16) return kvc::decode_kernel_paged_f16_128(G);
+        return nullptr;
+    }
+    if (c->d_head == 64 && (c->dtype == KVC_BF16 || c->dtype == KVC_FP16)) return find_decode(c);
+    return nullptr;
+}
+
 // Chunked-prefill kernel: 16-bit caches with d_h 64 or 128.
 const kvc::PrefillKernelInfo *find_prefill(const kvc_config *c) {
     const int G = c->n_heads / c->n_kv_heads;
@@ -149,11 +165,14 @@ bool kvc::encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const v
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16)) return false;
     const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const cuuint64_t dims[3] = {cuuint64_t(D), 16, cuuint64_t(n_blocks_total)};
-    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, 16ull * D * 2};
+    // each block of one KV head (16 rows of D elements) viewed as HR rows of
+    // 128 bytes: a box of 64 columns x HR covers the whole block with one copy
+    const cuuint32_t HR = cuuint32_t(16 * (D / 64));
+    const cuuint64_t dims[3] = {64, HR, cuuint64_t(n_blocks_total)};
+    const cuuint64_t strides[2] = {128, cuuint64_t(HR) * 128};
     const cuuint32_t elem[3] = {1, 1, 1};
     struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
-    const Job jobs[4] = {{k_pool, 16, k16}, {k_pool, 8, k8}, {v_pool, 16, v16}, {v_pool, 8, v8}};
+    const Job jobs[4] = {{k_pool, HR, k16}, {k_pool, HR / 2, k8}, {v_pool, HR, v16}, {v_pool, HR / 2, v8}};
     for (const Job &j : jobs) {
         const cuuint32_t box[3] = {64, j.rows, 1};
         if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -220,7 +239,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
                       int32_t num_blocks = 0) {
     if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
     if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
-    const kvc::DecodeKernelInfo *info = find_decode(cfg);
+    const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode(cfg);
     if (!info) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
         return KVC_ERR_ALIGNMENT;
@@ -315,8 +334,7 @@ kvc_status kvc_alloc_paged(const kvc_config *cfg, void *k_pool, void *v_pool, in
                            const int32_t *block_table, void *workspace, uint64_t ws_bytes, kvc_cache **out) {
     if (!cfg || !block_table || num_blocks <= 0 || cfg->max_context % 16 != 0) return KVC_ERR_INVALID;
     if (cfg->dtype == KVC_INT8) return KVC_ERR_UNSUPPORTED;
-    const kvc::DecodeKernelInfo *info = shape_ok(cfg) ? find_decode(cfg) : nullptr;
-    if (info && !info->tensor_maps) return KVC_ERR_UNSUPPORTED;  // the paged producer is the TMA kernel's
+    if (shape_ok(cfg) && !find_decode_paged(cfg)) return KVC_ERR_UNSUPPORTED;  // the paged producer is the TMA kernel's
     if (!aligned16(block_table)) return KVC_ERR_ALIGNMENT;
     return alloc_impl(cfg, k_pool, v_pool, nullptr, nullptr, workspace, ws_bytes, out, block_table, num_blocks);
 }

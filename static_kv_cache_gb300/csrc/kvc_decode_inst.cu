@@ -36,6 +36,27 @@ namespace kvc {
 #define KVC_GROUPED(G) decode_info<KVC_ELEM, KVC_INST_D, G>()
 #endif
 
+#if defined(KVC_INST_PAGED)
+// Kernels for paged pools with d_h = 128 (tiles in the half-row layout); the
+// build compiles this variant once per 16-bit type.
+#if KVC_INST_D != 128 || KVC_INST_TYPE == 2
+#error "the paged variant is built for 16-bit caches with d_h = 128"
+#endif
+#define KVC_PCAT2(a) decode_kernel_paged_##a##_128
+#define KVC_PCAT(a) KVC_PCAT2(a)
+const DecodeKernelInfo *KVC_PCAT(KVC_TAG)(int G) {
+    switch (G) {
+        case 2: return mma_decode_info<KVC_ELEM, 128, 2, true>();
+        case 3: return mma_decode_info<KVC_ELEM, 128, 3, true>();
+        case 4: return mma_decode_info<KVC_ELEM, 128, 4, true>();
+        case 5: return mma_decode_info<KVC_ELEM, 128, 5, true>();
+        case 6: return mma_decode_info<KVC_ELEM, 128, 6, true>();
+        case 7: return mma_decode_info<KVC_ELEM, 128, 7, true>();
+        case 8: return mma_decode_info<KVC_ELEM, 128, 8, true>();
+        default: return nullptr;
+    }
+}
+#else
 const DecodeKernelInfo *KVC_TABLE_FN(int G) {
     switch (G) {
         case 1: return decode_info<KVC_ELEM, KVC_INST_D, 1>();
@@ -49,5 +70,6 @@ const DecodeKernelInfo *KVC_TABLE_FN(int G) {
         default: return nullptr;
     }
 }
+#endif
 
 }  // namespace kvc

@@ -108,6 +108,13 @@ struct MmaCfg {
         return tile + uint32_t(col >> 6) * BLOCK_BYTES + uint32_t(r) * 128 +
                uint32_t((((col >> 3) & 7) ^ (r & 7)) << 4);
     }
+    // The same for a tile filled from a paged pool: rows of D elements kept
+    // whole, i.e. 128-byte half-rows hr = r * (D / 64) + col / 64 in order, the
+    // swizzle keyed on hr.  For D = 64 both layouts coincide.
+    __device__ __forceinline__ static uint32_t swz_pg(uint32_t tile, int r, int col) {
+        const uint32_t hr = uint32_t(r) * (D / 64) + uint32_t(col >> 6);
+        return tile + hr * 128 + uint32_t((((col >> 3) & 7) ^ int(hr & 7)) << 4);
+    }
 };
 
 // The producer warp: walks the CTA's pieces; for each tile one lane issues
@@ -213,7 +220,7 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
 template <typename C>
 __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Walker walk, uint32_t stage0,
                                                         uint32_t bar0, int ns, volatile int *flags, int lane) {
-    constexpr int TILE = C::TILE, CB = C::ROW_BYTES / 128, BS = 16;
+    constexpr int TILE = C::TILE, BS = 16;
     static_assert(TILE == 2 * BS, "a tile is two blocks");
     constexpr unsigned FULL = 0xffffffffu;
     const int64_t block_bytes = int64_t(BS) * C::ROW_BYTES;  // one KV head's rows of a block
@@ -270,15 +277,14 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
                     if (!boxed[jj]) continue;
+                    // one box per tensor covers the block's 16 (or first 8)
+                    // whole rows: the pool viewed as 128-byte half-rows
                     const int z = a.seg_base + phys[jj] * a.H_kv + pc.kv;
                     const CUtensorMap *mk = boxed[jj] == BS ? &a.tm_k32 : &a.tm_k8;
                     const CUtensorMap *mv = boxed[jj] == BS ? &a.tm_v32 : &a.tm_v8;
-#pragma unroll
-                    for (int cb = 0; cb < CB; ++cb) {
-                        const uint32_t off = cb * C::BLOCK_BYTES + jj * BS * 128;
-                        dev::tma_load_3d(kdst + off, mk, cb * 64, 0, z, full);
-                        dev::tma_load_3d(vdst + off, mv, cb * 64, 0, z, full);
-                    }
+                    const uint32_t off = jj * BS * C::ROW_BYTES;
+                    dev::tma_load_3d(kdst + off, mk, 0, 0, z, full);
+                    dev::tma_load_3d(vdst + off, mv, 0, 0, z, full);
                 }
             }
             bool generic = false;
@@ -298,7 +304,7 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
                         logical == new_row
                             ? (is_v ? a.v_new : a.k_new) + (int64_t(pc.b) * a.H_kv + pc.kv) * C::ROW_BYTES + c16 * 16
                             : (is_v ? a.V : a.K) + blk_off + int64_t(r) * C::ROW_BYTES + c16 * 16;
-                    dev::cp_async_16(C::swz(is_v ? vdst : kdst, BS * jj + r, c16 * 8), src);
+                    dev::cp_async_16(C::swz_pg(is_v ? vdst : kdst, BS * jj + r, c16 * 8), src);
                 }
             }
             if (generic) {
@@ -610,10 +616,14 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
     return false;
 }
 
-template <typename T, int D, int G>
+// PG: the tiles come from a paged pool in the half-row layout (MmaCfg::swz_pg);
+// only the d_h = 128 kernels need it (for d_h = 64 the layouts coincide).
+template <typename T, int D, int G, bool PG = false>
 __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
     using C = MmaCfg<T, D, G>;
+    constexpr bool PAGED_OK = PG || D == 64;         // the paged producer's layout is this kernel's
+    constexpr bool PGL = PG && D != 64;              // consumers address the half-row layout
     using Ops = MmaOps<T>;
     constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS;
     constexpr unsigned FULL = 0xffffffffu;
@@ -665,9 +675,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
-        const uint32_t issued = a.block_table
-                                    ? produce_tiles_paged<C>(a, walk, stage0, bar0, ns, flags, lane)
-                                    : produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
+        uint32_t issued;
+        if constexpr (PAGED_OK)
+            issued = a.block_table ? produce_tiles_paged<C>(a, walk, stage0, bar0, ns, flags, lane)
+                                   : produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
+        else
+            issued = produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
         dev::named_barrier_sync(2, C::THREADS);  // every warp is done
         if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);
@@ -728,6 +741,21 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         koff[j] = swz_lane_offset(k_row, k_half, lane, j);
         voff[j] = swz_lane_offset(v_row, v_half, lane, j);
     }
+    // the half-row layout of a paged tile: row r of the tile is D / 64
+    // half-rows hr = r * D/64 + col / 64, the swizzle keyed on hr mod 8
+    constexpr int CBK = PGL ? D / 64 : 1;
+    uint32_t koffp[CBK][4], voffp[CBK][4];
+    if constexpr (PGL) {
+#pragma unroll
+        for (int cb = 0; cb < CBK; ++cb)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                koffp[cb][j] = uint32_t(k_row * C::ROW_BYTES + cb * 128) +
+                               (uint32_t((2 * j + k_half) ^ ((k_row * CBK + cb) & 7)) << 4);
+                voffp[cb][j] = uint32_t(v_row * C::ROW_BYTES + cb * 128) +
+                               (uint32_t((2 * j + v_half) ^ ((v_row * CBK + cb) & 7)) << 4);
+            }
+    }
 
     uint32_t qb[KSTEPS][2];
     float o[KSTEPS][4];
@@ -787,7 +815,10 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     uint32_t r[4];
-                    dev::ldsm_x4(ks_base + (ks >> 2) * C::BLOCK_BYTES + mt * 2048 + koff[ks & 3], r);
+                    if constexpr (PGL)
+                        dev::ldsm_x4(ks_base + mt * 16 * C::ROW_BYTES + koffp[ks >> 2][ks & 3], r);
+                    else
+                        dev::ldsm_x4(ks_base + (ks >> 2) * C::BLOCK_BYTES + mt * 2048 + koff[ks & 3], r);
                     Ops::mma(s[mt], r, qb[ks][0], qb[ks][1]);
                 }
             }
@@ -848,7 +879,10 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
                     uint32_t r[4];
-                    dev::ldsm_x4_trans(vs_base + (mt >> 2) * C::BLOCK_BYTES + kst * 2048 + voff[mt & 3], r);
+                    if constexpr (PGL)
+                        dev::ldsm_x4_trans(vs_base + kst * 16 * C::ROW_BYTES + voffp[mt >> 2][mt & 3], r);
+                    else
+                        dev::ldsm_x4_trans(vs_base + (mt >> 2) * C::BLOCK_BYTES + kst * 2048 + voff[mt & 3], r);
                     if (nr < TILE) {  // stale rows past the copied ones
                         const int k0 = kst * 16 + 2 * tq;
                         r[0] = live_pair(r[0], k0, nr);
@@ -918,22 +952,23 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     dev::named_barrier_sync(2, C::THREADS);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool PG>
 cudaError_t set_mma_max_smem(int bytes) {
-    return cudaFuncSetAttribute(decode_mma_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(decode_mma_kernel<T, D, G, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 bytes);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool PG>
 cudaError_t launch_mma(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
-    return launch_pdl(decode_mma_kernel<T, D, G>, dim3(grid), dim3(MmaCfg<T, D, G>::THREADS), smem, s, a);
+    return launch_pdl(decode_mma_kernel<T, D, G, PG>, dim3(grid), dim3(MmaCfg<T, D, G>::THREADS), smem, s, a);
 }
 
-template <typename T, int D, int G>
+// PG: the kernel for paged pools with d_h = 128 (the half-row tile layout).
+template <typename T, int D, int G, bool PG = false>
 const DecodeKernelInfo *mma_decode_info() {
     using C = MmaCfg<T, D, G>;
     static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
-                                          &set_mma_max_smem<T, D, G>, &launch_mma<T, D, G>, true};
+                                          &set_mma_max_smem<T, D, G, PG>, &launch_mma<T, D, G, PG>, true};
     return &info;
 }
 

@@ -119,6 +119,9 @@ KVC_DECLARE_DECODE_TABLE(f32, 128)
 KVC_DECLARE_DECODE_TABLE(f32, 256)
 KVC_DECLARE_DECODE_TABLE(q8, 128)
 #undef KVC_DECLARE_DECODE_TABLE
+// paged pools with d_h = 128: the tensor-core kernel in the half-row tile layout
+const DecodeKernelInfo *decode_kernel_paged_bf16_128(int G);
+const DecodeKernelInfo *decode_kernel_paged_f16_128(int G);
 
 // Arguments of the chunked-prefill kernel (grid constant).
 struct PrefillArgs {
@@ -177,9 +180,6 @@ cudaError_t launch_append(uint8_t *K_layer, uint8_t *V_layer, const uint8_t *k_n
                           int num_sms, cudaStream_t stream, const int32_t *table = nullptr,
                           int max_blocks = 0, int num_blocks = 0);
 
-// Tensor maps of paged pools [n_blocks_total][16][D] (n_blocks_total = L *
-// num_blocks * H_kv): boxes of 64 columns x 16 rows (in the *32 slots) and x 8
-// rows, 128-byte swizzle.  Host only.
 // Launch `kernel` with programmatic stream serialization, so that its CTAs may
 // be scheduled while the previous kernel on the stream drains (the kernel
 // calls dev::grid_dependency_wait before touching global memory).
@@ -200,6 +200,10 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStrea
 }
 #endif
 
+// Tensor maps of paged pools [n_blocks_total][16][D] (n_blocks_total = L *
+// num_blocks * H_kv), each block viewed as 16 * D/64 rows of 128 bytes: boxes
+// of 64 columns x all of them (a whole block, in the *32 slots) and x half of
+// them (its first 8 rows), 128-byte swizzle.  Host only.
 bool encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
                       CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8);
 
