@@ -212,9 +212,10 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
 // The producer for a paged cache: a tile of 32 rows starts on a block
 // boundary (the split space is rounded to 16 rows per segment), so it is the
 // first 16 rows of two logical blocks.  Their physical blocks come from the
-// block table, 32 entries at a time (one per lane, shared by shuffles); a
-// full block arrives as one 16-row box per 64-column block of K and of V, a
-// partial one as an 8-row box and 16-byte cp.async copies.  A table entry
+// block table, 32 entries at a time (one per lane, shared by shuffles, the
+// next 32 loaded ahead); a full block arrives as one box of K and one of V
+// (the pool viewed as 128-byte half-rows), a partial one as an 8-row box and
+// 16-byte cp.async copies.  A table entry
 // outside [0, num_blocks) is recorded as a device-index error and its block
 // is not copied.
 template <typename C>
@@ -232,26 +233,24 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
     while (ok && walk.next(a, pc)) {
         const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
         const int new_row = a.k_new ? pc.n - 1 : -1;
-        int cached_base = -1 << 30;
-        int32_t cached = -1;  // lane l: physical block of logical block cached_base + l
+        // Table entries in windows of 32 (lane l: logical block base + l), one
+        // window ahead: tile t of the piece needs blocks first + 2t and
+        // first + 2t + 1, both in window t / 16; window k + 1 is loaded when
+        // window k comes into use, so its latency hides behind 16 tiles.
+        const int first = pc.lo / BS;
+        auto load_window = [&](int base) { return base + lane < a.max_blocks ? __ldg(trow + base + lane) : -1; };
+        int32_t cached = load_window(first);
+        int32_t ahead = load_window(first + 32);
+        int cached_base = first;
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE) {
             const int nr = min(TILE, pc.hi - row0);
-            if (round > 0) {
-                const bool w =
-                    dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns);
-                if (!__all_sync(FULL, w)) {
-                    if (lane == 0) {
-                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
-                        flags[0] = 1;
-                    }
-                    ok = false;
-                    break;
-                }
-            }
+            // the tile's blocks first: none of this needs the stage, so it
+            // stays off the path from the stage's release to its refill
             const int blk0 = row0 / BS;
-            if (blk0 + 1 >= cached_base + 32) {
-                cached_base = blk0;
-                cached = blk0 + lane < a.max_blocks ? __ldg(trow + blk0 + lane) : -1;
+            if (blk0 >= cached_base + 32) {   // the next window: already loaded
+                cached_base += 32;
+                cached = ahead;
+                ahead = load_window(cached_base + 32);
             }
             int phys[2], rows[2], boxed[2];
             uint32_t tx_rows = 0;
@@ -267,6 +266,18 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
                     rows[jj] = boxed[jj] = 0;  // not copied: its rows stay stale
                 }
                 tx_rows += uint32_t(boxed[jj]);
+            }
+            if (round > 0) {
+                const bool w =
+                    dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns);
+                if (!__all_sync(FULL, w)) {
+                    if (lane == 0) {
+                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                        flags[0] = 1;
+                    }
+                    ok = false;
+                    break;
+                }
             }
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
