@@ -63,3 +63,50 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_step_bytes_paged_and_mla():
+    """A paged step adds the 4-byte table entries of the live rows; an MLA
+    step reads each latent row once for all heads plus the two
+    up-projections."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from static_kv_cache_gb300 import synth
+    lengths = [1024, 17, 4000]
+    dense = bench.step_bytes(synth.WORKLOADS["llama3_8b"].with_(batch=3), lengths)
+    paged = bench.step_bytes(synth.WORKLOADS["llama3_8b_paged"].with_(batch=3), lengths)
+    assert paged["attn"] - dense["attn"] == 4 * (64 + 2 + 250)
+    assert paged["append"] == dense["append"]
+    w = synth.WORKLOADS["mla_dsv2"].with_(batch=3)
+    m = bench.step_bytes(w, lengths)
+    assert m["attn"] == sum(lengths) * 512 * 2 + 2 * 3 * 16 * 128 * 2 + 2 * 16 * 128 * 512 * 2
+    assert m["append"] == 2 * 3 * 512 * 2
+
+
+def test_block_table_covers_the_live_rows_once():
+    """The bench's paged inputs: each sequence gets ceil(valid / 16) distinct
+    physical blocks of a pool of exactly that many, unused entries 0."""
+    import numpy as np
+    from static_kv_cache_gb300 import synth
+    lengths = [1, 16, 17, 4096, 33]
+    table, nb = synth.block_table(lengths, 4096, seed=3)
+    need = [(n + 15) // 16 for n in lengths]
+    assert nb == sum(need) and table.shape == (5, 256) and table.dtype == np.int32
+    used = np.concatenate([table[b, :n] for b, n in enumerate(need)])
+    assert sorted(used.tolist()) == list(range(nb))
+    for b, n in enumerate(need):
+        assert (table[b, n:] == 0).all()
+
+
+def test_reference_arm_paged_and_mla_lines():
+    """The reference arm runs the oracle's paged gather and its MLA decode
+    on the same workloads the GPU arm measures."""
+    for wl in ("llama3_8b_paged", "mla_dsv2"):
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                            "--workload", wl, "--steps", "2", "--warmup", "0"],
+                           capture_output=True, text=True, timeout=600, cwd=ROOT)
+        assert r.returncode == 0, r.stderr
+        d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+        assert d["impl"] == "reference" and d["value"] > 0
+        assert ("block table" in d["cpu_baseline"]["sample"]) == (wl == "llama3_8b_paged")
+        assert ("MLA" in d["cpu_baseline"]["sample"]) == (wl == "mla_dsv2")
