@@ -118,6 +118,20 @@ def test_mla_decode_matches_the_oracle(shape, splits):
     assert hn.canaries_intact()
 
 
+@pytest.mark.parametrize("B,d_h", [(70, 128), (5, 256), (17, 16)])
+def test_mla_batch_and_head_width_edges(B, d_h):
+    """More than 64 sequences (a second absorb block), and the narrowest and
+    widest head widths the kernels take."""
+    lengths = [(37 * b) % 300 + 1 for b in range(B)]
+    hn = MlaHarness(1, B, 16, d_h, 256, 304, "bf16", seed=4600 + B + d_h)
+    hn.fill(0, lengths)
+    q = hn.query("edge")
+    out = hn.decode(0, q, lengths)
+    assert hn.kvc.kvc_mla_get_error(hn.h) == 0
+    mla_compare(out, hn.reference(0, q, lengths), f"B={B} d_h={d_h}")
+    assert hn.canaries_intact()
+
+
 @pytest.mark.parametrize("q_scale", [4.0])
 def test_mla_peaky_attention(q_scale):
     lengths = [300, 41, 512]

@@ -83,6 +83,7 @@ class PagedHarness:
 CASES = [
     # dtype, D, H, H_kv, B, T, lengths
     ("bf16", 128, 32, 8, 5, 704, [704, 1, 333, 40, 17]),
+    ("fp16", 128, 12, 2, 3, 400, [400, 9, 255]),
     ("fp16", 64, 12, 2, 3, 512, [512, 31, 257]),
     ("bf16", 128, 16, 2, 2, 1600, [1600, 15]),
     ("bf16", 64, 8, 1, 1, 2048, [2048]),
