@@ -242,7 +242,8 @@ def test_mla_full_size_sampled():
 def test_mla_host_errors():
     from static_kv_cache_gb300 import kvc
     buf = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
-    ws = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kvc.kvc_mla_workspace_bytes(kvc.make_mla_config(1, 2, 16, 128, 512, 64, "bf16")),
+                     dtype=torch.uint8, device="cuda")
     def alloc(*shape):
         cfg = kvc.make_mla_config(*shape)
         return kvc.kvc_mla_alloc(cfg, buf, ws, ws.numel())[0]
