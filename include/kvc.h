@@ -46,6 +46,13 @@
  *     Rewinding a sequence is lowering its length on the caller's side.
  *   - Calls on one handle that overlap on the GPU (different streams without
  *     ordering) race on the workspace; order them on one stream.
+ *   - Every kernel is launched with programmatic stream serialization: its
+ *     set-up may overlap the previous kernel on the stream, and it touches no
+ *     global memory before that kernel has completed and its writes are
+ *     visible, so stream order holds as for ordinary launches.  A kernel the
+ *     caller launches right after a library call with the same attribute, and
+ *     that does not wait (griddepcontrol.wait) itself, may start before the
+ *     library's kernel has finished.
  */
 #ifndef KVC_H
 #define KVC_H
