@@ -74,6 +74,8 @@ def parse_args(argv=None):
                    help="wall time budget of the CPU-oracle baseline sample")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="time direct calls instead of a CUDA graph of one step")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args(argv)
 
@@ -546,6 +548,32 @@ def bench_kvc(args, rank, world, local):
             state.step(stream)
     torch.cuda.synchronize()
 
+    # One step (every layer's call) captured as a CUDA graph and replayed: the
+    # calls only enqueue kernels on the stream, so the graph holds exactly the
+    # launches a direct step makes, without the host in the loop.
+    # A graph holds `per_graph` consecutive steps (a divisor of the step count,
+    # at most 8), so consecutive steps still overlap inside it.
+    graph, graph_note = None, "direct calls (--no-graph)"
+    per_graph = max(d for d in range(1, 9) if args.steps % d == 0)
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                g.capture_begin()
+                try:
+                    for _ in range(per_graph):
+                        state.step(stream)
+                finally:
+                    g.capture_end()
+            with torch.cuda.stream(stream):
+                for _ in range(max(3, args.warmup)):
+                    g.replay()
+            torch.cuda.synchronize()
+            graph, graph_note = g, f"CUDA graph of {per_graph} steps (every layer's call), replayed"
+        except Exception as exc:  # capture not available: time direct calls
+            graph, graph_note = None, f"direct calls (graph capture failed: {str(exc)[:120]})"
+    launches_per_step = state.launches_per_layer * w.n_layers
+
     # --- device-timed region: events at its two ends only (an event between
     # two launches would keep the second from overlapping the first's drain)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -558,8 +586,13 @@ def bench_kvc(args, rank, world, local):
     launches = 0
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for s in range(args.steps):
-            launches += state.step(stream)
+        if graph is not None:
+            for _ in range(args.steps // per_graph):
+                graph.replay()
+                launches += launches_per_step * per_graph
+        else:
+            for _ in range(args.steps):
+                launches += state.step(stream)
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -628,7 +661,8 @@ def bench_kvc(args, rank, world, local):
                          "bytes_per_launch": per_layer["attn"] + per_layer["append"],
                          "mean_launch_us": round(mean_decode_s * 1e6, 3),
                          "launches_per_call": state.launches_per_layer,
-                         "timing": "timed region / (steps x layers): one kvc decode-step call per layer, gaps included"},
+                         "timing": "timed region / (steps x layers): one kvc decode-step call per layer, gaps included",
+                         "launch": graph_note},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

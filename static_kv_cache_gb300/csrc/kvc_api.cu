@@ -384,14 +384,19 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
                          const void *v_new) {
     const kvc_config &c = h->cfg;
 
-    // Splits: every SM streams an equal share of the live rows; tiny
-    // problems use fewer CTAs so that each still gets several tiles.
+    // Splits: every SM streams an equal share of the live rows; small
+    // problems use fewer CTAs so that each still gets several tiles.  When
+    // the problem is small and every segment (sequence, KV head) holds at
+    // most 64 KB per tensor, one CTA per segment: the step is latency there,
+    // and a CTA that owns a whole segment needs no split combine.
     int grid = h->num_splits;
     if (grid == 0) {
-        const int64_t upper_rows =
-            int64_t(c.batch) * c.n_kv_heads * (max_valid_hint > 0 ? max_valid_hint : c.max_context);
+        const int64_t seg_rows = max_valid_hint > 0 ? max_valid_hint : c.max_context;
+        const int64_t upper_rows = int64_t(c.batch) * c.n_kv_heads * seg_rows;
         const int64_t min_rows = 4 * int64_t(h->decode->tile_rows);
         int64_t want = (upper_rows + min_rows - 1) / min_rows;
+        const int64_t segs = int64_t(c.batch) * c.n_kv_heads;
+        if (want < h->num_sms && segs <= h->num_sms && seg_rows * c.d_head * h->elem_bytes <= 65536) want = segs;
         if (want > h->num_sms) want = h->num_sms;
         if (want < 1) want = 1;
         grid = int(want);

@@ -157,6 +157,10 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
                                (max_valid_hint > 0 ? max_valid_hint : cfg->max_context);
     const int64_t min_rows = 4 * int64_t(info->tile_rows);
     int64_t grid = (upper_rows + min_rows - 1) / min_rows;
+    // small problem with short segments: one CTA per segment (no split combine)
+    const int64_t nseg = int64_t(cfg->batch) * cfg->n_kv_heads;
+    const int64_t seg_rows = max_valid_hint > 0 ? max_valid_hint : cfg->max_context;
+    if (grid < ds->num_sms && nseg <= ds->num_sms && seg_rows * cfg->d_head * eb <= 65536) grid = nseg;
     if (grid > ds->num_sms) grid = ds->num_sms;
     if (grid > kvc::MAX_CTAS) grid = kvc::MAX_CTAS;
     if (grid < 1) grid = 1;
