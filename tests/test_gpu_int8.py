@@ -208,3 +208,36 @@ def test_int8_host_errors():
     vl = torch.ones(2, dtype=torch.int32, device="cuda")
     st = kvc.kvc_decode_attn_static(cfg8, 0, hn.kbuf.ptr(), hn.vbuf.ptr(), q, vl, 1, out, None)
     assert st == kvc.KVC_ERR_UNSUPPORTED
+
+
+def test_int8_full_size_step_sampled():
+    """The bench's int8 configuration: the Llama-3 layer (B=16, ragged
+    U{1024..8192}) filled through the quantising append, one decode step;
+    sampled sequences checked against the oracle over their dequantised rows."""
+    w = synth.WORKLOADS["llama3_8b_int8"]
+    lengths = synth.live_lengths(w).tolist()
+    hn = Q8Harness(1, w.batch, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, seed=2600)
+    pre = [n - 1 for n in lengths]
+    k, v = hn.rows(max(pre), "full-pre")
+    for b, n in enumerate(pre):
+        ci = torch.full((w.batch,), w.max_context + 1, dtype=torch.int32, device="cuda")
+        ci[b] = 0
+        assert hn.kvc.kvc_append(hn.h, 0, k[:, :, :n].contiguous(), v[:, :, :n].contiguous(), ci, n, None) == 0
+    hn.kvc.kvc_get_error(hn.h, None)   # the skipped sequences' index errors
+    kn, vn = hn.rows(1, "full-step")
+    q = hn.query("full-step")
+    vl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    out = torch.empty((w.batch, w.n_heads, w.d_head), dtype=torch.bfloat16, device="cuda")
+    assert hn.kvc.kvc_decode_step(hn.h, 0, q, kn, vn, vl, w.max_context, out, None) == 0
+    assert hn.kvc.kvc_get_error(hn.h, None) == 0
+    qd = oracle.widen(_gpu.bits(q), "bf16")
+    for b in (0, 7, 15):
+        n = lengths[b]
+        codes_k = hn.K[0, b:b + 1, :, :n].cpu().numpy()
+        codes_v = hn.V[0, b:b + 1, :, :n].cpu().numpy()
+        sk = hn.KS[0, b:b + 1, :, :n].cpu().numpy().view(np.float32)
+        sv = hn.VS[0, b:b + 1, :, :n].cpu().numpy().view(np.float32)
+        ref = oracle.decode_attn(qd[b:b + 1], dequantize_rows(codes_k, sk), dequantize_rows(codes_v, sv),
+                                 np.array([n]), "fp64")
+        _gpu.compare(out[b:b + 1], ref, "bf16", f"int8 full size, sequence {b} (valid {n})")
+    assert hn.canaries_intact()

@@ -203,3 +203,29 @@ def test_paged_host_errors():
     q = torch.empty((2, 8, 4, 128), dtype=torch.bfloat16, device="cuda")
     ci = torch.zeros(2, dtype=torch.int32, device="cuda")
     assert kvc.kvc_prefill_attn(hn.h, 0, q, ci, 4, q, None) == kvc.KVC_ERR_UNSUPPORTED
+
+
+def test_paged_full_size_sampled():
+    """The bench's paged configuration: the Llama-3 layer (B=16, ragged
+    U{1024..8192}) in 16-row blocks under a random table, one fused step;
+    sampled sequences checked against the oracle over the gathered rows."""
+    w = synth.WORKLOADS["llama3_8b_paged"]
+    lengths = synth.live_lengths(w).tolist()
+    hn = PagedHarness(1, w.batch, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype,
+                      num_blocks=w.batch * (w.max_context // 16) + 5, seed=3600)
+    hn.fill(0, [n - 1 for n in lengths], "full")
+    k, v = hn.rows(1, "full-step")
+    q = hn.query("full-step")
+    vl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    out = torch.empty((w.batch, w.n_heads, w.d_head), dtype=hn.tdt, device="cuda")
+    assert hn.kvc.kvc_decode_step(hn.h, 0, q, k, v, vl, w.max_context, out) == 0
+    assert hn.kvc.kvc_get_error(hn.h, None) == 0
+    kp, vp = _gpu.bits(hn.K[0]), _gpu.bits(hn.V[0])
+    for b in (0, 5, 11, 15):
+        n = lengths[b]
+        Kd = paged.gather(kp, hn.table_host[b:b + 1], n)
+        Vd = paged.gather(vp, hn.table_host[b:b + 1], n)
+        assert np.array_equal(Kd[0, :, n - 1], _gpu.bits(k)[b, :, 0]), "new row written through the table"
+        ref = oracle.decode_attn(_gpu.bits(q)[b:b + 1], Kd, Vd, np.array([n]), w.dtype)
+        _gpu.compare(out[b:b + 1], ref, w.dtype, f"paged full size, sequence {b} (valid {n})")
+    assert hn.canaries_intact()

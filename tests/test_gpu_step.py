@@ -179,3 +179,37 @@ def test_step_host_errors():
     assert kvc.kvc_decode_step(hn.h, 0, q, k.data_ptr() + 2, v, vl, 1, out, None) == kvc.KVC_ERR_ALIGNMENT
     assert kvc.kvc_decode_step(None, 0, q, k, v, vl, 1, out, None) == kvc.KVC_ERR_INVALID
     assert hn.error() == 0
+
+
+@pytest.mark.parametrize("layers", [(0, 31)])
+def test_full_size_fused_step_llama3(layers):
+    """The bench's configuration: the Llama-3-shaped cache (32 layers, B=16,
+    ragged U{1024..8192}) stepped through kvc_decode_step, one fused launch
+    per layer; sampled layers checked against the oracle and the new rows
+    checked in place."""
+    w = synth.WORKLOADS["llama3_8b"]
+    hn = _gpu.Harness(w)
+    lengths = synth.live_lengths(w)
+    pre = (lengths - 1).tolist()
+    maxlen = int(lengths.max())
+    host = {}
+    for layer in layers:
+        _gpu.fill_prefix(hn, layer, pre)
+        host[layer] = (_gpu.bits(hn.K[layer, :, :, :maxlen]).copy(), _gpu.bits(hn.V[layer, :, :, :maxlen]).copy())
+    valid = lengths.cuda()
+    for layer in layers:
+        k, v = _gpu.new_rows(w, 1, "full-step", layer)
+        q = _gpu.query(w, "full-step", layer)
+        st, out = hn.step(layer, q, k, v, valid, hint=maxlen)
+        assert st == 0
+        Kh, Vh = host[layer]
+        kb, vb = _gpu.bits(k), _gpu.bits(v)
+        for b in range(w.batch):
+            Kh[b, :, pre[b]] = kb[b, :, 0]
+            Vh[b, :, pre[b]] = vb[b, :, 0]
+            assert np.array_equal(_gpu.bits(hn.K[layer, b, :, pre[b]]), kb[b, :, 0]), "new K row in place"
+            assert np.array_equal(_gpu.bits(hn.V[layer, b, :, pre[b]]), vb[b, :, 0]), "new V row in place"
+        ref = oracle.decode_attn(_gpu.bits(q), Kh, Vh, lengths.numpy(), w.dtype)
+        _gpu.compare(out, ref, w.dtype, f"fused step, layer {layer}")
+    assert hn.error() == 0
+    assert hn.canaries_intact()
