@@ -565,19 +565,19 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
 // of b's splits (slots [c0 + b, c1 + b], the CTAs whose ranges meet b's rows)
 // into o~ = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), round it once to
 // the cache type, then out[b, h] = W_UV[h] o~ on mma.sync (fp32
-// accumulation), rounded once.  Grid (H, ceil(B / 16), ceil(d_h / 32)), 512
-// threads.  The block's 32 rows of W_UV[h] start towards shared memory
+// accumulation), rounded once.  Grid (H, ceil(B / 16), ceil(d_h / 64)), 512
+// threads.  The block's 64 rows of W_UV[h] start towards shared memory
 // (cp.async) first; meanwhile warp k folds sequence 16 y + k (its lanes over
 // the splits, then over the columns, every split's loads issued together);
-// then warps 0-3 each take one
-// 8-row n-tile of the block's rows against the 16 sequences over all of d_c.
-// The d_h / 32 blocks of a (head, 16 sequences) pair fold the same partials.
+// then warps 0-7 each take one 8-row n-tile of the block's rows against the
+// 16 sequences over all of d_c.  The d_h / 64 blocks of a (head, 16
+// sequences) pair fold the same partials.
 // A sequence with an out-of-range length has no partials and keeps its out.
 template <int DC>
 struct MlaCombineSmem {
     static constexpr int AS = DC + 8;                     // row stride of o~ and of W rows, elements
     static constexpr int A = 16 * AS * 2;                 // o~ of 16 sequences
-    static constexpr int W = 32 * AS * 2;                 // 32 rows of W_UV[h]
+    static constexpr int W = 64 * AS * 2;                 // 64 rows of W_UV[h]
     static constexpr int WTS = 16 * MLA_MAX_CTAS * 4;     // split weights
     static constexpr int BYTES = A + W + WTS + 128;
 };
@@ -588,16 +588,16 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a
     using S = MlaCombineSmem<DC>;
     extern __shared__ __align__(16) uint8_t cmb[];
     T *os = reinterpret_cast<T *>(cmb);                               // [16][AS]
-    T *wrows = reinterpret_cast<T *>(cmb + S::A);                      // [32][AS]
+    T *wrows = reinterpret_cast<T *>(cmb + S::A);                      // [64][AS]
     float *wts = reinterpret_cast<float *>(cmb + S::A + S::W);        // [16][MLA_MAX_CTAS]
     int *s_c0 = reinterpret_cast<int *>(cmb + S::A + S::W + S::WTS);   // [16]
     int *s_c1 = s_c0 + 16;                                             // [16]
     const int h = blockIdx.x;
     const int b0 = blockIdx.y * 16;
-    const int i0 = blockIdx.z * 32;
+    const int i0 = blockIdx.z * 64;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr unsigned FULL = 0xffffffffu;
-    const int rows = min(32, a.d_h - i0);
+    const int rows = min(64, a.d_h - i0);
     dev::grid_dependency_wait();   // the previous kernel on the stream (the attention) has completed
     dev::allow_dependents();
     {
@@ -724,8 +724,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a
     }
     cp_async_wait_all();
     __syncthreads();
-    // out[b0 + m, h, i0 + 8 warp + n] for warps 0-3: A = o~ [16 x d_c], B = W rows [8 x d_c]
-    if (warp < 4 && 8 * warp < rows) {
+    // out[b0 + m, h, i0 + 8 warp + n] for warps 0-7: A = o~ [16 x d_c], B = W rows [8 x d_c]
+    if (warp < 8 && 8 * warp < rows) {
         const int l7 = lane & 7, j8 = lane >> 3;
         const uint32_t a_addr = dev::smem_addr(os + ((j8 & 1) * 8 + l7) * S::AS + (j8 >> 1) * 8);
         const uint32_t b_addr = dev::smem_addr(wrows + (8 * warp + l7) * S::AS + (j8 & 1) * 8 + (j8 >> 1) * 16);
@@ -790,7 +790,7 @@ const MlaKernelInfo *mla_info() {
             return launch_pdl(mla_absorb_kernel<T, DC>, grid, dim3(128), MlaAbsorbSmem<256>::BYTES, s, a);
         },
         [](const MlaCombineArgs &a, cudaStream_t s) {
-            const dim3 grid(a.H, (a.B + 15) / 16, (a.d_h + 31) / 32);
+            const dim3 grid(a.H, (a.B + 15) / 16, (a.d_h + 63) / 64);
             return launch_pdl(mla_combine_kernel<T, DC>, grid, dim3(512), MlaCombineSmem<DC>::BYTES, s, a);
         },
     };
