@@ -33,6 +33,7 @@ struct kvc_cache {
     int n_stages;
     int smem_bytes;
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
+    CUtensorMap pf_k32, pf_k8, pf_v32, pf_v8;  // the chunked prefill's (64-column blocks)
 };
 
 namespace {
@@ -89,6 +90,15 @@ const kvc::DecodeKernelInfo *find_decode_paged(const kvc_config *c) {
     return nullptr;
 }
 
+// Kernel for a contiguous cache: for 16-bit d_h = 128 with 2 to 8 query
+// heads per KV head the half-row kernel (one TMA box per tile and tensor
+// instead of one per 64-column block), otherwise the registry's.
+const kvc::DecodeKernelInfo *find_decode_dense(const kvc_config *c) {
+    if (c->d_head == 128 && (c->dtype == KVC_BF16 || c->dtype == KVC_FP16))
+        if (const kvc::DecodeKernelInfo *i = find_decode_paged(c)) return i;
+    return find_decode(c);
+}
+
 // Chunked-prefill kernel: 16-bit caches with d_h 64 or 128.
 const kvc::PrefillKernelInfo *find_prefill(const kvc_config *c) {
     const int G = c->n_heads / c->n_kv_heads;
@@ -135,7 +145,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                             const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
-                            CUtensorMap *v8) {
+                            CUtensorMap *v8, bool half_rows) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
     // 16-bit caches: boxes of 64 elements (128 bytes) per row; int8 codes:
@@ -145,11 +155,15 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
     const CUtensorMapDataType dt = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                       : dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
-    const cuuint64_t strides[2] = {cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
+    if (half_rows && (q8 || D % 64 != 0)) return false;
+    const cuuint64_t hr = half_rows ? cuuint64_t(D / 64) : 1;  // map rows per cache row
+    const cuuint64_t dims[3] = {half_rows ? 64 : cuuint64_t(D), cuuint64_t(max_ctx) * hr, cuuint64_t(n_segs)};
+    const cuuint64_t strides[2] = {half_rows ? 128 : cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
     const cuuint32_t elem[3] = {1, 1, 1};
     struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
-    const Job jobs[4] = {{k_base, 32, k32}, {k_base, 8, k8}, {v_base, 32, v32}, {v_base, 8, v8}};
+    // the larger box covers a whole decode tile (int8: 64 rows; 16-bit: 32)
+    const cuuint32_t r32 = q8 ? 64 : cuuint32_t(32 * hr), r8 = cuuint32_t(8 * hr);
+    const Job jobs[4] = {{k_base, r32, k32}, {k_base, r8, k8}, {v_base, r32, v32}, {v_base, r8, v8}};
     for (const Job &j : jobs) {
         const cuuint32_t box[3] = {cuuint32_t(128 / eb), j.rows, 1};
         if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem,
@@ -239,7 +253,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
                       int32_t num_blocks = 0) {
     if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
     if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
-    const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode(cfg);
+    const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode_dense(cfg);
     if (!info) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
         return KVC_ERR_ALIGNMENT;
@@ -297,12 +311,24 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
             delete h;
             return KVC_ERR_CUDA;
         }
-    } else if ((info->tensor_maps || pinfo) &&
-        !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
-                                int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
-                                &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
-        delete h;
-        return KVC_ERR_CUDA;
+    } else {
+        const int64_t n_segs = int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads;
+        if ((info->tensor_maps || pinfo) &&
+            !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
+                                    &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8, info->half_rows)) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
+        h->pf_k32 = h->tm_k32;
+        h->pf_k8 = h->tm_k8;
+        h->pf_v32 = h->tm_v32;
+        h->pf_v8 = h->tm_v8;
+        if (pinfo && info->half_rows &&
+            !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
+                                    &h->pf_k32, &h->pf_k8, &h->pf_v32, &h->pf_v8)) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
     }
     *out = h;
     return KVC_OK;
@@ -513,10 +539,10 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const in
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.seg_base = layer * c.batch * c.n_kv_heads;
-    a.tm_k32 = h->tm_k32;
-    a.tm_k8 = h->tm_k8;
-    a.tm_v32 = h->tm_v32;
-    a.tm_v8 = h->tm_v8;
+    a.tm_k32 = h->pf_k32;
+    a.tm_k8 = h->pf_k8;
+    a.tm_v32 = h->pf_v32;
+    a.tm_v8 = h->pf_v8;
     const cudaError_t e = h->prefill->launch(a, int(grid), h->prefill->smem, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

@@ -92,8 +92,9 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 }  // namespace q8
 
-// Producer: codes through the tensor maps (boxes of 128 codes x 32 or x 8
-// rows), tail rows and every row scale by cp.async.
+// Producer: codes through the tensor maps (one box of 128 codes x 64 rows
+// for a whole tile, boxes of x 8 rows in a tail tile), the tail's last rows
+// and every row scale by cp.async.
 template <typename C>
 __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker walk, uint32_t stage0,
                                                      uint32_t scale0, uint32_t bar0, int ns, int64_t kv_slab,
@@ -132,14 +133,14 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
             if (lane == 0) {
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
-                const int q32 = q >> 2;  // whole 32-row boxes, then 8-row boxes
-                for (int j = 0; j < q32; ++j) {
-                    dev::tma_load_3d(kdst + j * 32 * 128, &a.tm_k32, 0, row0 + 32 * j, z, full);
-                    dev::tma_load_3d(vdst + j * 32 * 128, &a.tm_v32, 0, row0 + 32 * j, z, full);
-                }
-                for (int j = 4 * q32; j < q; ++j) {
-                    dev::tma_load_3d(kdst + j * 8 * 128, &a.tm_k8, 0, row0 + 8 * j, z, full);
-                    dev::tma_load_3d(vdst + j * 8 * 128, &a.tm_v8, 0, row0 + 8 * j, z, full);
+                if (q == TILE / 8) {  // a whole tile: one box of K, one of V
+                    dev::tma_load_3d(kdst, &a.tm_k32, 0, row0, z, full);
+                    dev::tma_load_3d(vdst, &a.tm_v32, 0, row0, z, full);
+                } else {
+                    for (int j = 0; j < q; ++j) {
+                        dev::tma_load_3d(kdst + j * 8 * 128, &a.tm_k8, 0, row0 + 8 * j, z, full);
+                        dev::tma_load_3d(vdst + j * 8 * 128, &a.tm_v8, 0, row0 + 8 * j, z, full);
+                    }
                 }
             }
             // row scales: lane l takes rows l and l + 32 of K and of V

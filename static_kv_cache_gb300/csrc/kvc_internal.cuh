@@ -99,6 +99,7 @@ struct DecodeKernelInfo {
     cudaError_t (*set_max_smem)(int bytes);
     cudaError_t (*launch)(const DecodeArgs &a, int grid, int smem, cudaStream_t s);
     bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
+    bool half_rows;      // its maps view rows as 128-byte half-rows (encode_cache_maps)
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -157,12 +158,16 @@ KVC_DECLARE_PREFILL_TABLE(f16, 64)
 KVC_DECLARE_PREFILL_TABLE(f16, 128)
 #undef KVC_DECLARE_PREFILL_TABLE
 
-// Tensor maps of a K and a V cache [n_segs][max_ctx][D] of 16-bit elements
-// (n_segs = L * B * H_kv): boxes of 64 columns x 32 rows and x 8 rows with the
-// 128-byte swizzle.  Host only; returns false if the driver refuses.
+// Tensor maps of a K and a V cache [n_segs][max_ctx][D] (n_segs = L * B *
+// H_kv), 128-byte swizzle.  16-bit elements: boxes of 64 columns x 32 rows and
+// x 8 rows; with half_rows, each row viewed as D / 64 half-rows of 128 bytes
+// and boxes of 64 columns x 32 rows' and x 8 rows' half-rows (a whole tile, or
+// 8 rows of it, in one copy).  int8 codes: boxes of 128 columns x 64 (a
+// whole int8 decode tile) and x 8 rows.  Host only; returns false if the
+// driver refuses.
 bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
-                       CUtensorMap *v8);
+                       CUtensorMap *v8, bool half_rows = false);
 
 // Quantising append for int8 caches (kvc_append.cu): bf16 rows -> one fp32
 // scale per row and int8 codes, written at cache_index[b] + index_offset.
