@@ -44,7 +44,8 @@ KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_q8.cuh",
                   "static_kv_cache_gb300/csrc/kvc_mla.cuh",
                   "static_kv_cache_gb300/csrc/kvc_internal.cuh",
-                  "static_kv_cache_gb300/csrc/kvc_decode_inst.cu")
+                  "static_kv_cache_gb300/csrc/kvc_decode_inst.cu",
+                  "static_kv_cache_gb300/csrc/kvc_api.cu")   # tensor-map boxes
 
 
 def decode_kernel_name(w: synth.Workload) -> str:

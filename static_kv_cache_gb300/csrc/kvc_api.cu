@@ -90,15 +90,6 @@ const kvc::DecodeKernelInfo *find_decode_paged(const kvc_config *c) {
     return nullptr;
 }
 
-// Kernel for a contiguous cache: for 16-bit d_h = 128 with 2 to 8 query
-// heads per KV head the half-row kernel (one TMA box per tile and tensor
-// instead of one per 64-column block), otherwise the registry's.
-const kvc::DecodeKernelInfo *find_decode_dense(const kvc_config *c) {
-    if (c->d_head == 128 && (c->dtype == KVC_BF16 || c->dtype == KVC_FP16))
-        if (const kvc::DecodeKernelInfo *i = find_decode_paged(c)) return i;
-    return find_decode(c);
-}
-
 // Chunked-prefill kernel: 16-bit caches with d_h 64 or 128.
 const kvc::PrefillKernelInfo *find_prefill(const kvc_config *c) {
     const int G = c->n_heads / c->n_kv_heads;
@@ -145,7 +136,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                             const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
-                            CUtensorMap *v8, bool half_rows) {
+                            CUtensorMap *v8, bool tile_box) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
     // 16-bit caches: boxes of 64 elements (128 bytes) per row; int8 codes:
@@ -155,16 +146,29 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
     const CUtensorMapDataType dt = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                       : dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (half_rows && (q8 || D % 64 != 0)) return false;
-    const cuuint64_t hr = half_rows ? cuuint64_t(D / 64) : 1;  // map rows per cache row
-    const cuuint64_t dims[3] = {half_rows ? 64 : cuuint64_t(D), cuuint64_t(max_ctx) * hr, cuuint64_t(n_segs)};
-    const cuuint64_t strides[2] = {half_rows ? 128 : cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
-    const cuuint32_t elem[3] = {1, 1, 1};
+    if (tile_box && (q8 || D % 64 != 0)) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
     struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
     // the larger box covers a whole decode tile (int8: 64 rows; 16-bit: 32)
-    const cuuint32_t r32 = q8 ? 64 : cuuint32_t(32 * hr), r8 = cuuint32_t(8 * hr);
-    const Job jobs[4] = {{k_base, r32, k32}, {k_base, r8, k8}, {v_base, r32, v32}, {v_base, r8, v8}};
+    const cuuint32_t r32 = q8 ? 64 : 32;
+    if (tile_box) {
+        // (64 columns, rows, column blocks, segments); a block is 128 bytes
+        // further along the row, so the box lands block after block
+        const cuuint64_t dims4[4] = {64, cuuint64_t(max_ctx), cuuint64_t(D / 64), cuuint64_t(n_segs)};
+        const cuuint64_t strides4[3] = {cuuint64_t(D) * eb, 128, cuuint64_t(max_ctx) * D * eb};
+        const cuuint32_t box4[4] = {64, 32, cuuint32_t(D / 64), 1};
+        const Job tiles[2] = {{k_base, 32, k32}, {v_base, 32, v32}};
+        for (const Job &j : tiles)
+            if (encode(j.out, dt, 4, const_cast<void *>(j.base), dims4, strides4, box4, elem,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+    }
+    const Job jobs[4] = {{k_base, r32, k32}, {k_base, 8, k8}, {v_base, r32, v32}, {v_base, 8, v8}};
     for (const Job &j : jobs) {
+        if (tile_box && j.rows != 8) continue;  // encoded above
         const cuuint32_t box[3] = {cuuint32_t(128 / eb), j.rows, 1};
         if (encode(j.out, dt, 3, const_cast<void *>(j.base), dims, strides, box, elem,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -253,7 +257,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
                       int32_t num_blocks = 0) {
     if (!out || !shape_ok(cfg) || !k_base || !v_base) return KVC_ERR_INVALID;
     if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
-    const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode_dense(cfg);
+    const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode(cfg);
     if (!info) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
         return KVC_ERR_ALIGNMENT;
@@ -315,7 +319,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
         const int64_t n_segs = int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads;
         if ((info->tensor_maps || pinfo) &&
             !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
-                                    &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8, info->half_rows)) {
+                                    &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8, info->tile_box)) {
             delete h;
             return KVC_ERR_CUDA;
         }
@@ -323,7 +327,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
         h->pf_k8 = h->tm_k8;
         h->pf_v32 = h->tm_v32;
         h->pf_v8 = h->tm_v8;
-        if (pinfo && info->half_rows &&
+        if (pinfo && info->tile_box &&
             !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
                                     &h->pf_k32, &h->pf_k8, &h->pf_v32, &h->pf_v8)) {
             delete h;

@@ -118,11 +118,10 @@ struct MmaCfg {
 };
 
 // The producer warp: walks the CTA's pieces; for each tile one lane issues
-// the TMA boxes and the other lanes load the tail rows no box may cover.
-// HRL: the tensor maps view each row as D / 64 half-rows of 128 bytes, so one
-// box of K (and one of V) brings a whole tile in the half-row layout
-// (MmaCfg::swz_pg); otherwise a box brings one 64-column block of the tile.
-template <typename C, bool HRL = false>
+// the TMA boxes and the other lanes load the tail rows no box may cover.  A
+// full tile is one box of K and one of V (the 4-D map: all 64-column blocks);
+// a tail tile takes one 8-row box per 64-column block.
+template <typename C>
 __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walker walk, uint32_t stage0,
                                                       uint32_t bar0, int ns, int64_t kv_slab,
                                                       volatile int *flags, int lane) {
@@ -165,21 +164,9 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
                 // order them before the TMA unit overwrites the stage
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
-                if (HRL && q == 4) {
-                    dev::tma_load_3d(kdst, &a.tm_k32, 0, row0 * CB, z, full);
-                    dev::tma_load_3d(vdst, &a.tm_v32, 0, row0 * CB, z, full);
-                } else if (HRL) {
-                    for (int j = 0; j < q; ++j) {
-                        const uint32_t off = j * 8 * C::ROW_BYTES;
-                        dev::tma_load_3d(kdst + off, &a.tm_k8, 0, (row0 + 8 * j) * CB, z, full);
-                        dev::tma_load_3d(vdst + off, &a.tm_v8, 0, (row0 + 8 * j) * CB, z, full);
-                    }
-                } else if (q == 4) {
-#pragma unroll
-                    for (int cb = 0; cb < CB; ++cb) {
-                        dev::tma_load_3d(kdst + cb * C::BLOCK_BYTES, &a.tm_k32, cb * 64, row0, z, full);
-                        dev::tma_load_3d(vdst + cb * C::BLOCK_BYTES, &a.tm_v32, cb * 64, row0, z, full);
-                    }
+                if (q == 4) {
+                    dev::tma_load_4d(kdst, &a.tm_k32, 0, row0, 0, z, full);
+                    dev::tma_load_4d(vdst, &a.tm_v32, 0, row0, 0, z, full);
                 } else {
                     for (int j = 0; j < q; ++j)
 #pragma unroll
@@ -202,8 +189,7 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
                         row0 + r == new_row
                             ? (is_v ? a.v_new : a.k_new) + int64_t(seg) * C::ROW_BYTES + c16 * 16
                             : (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
-                    const uint32_t dst = is_v ? vdst : kdst;
-                    dev::cp_async_16(HRL ? C::swz_pg(dst, r, c16 * 8) : C::swz(dst, r, c16 * 8), src);
+                    dev::cp_async_16(C::swz(is_v ? vdst : kdst, r, c16 * 8), src);
                 }
                 dev::cp_async_arrive(full);
                 generic_written |= 1u << stage;
@@ -640,9 +626,8 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
     return false;
 }
 
-// PG: the tiles are in the half-row layout (MmaCfg::swz_pg), filled from a
-// paged pool or from a contiguous cache through half-row tensor maps; only
-// the d_h = 128 kernels need it (for d_h = 64 the layouts coincide).
+// PG: the tiles come from a paged pool in the half-row layout (MmaCfg::swz_pg);
+// only the d_h = 128 kernels need it (for d_h = 64 the layouts coincide).
 template <typename T, int D, int G, bool PG = false>
 __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
@@ -703,7 +688,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         uint32_t issued;
         if constexpr (PAGED_OK)
             issued = a.block_table ? produce_tiles_paged<C>(a, walk, stage0, bar0, ns, flags, lane)
-                                   : produce_tiles_tma<C, PGL>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
+                                   : produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         else
             issued = produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
@@ -994,7 +979,7 @@ const DecodeKernelInfo *mma_decode_info() {
     using C = MmaCfg<T, D, G>;
     static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
                                           &set_mma_max_smem<T, D, G, PG>, &launch_mma<T, D, G, PG>, true,
-                                          PG && D != 64};
+                                          true};
     return &info;
 }
 

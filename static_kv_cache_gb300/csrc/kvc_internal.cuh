@@ -99,7 +99,7 @@ struct DecodeKernelInfo {
     cudaError_t (*set_max_smem)(int bytes);
     cudaError_t (*launch)(const DecodeArgs &a, int grid, int smem, cudaStream_t s);
     bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
-    bool half_rows;      // its maps view rows as 128-byte half-rows (encode_cache_maps)
+    bool tile_box;       // its full-tile map is the 4-D one of encode_cache_maps
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -160,14 +160,15 @@ KVC_DECLARE_PREFILL_TABLE(f16, 128)
 
 // Tensor maps of a K and a V cache [n_segs][max_ctx][D] (n_segs = L * B *
 // H_kv), 128-byte swizzle.  16-bit elements: boxes of 64 columns x 32 rows and
-// x 8 rows; with half_rows, each row viewed as D / 64 half-rows of 128 bytes
-// and boxes of 64 columns x 32 rows' and x 8 rows' half-rows (a whole tile, or
-// 8 rows of it, in one copy).  int8 codes: boxes of 128 columns x 64 (a
-// whole int8 decode tile) and x 8 rows.  Host only; returns false if the
-// driver refuses.
+// x 8 rows (one 64-column block of a tile each).  With tile_box the 32-row
+// map is 4-D instead, (64 columns, rows, D / 64 column blocks, segments) with
+// the blocks 128 bytes apart, so one box brings a whole 32-row tile laid out
+// block after block.  int8 codes: boxes of 128 columns x 64 rows (a whole
+// int8 decode tile) and x 8 rows.  Host only; returns false if the driver
+// refuses.
 bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
-                       CUtensorMap *v8, bool half_rows = false);
+                       CUtensorMap *v8, bool tile_box = false);
 
 // Quantising append for int8 caches (kvc_append.cu): bf16 rows -> one fp32
 // scale per row and int8 codes, written at cache_index[b] + index_offset.
@@ -394,6 +395,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// The same for a 4-D tensor map.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
         : "memory");
 }
 

@@ -57,11 +57,6 @@ int elem_bytes(int32_t dtype) {
 }
 
 const kvc::DecodeKernelInfo *lookup_kernel(int32_t dtype, int D, int G) {
-    // 16-bit d_h = 128, 2 to 8 query heads per KV head: the half-row kernel
-    if (D == 128 && G >= 2 && G <= 8) {
-        if (dtype == KVC_BF16) return kvc::decode_kernel_paged_bf16_128(G);
-        if (dtype == KVC_FP16) return kvc::decode_kernel_paged_f16_128(G);
-    }
 #define KVC_NOALLOC_PICK(TAG, DD) \
     if (D == DD) return kvc::decode_kernel_##TAG##_##DD(G);
     switch (dtype) {
@@ -189,7 +184,7 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     if (info->tensor_maps &&
         !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context,
                                 int64_t(cfg->n_layers) * cfg->batch * cfg->n_kv_heads, k_base, v_base,
-                                &maps[0], &maps[1], &maps[2], &maps[3], info->half_rows))
+                                &maps[0], &maps[1], &maps[2], &maps[3], info->tile_box))
         return KVC_ERR_CUDA;
 
     // The array keeps the previous call's contents: the error word, the
