@@ -281,20 +281,20 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             const uint32_t vdst = kdst + C::TILE_BYTES;
-            if (lane == 0) {
-                if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
-                dev::mbar_expect_tx(full, 2u * tx_rows * C::ROW_BYTES);
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    if (!boxed[jj]) continue;
-                    // one box per tensor covers the block's 16 (or first 8)
-                    // whole rows: the pool viewed as 128-byte half-rows
-                    const int z = a.seg_base + phys[jj] * a.H_kv + pc.kv;
-                    const CUtensorMap *mk = boxed[jj] == BS ? &a.tm_k32 : &a.tm_k8;
-                    const CUtensorMap *mv = boxed[jj] == BS ? &a.tm_v32 : &a.tm_v8;
-                    const uint32_t off = jj * BS * C::ROW_BYTES;
-                    dev::tma_load_3d(kdst + off, mk, 0, 0, z, full);
-                    dev::tma_load_3d(vdst + off, mv, 0, 0, z, full);
+            if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();  // every issuing lane
+            if (lane == 0) dev::mbar_expect_tx(full, 2u * tx_rows * C::ROW_BYTES);
+            __syncwarp();
+            if (lane < 4) {
+                // lanes 0-3: (block 0, K) (block 0, V) (block 1, K) (block 1, V),
+                // all in one instruction.  One box covers the block's 16 (or
+                // first 8) whole rows: the pool viewed as 128-byte half-rows.
+                const int jj = lane >> 1;
+                const bool is_v = lane & 1;
+                const int bx = jj ? boxed[1] : boxed[0];
+                if (bx) {
+                    const int z = a.seg_base + (jj ? phys[1] : phys[0]) * a.H_kv + pc.kv;
+                    const CUtensorMap *m = bx == BS ? (is_v ? &a.tm_v32 : &a.tm_k32) : (is_v ? &a.tm_v8 : &a.tm_k8);
+                    dev::tma_load_3d((is_v ? vdst : kdst) + jj * BS * C::ROW_BYTES, m, 0, 0, z, full);
                 }
             }
             bool generic = false;
