@@ -78,7 +78,15 @@ def parse_args(argv=None):
     p.add_argument("--no-graph", action="store_true",
                    help="time direct calls instead of a CUDA graph of one step")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="time only the headline workload (skip the other target configs)")
     return p.parse_args(argv)
+
+
+# The other configurations the throughput target names (the Llama-2-70B layer
+# at 32k, B=1 and B=4) and the Qwen2.5 shape in both cache types: timed after
+# the headline in the default single-GPU run and reported under "configs".
+EXTRA_WORKLOADS = ("llama2_70b_b1", "llama2_70b_b4", "qwen2_5_1_5b_bf16", "qwen2_5_1_5b_fp32")
 
 
 def dist_env():
@@ -533,30 +541,22 @@ def workload_config(w: synth.Workload, lengths, world: int) -> dict:
 
 
 # --------------------------------------------------------------------------- arms
-def bench_kvc(args, rank, world, local):
-    torch.cuda.set_device(local)
-    init_dist(world, "nccl")
-    w = synth.WORKLOADS[args.workload]
-    if args.layers:
-        w = w.with_(n_layers=args.layers)
-    state = MlaState(w, local) if w.d_latent else DeviceState(w, local)
-    lengths = state.lengths.numpy()
-    per_layer = step_bytes(w, lengths)
-    bytes_step = (per_layer["attn"] + per_layer["append"]) * w.n_layers
+def time_steps(state, w, steps, warmup, no_graph, world, local, clocks=True) -> dict:
+    """Warm up, then time `steps` whole decode steps on one stream between
+    barrier + synchronize, with CUDA events at the two ends of the timed
+    region only (an event between two launches would keep the second from
+    overlapping the first's drain).  The steps replay a CUDA graph of
+    `per_graph` consecutive steps captured from the same C-ABI calls a direct
+    step makes (they only enqueue kernels), so launch-bound workloads measure
+    the GPU rather than the host loop."""
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             state.step(stream)
     torch.cuda.synchronize()
-
-    # One step (every layer's call) captured as a CUDA graph and replayed: the
-    # calls only enqueue kernels on the stream, so the graph holds exactly the
-    # launches a direct step makes, without the host in the loop.
-    # A graph holds `per_graph` consecutive steps (a divisor of the step count,
-    # at most 8), so consecutive steps still overlap inside it.
     graph, graph_note = None, "direct calls (--no-graph)"
-    per_graph = max(d for d in range(1, 9) if args.steps % d == 0)
-    if not args.no_graph:
+    per_graph = max(d for d in range(1, 9) if steps % d == 0)
+    if not no_graph:
         try:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
@@ -567,18 +567,15 @@ def bench_kvc(args, rank, world, local):
                 finally:
                     g.capture_end()
             with torch.cuda.stream(stream):
-                for _ in range(max(3, args.warmup)):
+                for _ in range(max(3, warmup)):
                     g.replay()
             torch.cuda.synchronize()
             graph, graph_note = g, f"CUDA graph of {per_graph} steps (every layer's call), replayed"
         except Exception as exc:  # capture not available: time direct calls
             graph, graph_note = None, f"direct calls (graph capture failed: {str(exc)[:120]})"
     launches_per_step = state.launches_per_layer * w.n_layers
-
-    # --- device-timed region: events at its two ends only (an event between
-    # two launches would keep the second from overlapping the first's drain)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = None if args.no_clocks else ClockSampler(local)
+    sampler = ClockSampler(local) if clocks else None
     barrier(world)
     torch.cuda.synchronize()
     if sampler:
@@ -588,21 +585,73 @@ def bench_kvc(args, rank, world, local):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         if graph is not None:
-            for _ in range(args.steps // per_graph):
+            for _ in range(steps // per_graph):
                 graph.replay()
                 launches += launches_per_step * per_graph
         else:
-            for _ in range(args.steps):
+            for _ in range(steps):
                 launches += state.step(stream)
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
+    clk = sampler.stop() if sampler else None
     elapsed = t_start.elapsed_time(t_end) / 1e3
     elapsed_max = reduce_max(elapsed, world, device=torch.device("cuda", local))
     err = state.error(stream)
     if err:
         raise state.kvc.KvcError(err, "device error word after the timed region")
+    del graph
+    return {"elapsed": elapsed, "elapsed_max": elapsed_max, "launches": launches, "launch": graph_note,
+            "clocks": clk, "stream": stream}
+
+
+def time_extra_configs(args, world, local, peak) -> dict:
+    """The other target configurations, one after another (each one's
+    buffers freed before the next): per config its whole-job GB/s, step
+    time, fraction of the HBM peak and the clocks seen while it ran."""
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        w = synth.WORKLOADS[name]
+        state = DeviceState(w, local)
+        per_layer = step_bytes(w, state.lengths.numpy())
+        bytes_call = per_layer["attn"] + per_layer["append"]
+        # about half a second of timed steps at the expected rate, within [20, --steps]
+        est_step_s = bytes_call * w.n_layers / (0.8 * peak * 1e9)
+        steps = int(min(max(20, round(0.5 / est_step_s)), max(20, args.steps)))
+        steps -= steps % 8 if steps >= 8 else 0
+        r = time_steps(state, w, steps, max(3, args.warmup), args.no_graph, world, local, not args.no_clocks)
+        call_s = r["elapsed"] / (steps * w.n_layers)
+        achieved = bytes_call / call_s / 1e9
+        out[name] = {
+            "value": round(job_throughput(bytes_call * w.n_layers, world, r["elapsed_max"], steps), 2),
+            "unit": UNIT, "steps": steps, "ms_per_step": round(r["elapsed_max"] / steps * 1e3, 4),
+            "frac": round(achieved / peak, 4), "achieved": round(achieved, 2),
+            "bytes_attn": per_layer["attn"], "bytes_append": per_layer["append"],
+            "mean_call_us": round(call_s * 1e6, 3), "kernel": decode_kernel_name(w),
+            "launches_per_call": state.launches_per_layer, "launch": r["launch"], "clocks": r["clocks"],
+            "workload": workload_config(w, state.lengths.numpy(), world)["workload"],
+        }
+        state.close()
+        del state
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_kvc(args, rank, world, local):
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
+    state = MlaState(w, local) if w.d_latent else DeviceState(w, local)
+    lengths = state.lengths.numpy()
+    per_layer = step_bytes(w, lengths)
+    bytes_step = (per_layer["attn"] + per_layer["append"]) * w.n_layers
+    r = time_steps(state, w, args.steps, args.warmup, args.no_graph, world, local, not args.no_clocks)
+    stream, graph_note, clocks, launches = r["stream"], r["launch"], r["clocks"], r["launches"]
+    elapsed, elapsed_max = r["elapsed"], r["elapsed_max"]
+    launches_per_call = state.launches_per_layer
 
     # --- end to end through the C ABI with host buffers
     e2e = None
@@ -640,6 +689,14 @@ def bench_kvc(args, rank, world, local):
 
     value = job_throughput(bytes_step, world, elapsed_max, args.steps)
     peak, peak_src = load_peaks()
+    extra = None
+    if world == 1 and not args.no_extra and args.workload == "llama3_8b" and not args.layers:
+        state.close()
+        del state
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        state = None
+        extra = time_extra_configs(args, world, local, peak)
     # one kvc call per layer and step; its average duration over the timed
     # region (gaps between calls included)
     mean_decode_s = elapsed / (args.steps * w.n_layers)
@@ -650,8 +707,9 @@ def bench_kvc(args, rank, world, local):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed_max / args.steps * 1e3, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(w, lengths, world),
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_config(w, lengths, world),
+                           accumulate="fp32 (products, softmax and sums; one rounding to the cache type at the end)"),
             "tokens_per_s_per_layer": round(world * w.batch * w.n_layers / (elapsed_max / args.steps), 1),
             "decode_tokens_per_s": round(world * w.batch / (elapsed_max / args.steps), 1),
             "decode_attn_pct_of_peak": round(100 * achieved / peak, 2),
@@ -660,14 +718,18 @@ def bench_kvc(args, rank, world, local):
                          "kernel": decode_kernel_name(w), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
                          "bytes_per_launch": per_layer["attn"] + per_layer["append"],
+                         "bytes_attn": per_layer["attn"], "bytes_append": per_layer["append"],
                          "mean_launch_us": round(mean_decode_s * 1e6, 3),
-                         "launches_per_call": state.launches_per_layer,
+                         "launches_per_call": launches_per_call,
                          "timing": "timed region / (steps x layers): one kvc decode-step call per layer, gaps included",
                          "launch": graph_note},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         }
+        if extra is not None:
+            line["configs"] = extra
         print(json.dumps(line), flush=True)
-    state.close()
+    if state is not None:
+        state.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -701,7 +763,8 @@ def bench_reference(args, rank, world, local):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / samples * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, lengths, world),
+            "data": "synthetic", "config": dict(workload_config(w, lengths, world),
+                                                accumulate="fp64 (the oracle: exact widening, fp64 throughout)"),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -910,8 +973,11 @@ def bench_prefill(args, rank, world, local):
                          "mean_launch_us": round(mean_launch_s * 1e6, 3)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         }
+        if extra is not None:
+            line["configs"] = extra
         print(json.dumps(line), flush=True)
-    state.close()
+    if state is not None:
+        state.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

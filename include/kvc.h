@@ -138,7 +138,9 @@ uint64_t kvc_bytes_per_token(const kvc_config *cfg);
 /* Bytes of device workspace kvc_alloc needs for cfg: split partials
  * (max, sum, accumulator per split of each sequence/KV head/query head),
  * one counter per (sequence, KV head), and the device error word.
- * 0 if cfg is invalid. */
+ * 0 if cfg is invalid.  The workspace starts with the int32 error word at
+ * byte 0 and the int32 arrival counters [B * H_kv] at byte 256 (for
+ * diagnostics; the rest of its layout is private). */
 uint64_t kvc_workspace_bytes(const kvc_config *cfg);
 
 /* Bytes of ONE of the two scale arrays of an int8 cache: one fp32 per row,
@@ -209,6 +211,20 @@ void kvc_free(kvc_cache *h);
  * the automatic choice, otherwise 1..1024.  Results agree across split
  * counts up to fp32 rounding. */
 kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n);
+
+/* Limit, in nanoseconds of GPU wall time, of one wait inside the decode
+ * kernels: the wait of a sequence's last context split for the partial
+ * results the other splits publish (the split combine, which has no
+ * counterpart on the pages).  0 restores the default of 1 s.  When
+ * the limit runs out the kernel records KVC_ERR_TIMEOUT in the device error
+ * word, abandons the launch (its output rows are undefined) and returns;
+ * kvc_get_error then reports it and resets the split counters, after which
+ * the handle works normally again.  Every other wait (the copies into shared
+ * memory, and the drain of copies in flight before a block exits) keeps the
+ * 1 s default, so no block ever exits with a copy still landing.  A short
+ * limit is meant for diagnostics: under load the other splits may
+ * legitimately take longer than it. */
+kvc_status kvc_set_wait_timeout_ns(kvc_cache *h, uint64_t ns);
 
 /* ---- the decode step ------------------------------------------------------ */
 
@@ -339,12 +355,26 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q,
  * counters on the stream first, so calls that overlap on the GPU (streams
  * without ordering between them) race; order them on one stream.  A sequence
  * with valid_len[b] outside [1, max_context] is skipped (its output rows are
- * left unwritten); this call has no handle, so that is not reported through
- * kvc_get_error. */
+ * left unwritten).  This call has no handle: errors found on the device
+ * (KVC_ERR_DEVICE_INDEX, KVC_ERR_TIMEOUT) go to the array's own error word,
+ * which kvc_static_get_error reads and clears; it keeps the first error until
+ * then. */
 kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t layer,
                                   const void *k_base, const void *v_base,
                                   const void *q, const int32_t *valid_len,
                                   int32_t max_valid_hint, void *out, void *stream);
+
+/* The error word of the scratch array that kvc_decode_attn_static uses on the
+ * current device (no counterpart on the pages, like that call): synchronise
+ * the stream, then read and clear the word.  KVC_OK if no such call recorded
+ * an error since the last read, otherwise the first recorded code:
+ * KVC_ERR_DEVICE_INDEX (a valid_len outside [1, max_context]; that sequence
+ * was skipped) or KVC_ERR_TIMEOUT (a bounded wait gave up; that call's
+ * output is undefined, and the next call clears the split counters it may
+ * have left set).  The word is shared by every such call on the device, so
+ * read it between calls to tell them apart.  Allocates nothing.
+ * KVC_ERR_CUDA if the synchronisation or the copy fails. */
+kvc_status kvc_static_get_error(void *stream);
 
 /* Synchronise the stream, then read and clear the device error word.
  * Returns KVC_OK if no kernel recorded an error since the last call,

@@ -41,5 +41,9 @@ def quantize_rows(x_bits: np.ndarray, dtype: str):
 
 
 def dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """code * scale in float64 (exact: an int8 times an fp32 fits a double)."""
-    return codes.astype(np.float64) * scales.astype(np.float64)[..., None]
+    """code * scale in float64 (exact: an int8 times an fp32 fits a double).
+    Scales of rows past the live length may hold a signalling-NaN poison;
+    their conversion raises the "invalid" flag, which is ignored (those rows
+    are never attended)."""
+    with np.errstate(invalid="ignore"):
+        return codes.astype(np.float64) * scales.astype(np.float64)[..., None]

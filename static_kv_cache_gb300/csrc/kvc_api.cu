@@ -19,6 +19,7 @@ struct kvc_cache {
     int elem_bytes;
     int group;               // n_heads / n_kv_heads
     int num_splits;          // 0: automatic
+    uint64_t flag_timeout_ns;  // limit of the split combine's wait for the other splits
     uint8_t *k_base;
     uint8_t *v_base;
     uint8_t *k_scale;        // int8 caches: per-row fp32 scales [L, B, H_kv, T_max]; else null
@@ -55,23 +56,7 @@ bool shape_ok(const kvc_config *c) {
 }
 
 const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
-    const int G = c->n_heads / c->n_kv_heads;
-    const int D = c->d_head;
-#define KVC_PICK(TAG, DD) \
-    if (D == DD) return kvc::decode_kernel_##TAG##_##DD(G);
-    switch (c->dtype) {
-        case KVC_BF16:
-            KVC_PICK(bf16, 32) KVC_PICK(bf16, 64) KVC_PICK(bf16, 128) KVC_PICK(bf16, 256) break;
-        case KVC_FP16:
-            KVC_PICK(f16, 32) KVC_PICK(f16, 64) KVC_PICK(f16, 128) KVC_PICK(f16, 256) break;
-        case KVC_FP32:
-            KVC_PICK(f32, 32) KVC_PICK(f32, 64) KVC_PICK(f32, 128) KVC_PICK(f32, 256) break;
-        case KVC_INT8:
-            KVC_PICK(q8, 128) break;
-        default: break;
-    }
-#undef KVC_PICK
-    return nullptr;
+    return kvc::find_decode_kernel(c->dtype, c->d_head, c->n_heads / c->n_kv_heads);
 }
 
 // Kernel for a paged pool: the tensor-core kernel (16-bit, 2 to 8 query heads
@@ -133,6 +118,52 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 }  // namespace
+
+const kvc::DecodeKernelInfo *kvc::find_decode_kernel(int32_t dtype, int D, int G) {
+#define KVC_PICK(TAG, DD) \
+    if (D == DD) return kvc::decode_kernel_##TAG##_##DD(G);
+    switch (dtype) {
+        case KVC_BF16:
+            KVC_PICK(bf16, 32) KVC_PICK(bf16, 64) KVC_PICK(bf16, 128) KVC_PICK(bf16, 256) break;
+        case KVC_FP16:
+            KVC_PICK(f16, 32) KVC_PICK(f16, 64) KVC_PICK(f16, 128) KVC_PICK(f16, 256) break;
+        case KVC_FP32:
+            KVC_PICK(f32, 32) KVC_PICK(f32, 64) KVC_PICK(f32, 128) KVC_PICK(f32, 256) break;
+        case KVC_INT8:
+            KVC_PICK(q8, 128) break;
+        default: break;
+    }
+#undef KVC_PICK
+    return nullptr;
+}
+
+int kvc::decode_stage_count(const DecodeKernelInfo *info, int smem_optin) {
+    const int budget = smem_optin < SMEM_BUDGET ? smem_optin : SMEM_BUDGET;
+    int n = (budget - info->fixed_smem) / info->stage_bytes;
+    if (n > 32) n = 32;
+    return n < info->consumer_warps + 1 ? 0 : n;
+}
+
+int kvc::decode_grid(const DecodeKernelInfo *info, int B, int H_kv, int D, int elem_bytes, int max_ctx,
+                     int max_valid_hint, int num_sms, int forced) {
+    // Splits: every SM streams an equal share of the live rows; small
+    // problems use fewer CTAs so that each still gets several tiles.  When
+    // the problem is small and every segment (sequence, KV head) holds at
+    // most 64 KB per tensor, one CTA per segment: the step is latency there,
+    // and a CTA that owns a whole segment needs no split combine.
+    int64_t want = forced;
+    if (want == 0) {
+        const int64_t seg_rows = max_valid_hint > 0 ? max_valid_hint : max_ctx;
+        const int64_t segs = int64_t(B) * H_kv;
+        const int64_t min_rows = 4 * int64_t(info->tile_rows);
+        want = (segs * seg_rows + min_rows - 1) / min_rows;
+        if (want < num_sms && segs <= num_sms && seg_rows * D * elem_bytes <= 65536) want = segs;
+        if (want > num_sms) want = num_sms;
+        if (want < 1) want = 1;
+    }
+    if (want > MAX_CTAS) want = MAX_CTAS;
+    return int(want);
+}
 
 bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                             const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
@@ -273,10 +304,8 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
 
     // As many pipeline stages as shared memory holds (at most 32), but at
     // least one more than there are consumer warps.
-    const int budget = smem < kvc::SMEM_BUDGET ? smem : kvc::SMEM_BUDGET;
-    int n_stages = (budget - info->fixed_smem) / info->stage_bytes;
-    if (n_stages > 32) n_stages = 32;
-    if (n_stages < info->consumer_warps + 1) return KVC_ERR_UNSUPPORTED;
+    const int n_stages = kvc::decode_stage_count(info, smem);
+    if (n_stages == 0) return KVC_ERR_UNSUPPORTED;
     const int smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;
     if (info->set_max_smem(smem_bytes) != cudaSuccess) return KVC_ERR_CUDA;
     const kvc::PrefillKernelInfo *pinfo = find_prefill(cfg);
@@ -295,6 +324,7 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     h->elem_bytes = elem_bytes_of(cfg->dtype);
     h->group = cfg->n_heads / cfg->n_kv_heads;
     h->num_splits = 0;
+    h->flag_timeout_ns = kvc::WAIT_TIMEOUT_NS;
     h->k_base = static_cast<uint8_t *>(k_base);
     h->v_base = static_cast<uint8_t *>(v_base);
     h->k_scale = static_cast<uint8_t *>(k_scale);
@@ -377,6 +407,12 @@ kvc_status kvc_set_num_splits(kvc_cache *h, int32_t n) {
     return KVC_OK;
 }
 
+kvc_status kvc_set_wait_timeout_ns(kvc_cache *h, uint64_t ns) {
+    if (!h) return KVC_ERR_INVALID;
+    h->flag_timeout_ns = ns == 0 ? kvc::WAIT_TIMEOUT_NS : ns;
+    return KVC_OK;
+}
+
 kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void *v_new,
                       const int32_t *cache_index, int32_t T_new, void *stream) {
     if (!h || layer < 0 || layer >= h->cfg.n_layers || T_new < 0) return KVC_ERR_INVALID;
@@ -414,27 +450,11 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
                          const void *v_new) {
     const kvc_config &c = h->cfg;
 
-    // Splits: every SM streams an equal share of the live rows; small
-    // problems use fewer CTAs so that each still gets several tiles.  When
-    // the problem is small and every segment (sequence, KV head) holds at
-    // most 64 KB per tensor, one CTA per segment: the step is latency there,
-    // and a CTA that owns a whole segment needs no split combine.
-    int grid = h->num_splits;
-    if (grid == 0) {
-        const int64_t seg_rows = max_valid_hint > 0 ? max_valid_hint : c.max_context;
-        const int64_t upper_rows = int64_t(c.batch) * c.n_kv_heads * seg_rows;
-        const int64_t min_rows = 4 * int64_t(h->decode->tile_rows);
-        int64_t want = (upper_rows + min_rows - 1) / min_rows;
-        const int64_t segs = int64_t(c.batch) * c.n_kv_heads;
-        if (want < h->num_sms && segs <= h->num_sms && seg_rows * c.d_head * h->elem_bytes <= 65536) want = segs;
-        if (want > h->num_sms) want = h->num_sms;
-        if (want < 1) want = 1;
-        grid = int(want);
-    }
-    if (grid > kvc::MAX_CTAS) grid = kvc::MAX_CTAS;
+    const int grid = kvc::decode_grid(h->decode, c.batch, c.n_kv_heads, c.d_head, h->elem_bytes, c.max_context,
+                                      max_valid_hint, h->num_sms, h->num_splits);
 
     const uint64_t slab = layer_slab_bytes(h);
-    kvc::DecodeArgs a;
+    kvc::DecodeArgs a{};
     a.K = h->k_base + slab * layer;
     a.V = h->v_base + slab * layer;
     a.q = q;
@@ -455,6 +475,7 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
     a.n_stages = h->n_stages;
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    a.flag_timeout_ns = h->flag_timeout_ns;
     a.seg_base = layer * c.batch * c.n_kv_heads;
     a.block_table = h->block_table;
     a.max_blocks = c.max_context / 16;
@@ -528,7 +549,7 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const in
     const int64_t grid = int64_t(c.batch) * c.n_kv_heads * q_blocks;
     if (grid > 0x7fffffff) return KVC_ERR_UNSUPPORTED;
     const uint64_t slab = layer_slab_bytes(h);
-    kvc::PrefillArgs a;
+    kvc::PrefillArgs a{};
     a.K = h->k_base + slab * layer;
     a.V = h->v_base + slab * layer;
     a.q = q;

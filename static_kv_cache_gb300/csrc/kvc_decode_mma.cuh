@@ -602,7 +602,7 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
             // the last split: wait for the others' partials
             bool pub = true;
             for (int c = c0 + lane; c <= c1; c += 32)
-                if (c != me) pub = pub && dev::flag_wait_bounded(a.ready + c + seg, flags, a.timeout_ns);
+                if (c != me) pub = pub && dev::flag_wait_bounded(a.ready + c + seg, flags, a.flag_timeout_ns);
             pub = __all_sync(FULL, pub);
             if (!pub) {
                 if (lane == 0) {

@@ -83,6 +83,9 @@ struct DecodeArgs {
     int32_t n_stages;
     float scale_log2;          // log2(e) / sqrt(D)
     unsigned long long timeout_ns;
+    // Limit of the last split's wait for the other splits' partials (the
+    // split combine's ready flags); every other wait keeps timeout_ns.
+    unsigned long long flag_timeout_ns;
     // Tensor maps of the whole K and V caches viewed as [L*B*H_kv][T_max][D]
     // (16-bit caches, tensor-core kernel only): boxes of 64 columns x 32 or
     // x 8 rows with the 128-byte swizzle.  seg_base = layer * B * H_kv.
@@ -123,6 +126,19 @@ KVC_DECLARE_DECODE_TABLE(q8, 128)
 // paged pools with d_h = 128: the tensor-core kernel in the half-row tile layout
 const DecodeKernelInfo *decode_kernel_paged_bf16_128(int G);
 const DecodeKernelInfo *decode_kernel_paged_f16_128(int G);
+
+// Launch planning shared by every decode entry point (kvc_api.cu).
+// The kernel for a contiguous cache of this element type, head width and
+// query-head group; nullptr where none is compiled.
+const DecodeKernelInfo *find_decode_kernel(int32_t dtype, int D, int G);
+// Pipeline stages that fit the shared memory a block may opt into (at most
+// 32, at least one more than the consumer warps); 0 if that many do not fit.
+int decode_stage_count(const DecodeKernelInfo *info, int smem_optin);
+// CTAs of one decode launch: `forced` when non-zero, otherwise one CTA per SM
+// with at least four tiles each, or one CTA per (sequence, KV head) segment
+// when the problem is small and every segment holds at most 64 KB per tensor.
+int decode_grid(const DecodeKernelInfo *info, int B, int H_kv, int D, int elem_bytes, int max_ctx,
+                int max_valid_hint, int num_sms, int forced);
 
 // Arguments of the chunked-prefill kernel (grid constant).
 struct PrefillArgs {

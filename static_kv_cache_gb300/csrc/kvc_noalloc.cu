@@ -56,33 +56,6 @@ int elem_bytes(int32_t dtype) {
     }
 }
 
-const kvc::DecodeKernelInfo *lookup_kernel(int32_t dtype, int D, int G) {
-#define KVC_NOALLOC_PICK(TAG, DD) \
-    if (D == DD) return kvc::decode_kernel_##TAG##_##DD(G);
-    switch (dtype) {
-        case KVC_BF16:
-            KVC_NOALLOC_PICK(bf16, 32) KVC_NOALLOC_PICK(bf16, 64) KVC_NOALLOC_PICK(bf16, 128)
-            KVC_NOALLOC_PICK(bf16, 256) break;
-        case KVC_FP16:
-            KVC_NOALLOC_PICK(f16, 32) KVC_NOALLOC_PICK(f16, 64) KVC_NOALLOC_PICK(f16, 128)
-            KVC_NOALLOC_PICK(f16, 256) break;
-        case KVC_FP32:
-            KVC_NOALLOC_PICK(f32, 32) KVC_NOALLOC_PICK(f32, 64) KVC_NOALLOC_PICK(f32, 128)
-            KVC_NOALLOC_PICK(f32, 256) break;
-        default: break;
-    }
-#undef KVC_NOALLOC_PICK
-    return nullptr;
-}
-
-// Pipeline stages that fit the shared-memory budget; 0 if none do.
-int stages_for(const kvc::DecodeKernelInfo *info, int smem_optin) {
-    const int budget = smem_optin < kvc::SMEM_BUDGET ? smem_optin : kvc::SMEM_BUDGET;
-    int n = (budget - info->fixed_smem) / info->stage_bytes;
-    if (n > 32) n = 32;
-    return n < info->consumer_warps + 1 ? 0 : n;
-}
-
 // One-time set-up for the current device: the scratch array's device
 // address, the SM count and the shared-memory limit.
 kvc_status setup_device(int dev, DeviceSetup **out) {
@@ -134,7 +107,7 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
                           reinterpret_cast<uintptr_t>(q);
     if (mis & 15u) return KVC_ERR_ALIGNMENT;
     const int G = cfg->n_heads / cfg->n_kv_heads;
-    const kvc::DecodeKernelInfo *info = lookup_kernel(cfg->dtype, cfg->d_head, G);
+    const kvc::DecodeKernelInfo *info = kvc::find_decode_kernel(cfg->dtype, cfg->d_head, G);
     if (!info) return KVC_ERR_UNSUPPORTED;
 
     int dev = 0;
@@ -145,25 +118,16 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
         std::lock_guard<std::mutex> lock(g_setup_mutex);
         kvc_status st = setup_device(dev, &ds);
         if (st != KVC_OK) return st;
-        n_stages = stages_for(info, ds->smem_optin);
+        n_stages = kvc::decode_stage_count(info, ds->smem_optin);
         if (n_stages == 0) return KVC_ERR_UNSUPPORTED;
         smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;
         st = ensure_smem_attribute(dev, info, smem_bytes);
         if (st != KVC_OK) return st;
     }
 
-    // Grid: the same choice as kvc_decode_attn, at most one CTA per SM.
-    const int64_t upper_rows = int64_t(cfg->batch) * cfg->n_kv_heads *
-                               (max_valid_hint > 0 ? max_valid_hint : cfg->max_context);
-    const int64_t min_rows = 4 * int64_t(info->tile_rows);
-    int64_t grid = (upper_rows + min_rows - 1) / min_rows;
-    // small problem with short segments: one CTA per segment (no split combine)
-    const int64_t nseg = int64_t(cfg->batch) * cfg->n_kv_heads;
-    const int64_t seg_rows = max_valid_hint > 0 ? max_valid_hint : cfg->max_context;
-    if (grid < ds->num_sms && nseg <= ds->num_sms && seg_rows * cfg->d_head * eb <= 65536) grid = nseg;
-    if (grid > ds->num_sms) grid = ds->num_sms;
-    if (grid > kvc::MAX_CTAS) grid = kvc::MAX_CTAS;
-    if (grid < 1) grid = 1;
+    // Grid: the choice kvc_decode_attn makes, at most one CTA per SM.
+    const int grid = kvc::decode_grid(info, cfg->batch, cfg->n_kv_heads, cfg->d_head, eb, cfg->max_context,
+                                      max_valid_hint, ds->num_sms, 0);
 
     // Scratch layout inside the array: error word, one counter per
     // (sequence, KV head), one publish flag per split slot, then the split
@@ -187,20 +151,24 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
                                 &maps[0], &maps[1], &maps[2], &maps[3], info->tile_box))
         return KVC_ERR_CUDA;
 
-    // The array keeps the previous call's contents: the error word, the
-    // counters and the publish flags must start at zero.
+    // The array keeps the previous call's contents: the counters and the
+    // publish flags must start at zero.  The error word is left alone: it
+    // keeps the first error any call recorded until kvc_static_get_error
+    // reads and clears it.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ds->scratch, 0, off_ml, s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaMemsetAsync(ds->scratch + off_tickets, 0, off_ml - off_tickets, s) != cudaSuccess) return KVC_ERR_CUDA;
 
     const uint64_t slab = uint64_t(cfg->batch) * cfg->n_kv_heads * uint64_t(cfg->max_context) *
                           cfg->d_head * eb;
-    kvc::DecodeArgs a;
+    kvc::DecodeArgs a{};
     a.K = static_cast<const uint8_t *>(k_base) + slab * layer;
     a.V = static_cast<const uint8_t *>(v_base) + slab * layer;
     a.q = q;
     a.out = out;
     a.k_new = nullptr;
     a.v_new = nullptr;
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     a.valid_len = valid_len;
     a.part_ml = reinterpret_cast<float *>(ds->scratch + off_ml);
     a.part_acc = reinterpret_cast<float *>(ds->scratch + off_acc);
@@ -213,6 +181,7 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     a.n_stages = n_stages;
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
+    a.flag_timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.seg_base = layer * cfg->batch * cfg->n_kv_heads;
     a.block_table = nullptr;
     a.max_blocks = a.num_blocks = 0;
@@ -225,4 +194,21 @@ extern "C" kvc_status kvc_decode_attn_static(const kvc_config *cfg, int32_t laye
     }
     const cudaError_t e = info->launch(a, int(grid), smem_bytes, s);
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+extern "C" kvc_status kvc_static_get_error(void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
+    DeviceSetup *ds = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        const kvc_status st = setup_device(dev, &ds);
+        if (st != KVC_OK) return st;
+    }
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    int32_t word = 0;  // host stack: the read allocates nothing
+    if (cudaMemcpy(&word, ds->scratch, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ERR_CUDA;
+    if (word != 0 && cudaMemset(ds->scratch, 0, sizeof word) != cudaSuccess) return KVC_ERR_CUDA;
+    if (word != 0 && cudaDeviceSynchronize() != cudaSuccess) return KVC_ERR_CUDA;
+    return static_cast<kvc_status>(word);
 }

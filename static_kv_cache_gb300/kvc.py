@@ -90,6 +90,10 @@ _lib.kvc_decode_attn_static.argtypes = [_cfgp, _i32, _vp, _vp, _vp, _vp, _i32, _
 _lib.kvc_decode_attn_static.restype = _i32
 _lib.kvc_get_error.argtypes = [_vp, _vp]
 _lib.kvc_get_error.restype = _i32
+_lib.kvc_static_get_error.argtypes = [_vp]
+_lib.kvc_static_get_error.restype = _i32
+_lib.kvc_set_wait_timeout_ns.argtypes = [_vp, _u64]
+_lib.kvc_set_wait_timeout_ns.restype = _i32
 
 
 def _ptr(x):
@@ -174,6 +178,10 @@ def kvc_set_num_splits(h, n: int) -> int:
     return _lib.kvc_set_num_splits(h, int(n))
 
 
+def kvc_set_wait_timeout_ns(h, ns: int) -> int:
+    return _lib.kvc_set_wait_timeout_ns(h, int(ns))
+
+
 def kvc_append(h, layer: int, k_new, v_new, cache_index, T_new: int, stream=None) -> int:
     return _lib.kvc_append(h, int(layer), _ptr(k_new), _ptr(v_new), _ptr(cache_index),
                            int(T_new), _stream(stream))
@@ -203,6 +211,10 @@ def kvc_decode_attn_static(cfg: kvc_config, layer: int, k_base, v_base, q, valid
 
 def kvc_get_error(h, stream=None) -> int:
     return _lib.kvc_get_error(h, _stream(stream))
+
+
+def kvc_static_get_error(stream=None) -> int:
+    return _lib.kvc_static_get_error(_stream(stream))
 
 
 def check(status: int, what: str = "") -> None:

@@ -84,6 +84,7 @@ def test_handle_calls_reject_null(kvc_library_path):
     assert kvc.kvc_decode_attn(None, 0, 16, 16, 0, 16) == kvc.KVC_ERR_INVALID
     assert kvc.kvc_get_error(None) == kvc.KVC_ERR_INVALID
     assert kvc.kvc_set_num_splits(None, 1) == kvc.KVC_ERR_INVALID
+    assert kvc.kvc_set_wait_timeout_ns(None, 1000) == kvc.KVC_ERR_INVALID
     kvc.kvc_free(None)
 
 

@@ -178,3 +178,34 @@ def test_prefill_host_errors():
     qf = torch.zeros((2, 8, 4, 128), dtype=torch.float32, device="cuda")
     assert kvc.kvc_prefill_attn(hf.h, 0, qf, ci, 4, qf, None) == kvc.KVC_ERR_UNSUPPORTED
     assert hn.error() == 0
+
+
+@pytest.mark.parametrize("prefixes", [None, [4096, 0, 4095, 31]], ids=["bench_prefixes", "longest_prefixes"])
+def test_benchmarked_prefill_layer_against_the_oracle(prefixes):
+    """One layer of the benchmarked chunked-prefill workload, in the launch
+    configuration the benchmark times: Llama-3-8B-shaped cache (H=32, H_kv=8,
+    d_h=128, bf16), B=4, a 512-token chunk each, after the workload's own
+    live prefixes (drawn from U{0..4096}) and after the longest prefixes that
+    range allows (4096 rows: the chunk's last CTAs stream 4608 key rows, over
+    30 rounds of the ring of stages).  Every chunk row of sampled (sequence,
+    KV head) groups -- one per sequence, two for the longest prefix -- is
+    compared with the fp64 oracle element by element, and every output is
+    checked finite."""
+    w = synth.WORKLOADS["llama3_8b_prefill"].with_(n_layers=1)
+    prefix = synth.live_lengths(w) if prefixes is None else torch.tensor(prefixes, dtype=torch.int32)
+    T, g = w.chunk, w.group
+    hn = _gpu.Harness(w)
+    _gpu.fill_prefix(hn, 0, prefix.tolist(), "bench")
+    q, out = _chunk(hn, 0, prefix.tolist(), T, "bench")
+    assert hn.error() == 0 and hn.canaries_intact()
+    assert torch.isfinite(out.float()).all(), "a masked or padded row was read"
+    longest = int(np.argmax(prefix.numpy()))
+    groups = [(b, (3 * b + 1) % w.n_kv_heads) for b in range(w.batch)] + [(longest, w.n_kv_heads - 1)]
+    for b, kv in groups:
+        ctx = int(prefix[b]) + T
+        Kh = _gpu.bits(hn.K[0, b:b + 1, kv:kv + 1, :ctx])
+        Vh = _gpu.bits(hn.V[0, b:b + 1, kv:kv + 1, :ctx])
+        qh = _gpu.bits(q[b:b + 1, kv * g:(kv + 1) * g])
+        ref = oracle.prefill_attn(qh, Kh, Vh, [int(prefix[b])], T, w.dtype)
+        _compare(out[b:b + 1, kv * g:(kv + 1) * g], ref, w.dtype,
+                 f"sequence {b} (prefix {int(prefix[b])}), KV head {kv}")
