@@ -50,13 +50,13 @@ KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
 
 def decode_kernel_name(w: synth.Workload) -> str:
     """The decode kernel the library picks for a workload: the tensor-core
-    kernel for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128,
+    kernel for 16-bit caches with head groups of 2 to 8, 16, 32 or 64 and d_h of 64 or 128,
     the CUDA-core kernel otherwise."""
     if w.d_latent:
         return "mla_decode_kernel"
     if w.dtype == "int8":
         return "decode_q8_kernel"
-    if w.dtype in ("bf16", "fp16") and 2 <= w.group <= 8 and w.d_head in (64, 128):
+    if w.dtype in ("bf16", "fp16") and (2 <= w.group <= 8 or w.group in (16, 32, 64)) and w.d_head in (64, 128):
         return "decode_mma_kernel"
     return "decode_split_kernel"
 
@@ -84,9 +84,10 @@ def parse_args(argv=None):
 
 
 # The other configurations the throughput target names (the Llama-2-70B layer
-# at 32k, B=1 and B=4) and the Qwen2.5 shape in both cache types: timed after
-# the headline in the default single-GPU run and reported under "configs".
-EXTRA_WORKLOADS = ("llama2_70b_b1", "llama2_70b_b4", "qwen2_5_1_5b_bf16", "qwen2_5_1_5b_fp32")
+# at 32k, B=1 and B=4), the Qwen2.5 shape in both cache types and the 32-head
+# multi-query shape: timed after the headline in the default single-GPU run
+# and reported under "configs".
+EXTRA_WORKLOADS = ("llama2_70b_b1", "llama2_70b_b4", "qwen2_5_1_5b_bf16", "qwen2_5_1_5b_fp32", "mqa_32h")
 
 
 def dist_env():

@@ -99,7 +99,10 @@ typedef enum { KVC_BF16 = 0, KVC_FP32 = 1, KVC_FP16 = 2, KVC_INT8 = 3 } kvc_dtyp
  *   d_head       d_h, head width: 32, 64, 128 or 256
  *   max_context  T_max, rows allocated per (layer, sequence, KV head)
  *   dtype        kvc_dtype
- * Supported head groups g = n_heads / n_kv_heads: 1 to 8. */
+ * Supported head groups g = n_heads / n_kv_heads: 1 to 8 for every cache
+ * type and head width; 16, 32 and 64 (multi-query attention, "10.3" section
+ * 4.1: one KV head shared by all query heads, g = n_heads) for 16-bit caches
+ * (KVC_BF16, KVC_FP16) with d_head 64 or 128. */
 typedef struct {
     int32_t n_layers;
     int32_t batch;
@@ -192,7 +195,7 @@ uint64_t kvc_pool_bytes(const kvc_config *cfg, int32_t num_blocks);
  * sequence's live length are never read.  A table entry outside
  * [0, num_blocks) is recorded as KVC_ERR_DEVICE_INDEX and its rows are
  * neither read nor written.  cfg->max_context must be a multiple of 16.
- * Built for 16-bit caches with head groups of 2 to 8 and d_h of 64 or 128
+ * Built for 16-bit caches with head groups of 2 to 8, 16, 32 or 64 and d_h of 64 or 128
  * (KVC_ERR_UNSUPPORTED otherwise); kvc_prefill_attn returns
  * KVC_ERR_UNSUPPORTED on a paged handle.  Other arguments and errors as for
  * kvc_alloc. */
@@ -276,7 +279,7 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q,
  * rows [0, valid_len[b]).  The result equals kvc_append(h, layer, k_new,
  * v_new, valid_len[b] - 1, T_new = 1) followed by kvc_decode_attn with the
  * same arguments: the cache bytes are identical and the output agrees to
- * fp32 rounding.  For 16-bit caches with head groups of 2 to 8 and d_h of 64
+ * fp32 rounding.  For 16-bit caches with head groups of 2 to 8, 16, 32 or 64 and d_h of 64
  * or 128 it is one launch that reads the new rows straight from k_new /
  * v_new while it streams the older ones; otherwise it enqueues the append
  * and the attention back to back.

@@ -65,7 +65,7 @@ const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
 // kernel (the layouts coincide).  Null otherwise.
 const kvc::DecodeKernelInfo *find_decode_paged(const kvc_config *c) {
     const int G = c->n_heads / c->n_kv_heads;
-    if (G < 2 || G > 8) return nullptr;
+    if (G < 2 || (G > 8 && G != 16 && G != 32 && G != 64)) return nullptr;
     if (c->d_head == 128) {
         if (c->dtype == KVC_BF16) return kvc::decode_kernel_paged_bf16_128(G);
         if (c->dtype == KVC_FP16) return kvc::decode_kernel_paged_f16_128(G);

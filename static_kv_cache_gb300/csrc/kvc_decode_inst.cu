@@ -29,11 +29,14 @@ namespace kvc {
 
 // 16-bit caches with 2 to 8 query heads per KV head and d_h of 64 or 128 run
 // the tensor-core kernel; one query head per KV head, fp32 caches and the
-// other head widths run the CUDA-core kernel.
+// other head widths run the CUDA-core kernel.  Groups of 16, 32 and 64 heads
+// (multi-query attention) run the tensor-core kernel only.
 #if KVC_INST_TYPE != 2 && (KVC_INST_D == 64 || KVC_INST_D == 128)
 #define KVC_GROUPED(G) mma_decode_info<KVC_ELEM, KVC_INST_D, G>()
+#define KVC_LARGE_GROUP(G) mma_decode_info<KVC_ELEM, KVC_INST_D, G>()
 #else
 #define KVC_GROUPED(G) decode_info<KVC_ELEM, KVC_INST_D, G>()
+#define KVC_LARGE_GROUP(G) nullptr
 #endif
 
 #if defined(KVC_INST_PAGED)
@@ -53,6 +56,9 @@ const DecodeKernelInfo *KVC_PCAT(KVC_TAG)(int G) {
         case 6: return mma_decode_info<KVC_ELEM, 128, 6, true>();
         case 7: return mma_decode_info<KVC_ELEM, 128, 7, true>();
         case 8: return mma_decode_info<KVC_ELEM, 128, 8, true>();
+        case 16: return mma_decode_info<KVC_ELEM, 128, 16, true>();
+        case 32: return mma_decode_info<KVC_ELEM, 128, 32, true>();
+        case 64: return mma_decode_info<KVC_ELEM, 128, 64, true>();
         default: return nullptr;
     }
 }
@@ -67,6 +73,9 @@ const DecodeKernelInfo *KVC_TABLE_FN(int G) {
         case 6: return KVC_GROUPED(6);
         case 7: return KVC_GROUPED(7);
         case 8: return KVC_GROUPED(8);
+        case 16: return KVC_LARGE_GROUP(16);
+        case 32: return KVC_LARGE_GROUP(32);
+        case 64: return KVC_LARGE_GROUP(64);
         default: return nullptr;
     }
 }

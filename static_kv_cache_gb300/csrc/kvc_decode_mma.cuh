@@ -1,6 +1,7 @@
 // kvc_decode_mma.cuh -- the decode attention of kvc_decode.cuh with the two
 // contractions on the warp tensor-core path, for 16-bit caches and head
-// groups of 2 to 8.
+// groups of 2 to 8, 16, 32 and 64 (multi-query attention: "10.3", section
+// 4.1, one KV head shared by every query head).
 //
 // Same mathematics, decomposition and pipeline protocol as
 // decode_split_kernel ("10.3 -- KV cache implementation details", section 5,
@@ -41,6 +42,15 @@
 // piece; a merge warp combines the NW states, then writes the output or the
 // split partial (and, for the last CTA of a segment, combines the partials)
 // while the consumers keep the stage ring draining.
+//
+// Groups of more than 8 query heads (G = 8 * NC, NC = 2, 4 or 8) take the
+// heads in chunks of 8, one chunk per consumer warp: the NW consumers form
+// NW / NC streams of NC warps, the streams take the tiles round robin, and
+// the NC warps of a stream all read the same tile, each for its own 8 heads
+// (the tile's empty barrier completes after NC arrivals).  Every K/V byte is
+// still read from HBM once for the whole group; each warp's registers hold
+// the same state as for an 8-head group.  The merge warp combines the
+// streams' states one 8-head chunk at a time.
 #pragma once
 
 #include "kvc_decode.cuh"
@@ -85,8 +95,11 @@ struct MmaCfg {
     static constexpr int KSTEPS = D / 16;               // k-steps of S^T, m-tiles of O^T
     static constexpr int NW = 8;                        // consumer warps (+ producer + merger)
     static constexpr int THREADS = (NW + 2) * 32;
-    static constexpr int SCR_ACC_FLOATS = NW * G * D;
-    static constexpr int SCR_ML_FLOATS = NW * G * 2;
+    static constexpr int NC = (G + 7) / 8;              // 8-head chunks of the group
+    static constexpr int GW = G < 8 ? G : 8;            // heads of one consumer warp
+    static constexpr int NSTREAM = NW / NC;             // streams of NC warps taking tiles round robin
+    static constexpr int SCR_ACC_FLOATS = NSTREAM * G * D;
+    static constexpr int SCR_ML_FLOATS = NSTREAM * G * 2;
     static constexpr int VL_CACHE = 256;                // valid lengths kept in shared memory
     static constexpr int N_FLAGS = 8;                   // abort flag, then the final-combine job
     // 1 KB of slack to align the stages to the 1024-byte swizzle atom, the two
@@ -98,7 +111,8 @@ struct MmaCfg {
     static constexpr int HELP_MIN_OTHERS = 4;
 
     static_assert(sizeof(T) == 2, "the tensor-core path takes 16-bit caches");
-    static_assert(G >= 1 && G <= 8, "the query group must fit the N = 8 side of the tile");
+    static_assert(G >= 1 && (G <= 8 || (G % 8 == 0 && NW % NC == 0)),
+                  "a group of more than 8 heads is taken in whole 8-head chunks, one per consumer warp");
     static_assert(D % 64 == 0, "head width must be a multiple of 64 (128-byte swizzle blocks)");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the swizzle-atom alignment");
 
@@ -347,9 +361,11 @@ __device__ __forceinline__ uint32_t swz_lane_offset(int row, int half, int lane,
     return uint32_t(row) * 128 + ((uint32_t(2 * j) ^ uint32_t(half ^ (lane & 7))) << 4);
 }
 
-// A softmax state over a set of keys for the G heads of one KV head, as the
-// merge lanes hold it: lane l owns columns [l * D/32, (l + 1) * D/32).
-template <int D, int G>
+// A softmax state over a set of keys for G heads of one KV head, as the
+// merge lanes hold it: lane l owns columns [l * D/32, (l + 1) * D/32).  The
+// G heads are heads [h0, h0 + G) of a group of GS (the arrays below are laid
+// out per GS heads); for groups of up to 8 heads GS = G and h0 = 0.
+template <int D, int G, int GS = G>
 struct LaneState {
     static constexpr int DPL = D / 32;
     float acc[G][DPL];  // unnormalised output
@@ -369,18 +385,19 @@ struct LaneState {
     // Combine the states of slots [0, n) of a shared-memory array laid out
     // [slot][G][D] (acc) and [slot][G][2] (max, sum) into this state, which
     // it replaces.
-    __device__ __forceinline__ void reduce_slots(const float *sacc, const float *sml, int n, int lane) {
+    __device__ __forceinline__ void reduce_slots(const float *sacc, const float *sml, int n, int lane,
+                                                 int h0 = 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float M = -INFINITY;
-            for (int w = 0; w < n; ++w) M = fmaxf(M, sml[(w * G + h) * 2]);
+            for (int w = 0; w < n; ++w) M = fmaxf(M, sml[(w * GS + h0 + h) * 2]);
             float L = 0.f;
 #pragma unroll
             for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
             for (int w = 0; w < n; ++w) {
-                const float e = exp2f(sml[(w * G + h) * 2] - M);
-                L = fmaf(sml[(w * G + h) * 2 + 1], e, L);
-                const float *src = sacc + (w * G + h) * D + lane * DPL;
+                const float e = exp2f(sml[(w * GS + h0 + h) * 2] - M);
+                L = fmaf(sml[(w * GS + h0 + h) * 2 + 1], e, L);
+                const float *src = sacc + (w * GS + h0 + h) * D + lane * DPL;
                 if constexpr (DPL == 4) {
                     const float4 v = *reinterpret_cast<const float4 *>(src);
                     acc[h][0] = fmaf(v.x, e, acc[h][0]);
@@ -425,14 +442,14 @@ struct LaneState {
     // loads are issued together.
     template <int U>
     __device__ __forceinline__ void fold_partials(const DecodeArgs &a, int seg, int first, int last, int step,
-                                                  int skip, int lane) {
+                                                  int skip, int lane, int h0 = 0) {
         for (int c = first; c <= last; c += U * step) {
             float pm[U][G], pl[U][G], pa[U][G][DPL];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int cu = c + u * step;
                 const bool use = cu <= last && cu != skip;
-                const int64_t sl = int64_t(cu + seg) * G;
+                const int64_t sl = int64_t(cu + seg) * GS + h0;
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     pm[u][h] = -INFINITY;
@@ -474,8 +491,8 @@ struct LaneState {
     }
 
     // Publish this state as the split partial of slot `slot`.
-    __device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t slot, int lane) const {
-        const int64_t sl = slot * G;
+    __device__ __forceinline__ void store_partial(const DecodeArgs &a, int64_t slot, int lane, int h0 = 0) const {
+        const int64_t sl = slot * GS + h0;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float *dst = a.part_acc + (sl + h) * D + lane * DPL;
@@ -498,10 +515,10 @@ struct LaneState {
 
     // out[b, kv*G + h, :] = acc / l, rounded once.
     template <typename T>
-    __device__ __forceinline__ void write_output(const DecodeArgs &a, int b, int kv, int lane) const {
+    __device__ __forceinline__ void write_output(const DecodeArgs &a, int b, int kv, int lane, int h0 = 0) const {
         using Ops = ElemOps<T>;
-        const int H = a.H_kv * G;
-        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(b) * H + kv * G) * D + lane * DPL;
+        const int H = a.H_kv * GS;
+        T *ob = reinterpret_cast<T *>(a.out) + (int64_t(b) * H + kv * GS + h0) * D + lane * DPL;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float inv = 1.f / l[h];
@@ -626,6 +643,104 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
     return false;
 }
 
+// The merge warp for groups of more than 8 heads: the same protocol as
+// merge_pieces, with the streams' states combined one 8-head chunk at a time
+// (a lane holds one chunk's state, as for an 8-head group).  The ticket is
+// taken once per piece, before any chunk is published; a split publishes
+// every chunk, then its ready flag; the last split waits for the others'
+// flags, then folds their partials and writes the output chunk by chunk.
+// The consumers' states are released once every chunk has been read.  The
+// final combine is never handed to the whole CTA.
+template <typename T, int D, int G, int NSLOT>
+__device__ __forceinline__ void merge_pieces_chunked(const DecodeArgs &a, const Plan &plan, Walker walk,
+                                                     const float *scr_acc, const float *scr_ml, uint32_t scr_full,
+                                                     uint32_t scr_free, volatile int *flags, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr int NC = G / 8;
+    constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
+    static_assert(G % 8 == 0 && NC > 1, "for groups of whole 8-head chunks");
+    static_assert(2 * CHUNKS <= 32, "one 16-byte chunk of the new rows per lane");
+    const int64_t kv_slab = int64_t(a.max_ctx) * ROW_BYTES;
+    LaneState<D, 8, G> st;
+    uint32_t piece = 0;
+    Piece pc;
+    while (walk.next(a, pc)) {
+        if (a.k_new && pc.hi == pc.n && lane < 2 * CHUNKS) {
+            // fused step: store the new K and V rows into the cache (as merge_pieces)
+            const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
+            const bool is_v = lane >= CHUNKS;
+            const int c16 = is_v ? lane - CHUNKS : lane;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) + seg * ROW_BYTES) + c16);
+            uint8_t *cache = const_cast<uint8_t *>(is_v ? a.V : a.K);
+            int64_t row_off = seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES;
+            if (a.block_table) {
+                const int p = pc.n - 1;
+                const int phys = __ldg(a.block_table + int64_t(pc.b) * a.max_blocks + p / 16);
+                row_off = phys >= 0 && phys < a.num_blocks
+                              ? ((int64_t(phys) * a.H_kv + pc.kv) * 16 + p % 16) * ROW_BYTES
+                              : -1;
+            }
+            if (row_off >= 0) reinterpret_cast<uint4 *>(cache + row_off)[c16] = v;
+        }
+        bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
+        ok = __all_sync(FULL, ok);
+        if (!ok) {
+            if (lane == 0) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            return;
+        }
+        const int seg = pc.b * a.H_kv + pc.kv;
+        const int c0 = int(pc.seg_start / plan.chunk);
+        const int c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
+        const int me = int(blockIdx.x);
+        int mode = 0;  // 0: the piece is the whole segment, 1: publish a partial, 2: last split
+        if (c0 != c1) {
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(a.tickets + seg, 1);
+            ticket = __shfl_sync(FULL, ticket, 0);
+            mode = ticket < c1 - c0 ? 1 : 2;
+        }
+        if (mode == 2) {
+            bool pub = true;
+            for (int c = c0 + lane; c <= c1; c += 32)
+                if (c != me) pub = pub && dev::flag_wait_bounded(a.ready + c + seg, flags, a.flag_timeout_ns);
+            pub = __all_sync(FULL, pub);
+            if (!pub) {
+                if (lane == 0) {
+                    if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                    flags[0] = 1;
+                }
+                return;
+            }
+            __threadfence();
+        }
+#pragma unroll 1
+        for (int hc = 0; hc < NC; ++hc) {
+            st.reduce_slots(scr_acc, scr_ml, NSLOT, lane, 8 * hc);
+            if (mode == 1) {
+                st.store_partial(a, me + seg, lane, 8 * hc);
+            } else {
+                if (mode == 2) st.template fold_partials<fold_batch<D, 8>()>(a, seg, c0, c1, 1, me, lane, 8 * hc);
+                st.template write_output<T>(a, pc.b, pc.kv, lane, 8 * hc);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(scr_free);
+        ++piece;
+        if (mode == 1) {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) dev::flag_store(a.ready + me + seg, 1);
+        } else if (mode == 2) {
+            for (int c = c0 + lane; c <= c1; c += 32)
+                if (c != me) dev::flag_store(a.ready + c + seg, 0);
+            if (lane == 0) a.tickets[seg] = 0;
+        }
+    }
+}
+
 // PG: the tiles come from a paged pool in the half-row layout (MmaCfg::swz_pg);
 // only the d_h = 128 kernels need it (for d_h = 64 the layouts coincide).
 template <typename T, int D, int G, bool PG = false>
@@ -661,7 +776,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         dev::prefetch_tensormap(&a.tm_v8);
         for (int s = 0; s < ns; ++s) {
             dev::mbar_init(bar0 + 8 * s, 1);
-            dev::mbar_init(bar0 + 8 * (ns + s), 1);
+            dev::mbar_init(bar0 + 8 * (ns + s), C::NC);  // released by the NC warps of a stream
         }
         dev::mbar_init(scr_full, NW);
         dev::mbar_init(scr_free, 1);
@@ -702,9 +817,17 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     float *fin_acc = reinterpret_cast<float *>(smem);
     float *fin_ml = fin_acc + (NW + 1) * G * D;
     constexpr int FOLD_U = fold_batch<D, G>();
+    constexpr int NC = C::NC, NSTREAM = C::NSTREAM;
 
     // ---------------------------------------------------------------- merger
-    if (warp == 1) {
+    if constexpr (NC > 1) {
+        if (warp == 1) {
+            merge_pieces_chunked<T, D, G, NSTREAM>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
+            __syncwarp();
+            dev::named_barrier_sync(2, C::THREADS);
+            return;
+        }
+    } else if (warp == 1) {
         LaneState<D, G> st;
         FinalCombine job;
         const bool help = merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
@@ -736,6 +859,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp - 2;
+    const int strm = cw / NC;  // this warp's stream: tiles strm, strm + NSTREAM, ...
+    const int h0 = (cw % NC) * 8;  // first head of this warp's chunk (0 for groups up to 8)
     const int gq = lane >> 2;  // fragment row group: query head of B / C columns
     const int tq = lane & 3;   // quad lane
     const int H = a.H_kv * G;
@@ -776,11 +901,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     Piece pc;
     while (walk.next(a, pc)) {
         {
-            const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + gq) * D;
+            const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + h0 + gq) * D;
+            const bool qv = h0 + gq < G;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                qb[ks][0] = gq < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
-                qb[ks][1] = gq < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
+                qb[ks][0] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
+                qb[ks][1] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
             }
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -795,10 +921,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                 stage = 0;
                 ++round;
             }
-            if (int(t % NW) != cw) continue;
+            if (int(t % NSTREAM) != strm) continue;
             const int nr = min(TILE, pc.hi - row0);
             // Wait for the previous release of this stage first, then for its
-            // data: the reasoning is the one in decode_split_kernel.
+            // data: the reasoning is the one in decode_split_kernel, with a
+            // stream's NC warps in place of one warp (tile t - ns needs all of
+            // its stream's arrivals; t can only be released with this warp's).
             const uint32_t full_bar = bar0 + 8 * cur_stage;
             const uint32_t empty_bar = bar0 + 8 * (ns + cur_stage);
             bool ok = !flags[0] &&
@@ -917,27 +1045,27 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                   (piece == 0 || dev::mbar_wait_bounded(scr_free, (piece - 1) & 1, flags, a.timeout_ns));
         ok = __all_sync(FULL, ok);
         if (ok) {
-            const int h0 = 2 * tq, h1 = 2 * tq + 1;
+            const int ha = h0 + 2 * tq, hb = h0 + 2 * tq + 1;  // heads of this lane's two columns
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) {
                 const int d = 16 * mt + gq;
-                if (h0 < G) {
-                    scr_acc[(cw * G + h0) * D + d] = o[mt][0];
-                    scr_acc[(cw * G + h0) * D + d + 8] = o[mt][2];
+                if (ha < G) {
+                    scr_acc[(strm * G + ha) * D + d] = o[mt][0];
+                    scr_acc[(strm * G + ha) * D + d + 8] = o[mt][2];
                 }
-                if (h1 < G) {
-                    scr_acc[(cw * G + h1) * D + d] = o[mt][1];
-                    scr_acc[(cw * G + h1) * D + d + 8] = o[mt][3];
+                if (hb < G) {
+                    scr_acc[(strm * G + hb) * D + d] = o[mt][1];
+                    scr_acc[(strm * G + hb) * D + d + 8] = o[mt][3];
                 }
             }
             if (gq == 0) {
-                if (h0 < G) {
-                    scr_ml[(cw * G + h0) * 2] = m0;
-                    scr_ml[(cw * G + h0) * 2 + 1] = l0;
+                if (ha < G) {
+                    scr_ml[(strm * G + ha) * 2] = m0;
+                    scr_ml[(strm * G + ha) * 2 + 1] = l0;
                 }
-                if (h1 < G) {
-                    scr_ml[(cw * G + h1) * 2] = m1;
-                    scr_ml[(cw * G + h1) * 2 + 1] = l1;
+                if (hb < G) {
+                    scr_ml[(strm * G + hb) * 2] = m1;
+                    scr_ml[(strm * G + hb) * 2 + 1] = l1;
                 }
             }
         } else if (lane == 0) {
@@ -949,15 +1077,17 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         ++piece;
     }
 
-    // ---- the final combine, when the merger asks for it
-    dev::named_barrier_sync(3, (NW + 1) * 32);
-    if (flags[1]) {
-        const int seg = flags[2], c0 = flags[3], c1 = flags[4], me = flags[5];
-        LaneState<D, G> st;
-        st.clear();
-        st.template fold_partials<FOLD_U>(a, seg, c0 + cw, c1, NW + 1, me, lane);
-        st.store_slot(fin_acc, fin_ml, cw, lane);
+    // ---- the final combine, when the merger asks for it (groups up to 8 heads)
+    if constexpr (NC == 1) {
         dev::named_barrier_sync(3, (NW + 1) * 32);
+        if (flags[1]) {
+            const int seg = flags[2], c0 = flags[3], c1 = flags[4], me = flags[5];
+            LaneState<D, G> st;
+            st.clear();
+            st.template fold_partials<FOLD_U>(a, seg, c0 + cw, c1, NW + 1, me, lane);
+            st.store_slot(fin_acc, fin_ml, cw, lane);
+            dev::named_barrier_sync(3, (NW + 1) * 32);
+        }
     }
     dev::named_barrier_sync(2, C::THREADS);
 }

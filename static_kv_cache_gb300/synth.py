@@ -99,6 +99,11 @@ WORKLOADS = {
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1014),
+    # Multi-query attention ("10.3", section 4.1): 32 query heads share one KV
+    # head of width 128; B=128 ragged U{1024..8192}, so one layer's live K/V
+    # (about 300 MB) matches the Llama-3-8B-shaped GQA layer's.
+    "mqa_32h": Workload("mqa_32h", 32, 128, 32, 1, 128, 8192, "bf16", steps=1,
+                        ragged=(1024, 8192), seed=1040),
     # Chunked prefill on the Llama-3-8B-shaped cache: 4 sequences with live
     # prefixes U{0..4096}, a 512-token chunk each (appended, then attended).
     "llama3_8b_prefill": Workload("llama3_8b_prefill", 32, 4, 32, 8, 128, 8192, "bf16", steps=1,

@@ -72,10 +72,21 @@ def test_invalid_configs(kvc_library_path, bad):
     assert kvc.kvc_alloc(cfg, 16, 16, 16, 1 << 20)[0] == kvc.KVC_ERR_INVALID
 
 
-@pytest.mark.parametrize("cfg", [(1, 1, 16, 1, 128, 64, "bf16"), (1, 1, 8, 8, 96, 64, "bf16")])
+@pytest.mark.parametrize("cfg", [(1, 1, 12, 1, 128, 64, "bf16"), (1, 1, 8, 8, 96, 64, "bf16"),
+                                 (1, 1, 32, 1, 128, 64, "fp32"), (1, 1, 16, 1, 256, 64, "bf16"),
+                                 (1, 1, 128, 1, 128, 64, "bf16")])
 def test_unsupported_configs(kvc_library_path, cfg):
     from static_kv_cache_gb300 import kvc
     assert kvc.kvc_check_config(kvc.make_config(*cfg)) == kvc.KVC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("cfg", [(1, 1, 16, 1, 128, 64, "bf16"), (1, 1, 32, 1, 128, 64, "fp16"),
+                                 (1, 1, 64, 1, 64, 64, "bf16"), (1, 1, 32, 2, 128, 64, "bf16")])
+def test_multi_query_configs_are_supported(kvc_library_path, cfg):
+    """Groups of 16, 32 and 64 query heads per KV head ("10.3", section 4.1)
+    on 16-bit caches with d_h 64 or 128."""
+    from static_kv_cache_gb300 import kvc
+    assert kvc.kvc_check_config(kvc.make_config(*cfg)) == kvc.KVC_OK
 
 
 def test_handle_calls_reject_null(kvc_library_path):

@@ -146,6 +146,13 @@ def test_full_size_one_step(name, layers):
     _one_step(synth.WORKLOADS[name], layers)
 
 
+def test_full_size_mqa_one_step():
+    """The benchmarked multi-query shape (32 query heads on one KV head,
+    B=128, ragged U{1024..8192}), two of its layers: every sequence's append
+    and the whole layer's attention against the oracle."""
+    _one_step(synth.WORKLOADS["mqa_32h"].with_(n_layers=2), (1,))
+
+
 # --------------------------------------------------------------------------
 # Shapes spanning several tiles, ragged tails, every element type and
 # several head groups / widths, with the automatic and forced split counts.
@@ -164,6 +171,13 @@ CASES = [
     ("fp32", 32, 3, 1, 3, 333, 10),
     ("bf16", 64, 12, 4, 6, 1200, 11),
     ("fp16", 256, 16, 2, 2, 257, 12),
+    # head groups of 16, 32 and 64 ("10.3", section 4.1: multi-query
+    # attention, one KV head shared by every query head)
+    ("bf16", 128, 32, 1, 4, 2500, 13),
+    ("bf16", 128, 32, 2, 3, 1800, 14),
+    ("fp16", 64, 16, 1, 5, 1200, 15),
+    ("bf16", 128, 64, 1, 2, 1300, 16),
+    ("fp16", 128, 64, 2, 2, 900, 17),
 ]
 
 
@@ -225,6 +239,29 @@ def test_single_live_row_returns_v_exactly():
     assert st == 0
     want = v[:, :, 0].repeat_interleave(w.group, dim=1)
     assert torch.equal(out.view(torch.int16), want.contiguous().view(torch.int16))
+
+
+def test_mqa_equals_mha_on_repeated_heads():
+    """Multi-query attention (one KV head for all 32 query heads) equals MHA
+    over a cache holding that head repeated 32 times ("10.3", section 4.1)."""
+    g = 32
+    wq = synth.Workload("mqa", 1, 3, 32, 1, 128, 900, "bf16", steps=1, seed=42)
+    wm = wq.with_(n_kv_heads=32)
+    hq, hm = _gpu.Harness(wq), _gpu.Harness(wm)
+    lengths = torch.tensor([900, 1, 517], dtype=torch.int32)
+    _gpu.fill_prefix(hq, 0, lengths.tolist())
+    hm.K[0] = hq.K[0].repeat_interleave(g, dim=1)
+    hm.V[0] = hq.V[0].repeat_interleave(g, dim=1)
+    q = _gpu.query(wq, "m")
+    st, oq = hq.decode(0, q, lengths.cuda(), hint=900)
+    assert st == 0
+    st, om = hm.decode(0, q, lengths.cuda(), hint=900)
+    assert st == 0
+    assert (oq.float() - om.float()).abs().max().item() <= 2e-2
+    ref = oracle.decode_attn(_gpu.bits(q), _gpu.bits(hq.K[0]).copy(), _gpu.bits(hq.V[0]).copy(),
+                             lengths.numpy(), "bf16")
+    _gpu.compare(oq, ref, "bf16", "mqa")
+    assert hq.error() == 0 and hm.error() == 0
 
 
 def test_gqa_equals_mha_on_repeated_heads():
@@ -301,8 +338,12 @@ def test_alloc_errors():
     assert kvc.kvc_alloc(cfg, k.data_ptr() + 8, v, ws, need)[0] == kvc.KVC_ERR_ALIGNMENT
     bad = kvc.make_config(1, 1, 8, 3, 128, 64, "bf16")
     assert kvc.kvc_alloc(bad, k, v, ws, need)[0] == kvc.KVC_ERR_INVALID
-    unsup = kvc.make_config(1, 1, 16, 1, 128, 64, "bf16")    # g = 16
+    unsup = kvc.make_config(1, 1, 12, 1, 128, 64, "bf16")    # g = 12: not a whole number of 8-head chunks
     assert kvc.kvc_alloc(unsup, k, v, ws, need)[0] == kvc.KVC_ERR_UNSUPPORTED
+    for g, d, dt in ((16, 32, "bf16"), (32, 128, "fp32"), (128, 128, "bf16")):   # no kernel for these
+        assert kvc.kvc_check_config(kvc.make_config(1, 1, g, 1, d, 64, dt)) == kvc.KVC_ERR_UNSUPPORTED
+    for g, d in ((16, 64), (32, 128), (64, 128)):
+        assert kvc.kvc_check_config(kvc.make_config(1, 1, g, 1, d, 64, "bf16")) == kvc.KVC_OK
     st, h = kvc.kvc_alloc(cfg, k, v, ws, need)
     assert st == 0 and h
     kvc.kvc_free(h)

@@ -87,6 +87,8 @@ CASES = [
     ("fp16", 64, 12, 2, 3, 512, [512, 31, 257]),
     ("bf16", 128, 16, 2, 2, 1600, [1600, 15]),
     ("bf16", 64, 8, 1, 1, 2048, [2048]),
+    ("bf16", 128, 32, 1, 3, 800, [800, 17, 401]),
+    ("fp16", 64, 32, 2, 2, 512, [512, 100]),
 ]
 
 

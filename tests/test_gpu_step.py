@@ -68,6 +68,8 @@ SEQ = [
     ("bf16_g4_d128", "bf16", 128, 16, 4, 5, 700, [0, 31, 32, 250, 690]),
     ("fp16_g6_d64", "fp16", 64, 12, 2, 3, 300, [7, 64, 200]),
     ("bf16_g8_d128", "bf16", 128, 8, 1, 2, 520, [1, 480]),
+    ("bf16_g32_d128_mqa", "bf16", 128, 32, 1, 3, 600, [0, 33, 590]),
+    ("fp16_g16_d64", "fp16", 64, 32, 2, 2, 400, [64, 391]),
     ("fp32_g6_d128_two_launches", "fp32", 128, 12, 2, 3, 300, [0, 40, 290]),
     ("bf16_g1_d128_two_launches", "bf16", 128, 4, 4, 2, 300, [5, 100]),
 ]
@@ -110,7 +112,8 @@ EDGE_LENGTHS = [1, 2, 8, 9, 31, 32, 33, 40, 64, 65, 511, 700]
 
 
 @pytest.mark.parametrize("splits", [0, 1, 3, 13, 152])
-@pytest.mark.parametrize("dtype,D,H,H_kv", [("bf16", 128, 16, 4), ("fp16", 64, 6, 2)])
+@pytest.mark.parametrize("dtype,D,H,H_kv", [("bf16", 128, 16, 4), ("fp16", 64, 6, 2), ("bf16", 128, 32, 1),
+                                           ("fp16", 128, 32, 2)])
 def test_fused_step_equals_append_then_decode(splits, dtype, D, H, H_kv):
     B, T = len(EDGE_LENGTHS), 700
     w = synth.Workload(f"edge_{dtype}", 1, B, H, H_kv, D, T, dtype, steps=1, seed=931)
