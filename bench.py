@@ -968,17 +968,14 @@ def bench_prefill(args, rank, world, local):
                        "parallelism": f"replicas x{world}"},
             "prefill_tokens_per_s": round(world * w.batch * w.chunk / (elapsed / args.steps), 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_tc_kernel",
                          "peak_source": peak_src, "flops_per_launch": work["flops"],
                          "bytes_per_launch": work["bytes"],
                          "mean_launch_us": round(mean_launch_s * 1e6, 3)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         }
-        if extra is not None:
-            line["configs"] = extra
         print(json.dumps(line), flush=True)
-    if state is not None:
-        state.close()
+    state.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -35,6 +35,7 @@ struct kvc_cache {
     int smem_bytes;
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
     CUtensorMap pf_k32, pf_k8, pf_v32, pf_v8;  // the chunked prefill's (64-column blocks)
+    CUtensorMap pf_k128, pf_v128;             // and its whole-tile boxes (128 rows)
 };
 
 namespace {
@@ -209,6 +210,25 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
     return true;
 }
 
+bool kvc::encode_row_box_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
+                              const void *v_base, int rows, CUtensorMap *k, CUtensorMap *v) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16) || rows < 1 || rows > 256) return false;
+    const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(max_ctx) * D * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(rows), 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const void *bases[2] = {k_base, v_base};
+    CUtensorMap *outs[2] = {k, v};
+    for (int i = 0; i < 2; ++i)
+        if (encode(outs[i], dt, 3, const_cast<void *>(bases[i]), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    return true;
+}
+
 bool kvc::encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
                            CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -360,6 +380,11 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
         if (pinfo && info->tile_box &&
             !kvc::encode_cache_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
                                     &h->pf_k32, &h->pf_k8, &h->pf_v32, &h->pf_v8)) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
+        if (pinfo && !kvc::encode_row_box_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base,
+                                               128, &h->pf_k128, &h->pf_v128)) {
             delete h;
             return KVC_ERR_CUDA;
         }
@@ -544,8 +569,8 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const in
     if (!h->prefill) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
     const kvc_config &c = h->cfg;
-    const int64_t rows = int64_t(T_new) * h->group;
-    const int64_t q_blocks = (rows + h->prefill->q_rows - 1) / h->prefill->q_rows;
+    const int64_t tokens_per_cta = h->prefill->rows / h->group;  // >= 1: find_prefill checked the group
+    const int64_t q_blocks = (T_new + tokens_per_cta - 1) / tokens_per_cta;
     const int64_t grid = int64_t(c.batch) * c.n_kv_heads * q_blocks;
     if (grid > 0x7fffffff) return KVC_ERR_UNSUPPORTED;
     const uint64_t slab = layer_slab_bytes(h);
@@ -560,10 +585,13 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const in
     a.H_kv = c.n_kv_heads;
     a.max_ctx = c.max_context;
     a.T_new = T_new;
+    a.group = h->group;
     a.q_blocks = int(q_blocks);
     a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(c.d_head)));
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.seg_base = layer * c.batch * c.n_kv_heads;
+    a.tm_k128 = h->pf_k128;
+    a.tm_v128 = h->pf_v128;
     a.tm_k32 = h->pf_k32;
     a.tm_k8 = h->pf_k8;
     a.tm_v32 = h->pf_v32;

@@ -149,23 +149,26 @@ struct PrefillArgs {
     const int32_t *cache_index;  // [B]: row of each sequence's first chunk token
     int32_t *err;
     int32_t B, H_kv, max_ctx, T_new;
-    int32_t q_blocks;            // CTAs per (sequence, KV head): ceil(T_new * g / q_rows)
+    int32_t group;               // g = H / H_kv query heads per KV head
+    int32_t q_blocks;            // CTAs per (sequence, KV head): ceil(T_new / (rows / g))
     float scale_log2;            // log2(e) / sqrt(D)
     unsigned long long timeout_ns;
     int32_t seg_base;            // layer * B * H_kv (tensor-map segment of this layer)
-    CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;
+    // the cache viewed as [L*B*H_kv][T_max][D]: boxes of 64 columns x 128,
+    // 32 and 8 rows, 128-byte swizzle
+    CUtensorMap tm_k128, tm_v128, tm_k32, tm_k8, tm_v32, tm_v8;
 };
 
 // One compiled prefill kernel.
 struct PrefillKernelInfo {
-    int q_rows;  // query rows (chunk tokens x group heads) per CTA
+    int rows;    // query rows per CTA: rows / g chunk tokens of the g heads of a KV head
     int smem;    // dynamic shared memory per CTA
     cudaError_t (*set_max_smem)(int bytes);
     cudaError_t (*launch)(const PrefillArgs &a, int grid, int smem, cudaStream_t s);
 };
 
 // Registry of prefill kernels (16-bit caches, D = 64 or 128); nullptr for an
-// unsupported group size.
+// unsupported group size (more query heads per KV head than rows per CTA).
 #define KVC_DECLARE_PREFILL_TABLE(TAG, D) \
     const PrefillKernelInfo *prefill_kernel_##TAG##_##D(int G);
 KVC_DECLARE_PREFILL_TABLE(bf16, 64)
@@ -185,6 +188,11 @@ KVC_DECLARE_PREFILL_TABLE(f16, 128)
 bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
                        CUtensorMap *v8, bool tile_box = false);
+
+// Tensor maps of 16-bit K and V caches [n_segs][max_ctx][D] with boxes of 64
+// columns x `rows` rows (at most 256), 128-byte swizzle.  Host only.
+bool encode_row_box_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
+                         const void *v_base, int rows, CUtensorMap *k, CUtensorMap *v);
 
 // Quantising append for int8 caches (kvc_append.cu): bf16 rows -> one fp32
 // scale per row and int8 codes, written at cache_index[b] + index_offset.

@@ -2,7 +2,7 @@
 // element type and head width, selected at compile time by KVC_INST_TYPE
 // (0 bf16, 1 fp16) and KVC_INST_D (64 or 128).  The build compiles this file
 // once per pair, in parallel.
-#include "kvc_prefill.cuh"
+#include "kvc_prefill_tc.cuh"
 
 #ifndef KVC_INST_TYPE
 #error "KVC_INST_TYPE must be defined"
@@ -28,17 +28,9 @@
 namespace kvc {
 
 const PrefillKernelInfo *KVC_PTABLE_FN(int G) {
-    switch (G) {
-        case 1: return prefill_info<KVC_ELEM, KVC_INST_D, 1>();
-        case 2: return prefill_info<KVC_ELEM, KVC_INST_D, 2>();
-        case 3: return prefill_info<KVC_ELEM, KVC_INST_D, 3>();
-        case 4: return prefill_info<KVC_ELEM, KVC_INST_D, 4>();
-        case 5: return prefill_info<KVC_ELEM, KVC_INST_D, 5>();
-        case 6: return prefill_info<KVC_ELEM, KVC_INST_D, 6>();
-        case 7: return prefill_info<KVC_ELEM, KVC_INST_D, 7>();
-        case 8: return prefill_info<KVC_ELEM, KVC_INST_D, 8>();
-        default: return nullptr;
-    }
+    // one kernel per (element type, head width): the group only changes how
+    // the CTA's 128 query rows map to (head, token)
+    return G >= 1 && G <= TcPrefillCfg<KVC_ELEM, KVC_INST_D>::BM ? prefill_tc_info<KVC_ELEM, KVC_INST_D>() : nullptr;
 }
 
 }  // namespace kvc
