@@ -18,11 +18,13 @@
 //                        A = Q and B = K_j K-major in shared memory, S in
 //                        tensor memory (two buffers, so S_{j+1} is computed
 //                        while the softmax works on S_j)
-//   softmax              thread r of the four softmax warps owns row r (its
-//                        TMEM lane): tcgen05.ld of the row, causal mask on
-//                        the tiles that cross a row's limit, running max and
-//                        sum in fp32 (log2 domain); P rounded to the cache
-//                        type into shared memory (K-major, 128-byte swizzle)
+//   softmax              two threads own row r (its TMEM lane), 64 columns
+//                        each: tcgen05.ld of the row, causal mask on the
+//                        tiles that cross a row's limit, running max and sum
+//                        in fp32 (log2 domain; the two halves' maxima are
+//                        swapped through shared memory); P rounded to the
+//                        cache type into shared memory (K-major, 128-byte
+//                        swizzle)
 //   O += P_j . V_j       tcgen05.mma, N = d_h; B = V_j as stored ([key][d]:
 //                        the N dimension contiguous, an MN-major operand); O
 //                        stays in tensor memory for the whole key range.
@@ -32,9 +34,10 @@
 // tcgen05.st), after the previous P.V has completed.  The final O / l is
 // rounded once to the cache type.
 //
-// Warps: 0-3 softmax and epilogue, 4 producer (TMA boxes of 128 keys x 64
-// columns, 128-byte swizzle, two stages of K and V), 5 MMA issuer (one
-// thread) and tensor-memory owner.  Rows past the chunk's last visible key
+// Warps: 0-7 softmax and epilogue (two per TMEM lane quarter), 8 producer
+// (TMA boxes of 128 keys x 64 columns, 128-byte swizzle; a ring of K tiles,
+// released as soon as S has read them, and a ring of V tiles, released after
+// P.V), 9 MMA issuer (one thread) and tensor-memory owner.  Rows past the chunk's last visible key
 // are never read: a partial last tile is boxed in 32- and 8-row groups, its
 // remaining live rows copied by the producer's lanes, the rest zeroed.  Every
 // wait is bounded; a timeout records KVC_ERR_TIMEOUT, every role leaves its
@@ -59,14 +62,21 @@ struct TcPrefillCfg {
     static constexpr int BLK = 128 * 128;          // one column block of a 128-row tile
     static constexpr int Q_BYTES = CB * BLK;
     static constexpr int P_BYTES = (BN / 64) * BLK;
-    static constexpr int KT_BYTES = CB * BLK;
-    static constexpr int STAGE_BYTES = 2 * KT_BYTES;  // K tile, then V tile
-    static constexpr int NS = D == 64 ? 4 : 2;
-    // full[NS], empty[NS], s_full[2], p_full, p_free, q_full, mma_done
-    static constexpr int NBAR = 2 * NS + 6;
-    static constexpr int BAR_OFF = Q_BYTES + P_BYTES + NS * STAGE_BYTES;
-    static constexpr int SMEM = 1024 + BAR_OFF + 8 * NBAR + 32;  // + TMEM address, abort flag
-    static constexpr int THREADS = 192;
+    static constexpr int KT_BYTES = CB * BLK;        // one K (or V) tile
+    // K tiles are released as soon as S = Q.K^T has used them, V tiles only
+    // after P.V: separate rings, the K ring the deeper
+    static constexpr int NSK = D == 64 ? 4 : 2;
+    static constexpr int NSV = D == 64 ? 4 : 2;
+    // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2], p_full,
+    // p_free, q_full, mma_done, pair[4]
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 10;
+    static constexpr int BAR_OFF = Q_BYTES + P_BYTES + (NSK + NSV) * KT_BYTES;
+    // the two softmax threads of a row swap their halves' maxima (and at the
+    // end their sums) here: [tile parity][half][row]
+    static constexpr int XCH_OFF = BAR_OFF + 8 * NBAR + 32;  // after the TMEM address and the abort flag
+    static constexpr int SMEM = 1024 + XCH_OFF + 2 * 2 * BM * 4;
+    static constexpr int NSW = 8;                  // softmax warps: two per TMEM lane quarter
+    static constexpr int THREADS = (NSW + 2) * 32;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256;
     static constexpr float RESCALE_LOG2 = 8.f;
@@ -80,12 +90,27 @@ struct TcPrefillCfg {
     }
 };
 
+// 2^x on the special-function unit (the PTX instruction; flushes subnormal
+// results to zero, which only affects probabilities below 2^-126).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
     using C = TcPrefillCfg<T, D>;
     using Ops = MmaOps<T>;
-    constexpr int BM = C::BM, BN = C::BN, CB = C::CB, NS = C::NS, BLK = C::BLK;
+    constexpr int BM = C::BM, BN = C::BN, CB = C::CB, NSK = C::NSK, NSV = C::NSV, BLK = C::BLK;
     constexpr unsigned FULL = 0xffffffffu;
     constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t IDESC_S = tc::idesc_f16_f32acc(BF16, BM, BN, false, false);
@@ -94,13 +119,16 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = dev::smem_addr(smem);
-    const uint32_t q_s = sb, p_s = sb + C::Q_BYTES, st_s = p_s + C::P_BYTES;
-    const uint32_t bar = sb + C::BAR_OFF;  // full[NS], empty[NS], then the single barriers
-    const uint32_t s_full = bar + 16 * NS, p_full = s_full + 16, p_free = p_full + 8, q_full = p_free + 8,
-                   mma_done = q_full + 8;
+    const uint32_t q_s = sb, p_s = sb + C::Q_BYTES, k_s = p_s + C::P_BYTES, v_s = k_s + NSK * C::KT_BYTES;
+    const uint32_t kfull = sb + C::BAR_OFF, kempty = kfull + 8 * NSK, vfull = kempty + 8 * NSK,
+                   vempty = vfull + 8 * NSV;
+    const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 8, q_full = p_free + 8,
+                   mma_done = q_full + 8, pair_bar = mma_done + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + 8 * C::NBAR);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::BAR_OFF + 8 * C::NBAR + 16);
+    float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int PRODUCER = C::NSW, ISSUER = C::NSW + 1;  // the two single warps after the softmax warps
 
     const int G = a.group;
     const int TB = BM / G;                         // chunk tokens per CTA
@@ -112,20 +140,25 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&a.tm_k128);
         dev::prefetch_tensormap(&a.tm_v128);
-        for (int s = 0; s < NS; ++s) {
-            dev::mbar_init(bar + 8 * s, 1);         // TMA bytes (+ the producer's arrival)
-            dev::mbar_init(bar + 8 * (NS + s), 1);  // released by the commit after P.V
+        for (int s = 0; s < NSK; ++s) {
+            dev::mbar_init(kfull + 8 * s, 1);   // TMA bytes (+ the producer's arrival)
+            dev::mbar_init(kempty + 8 * s, 1);  // released by the commit after S = Q.K^T
+        }
+        for (int s = 0; s < NSV; ++s) {
+            dev::mbar_init(vfull + 8 * s, 1);
+            dev::mbar_init(vempty + 8 * s, 1);  // released by the commit after P.V
         }
         dev::mbar_init(s_full, 1);
         dev::mbar_init(s_full + 8, 1);
-        dev::mbar_init(p_full, 4);   // one arrival per softmax warp
+        dev::mbar_init(p_full, C::NSW);  // one arrival per softmax warp
         dev::mbar_init(p_free, 1);
-        dev::mbar_init(q_full, 4);
+        dev::mbar_init(q_full, C::NSW);
         dev::mbar_init(mma_done, 1);
+        for (int qd = 0; qd < 4; ++qd) dev::mbar_init(pair_bar + 8 * qd, 2);  // the two warps of a lane quarter
         flags[0] = 0;
         dev::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == ISSUER) {
         tc::tmem_alloc(dev::smem_addr(tmem_slot), C::TMEM_COLS);
         tc::tmem_relinquish();
     }
@@ -146,84 +179,90 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     const int kend = c + t0 + ntok;  // keys [0, kend) are visible to some row of the CTA
     const int ntiles = bad ? 0 : (kend + BN - 1) / BN;
 
-    int issued = 0;  // tiles whose copies the producer issued
-    if (warp == 4) {
+    int issued_k = 0, issued_v = 0;  // tiles whose copies the producer issued
+    if (warp == PRODUCER) {
         // ------------------------------------------------------------ producer
+        // K of tile j + 1 goes out before V of tile j: S needs K a whole
+        // softmax earlier than P.V needs V.
         const int z = a.seg_base + seg;
         const int64_t kv_slab = int64_t(a.max_ctx) * C::ROW_BYTES;
         const uint8_t *kseg = a.K + int64_t(seg) * kv_slab;
         const uint8_t *vseg = a.V + int64_t(seg) * kv_slab;
-        uint32_t generic_written = 0;
-        for (int j = 0; j < ntiles; ++j) {
-            const int s = j % NS;
-            const uint32_t round = uint32_t(j / NS);
-            if (round > 0) {
-                const bool w = dev::mbar_wait_bounded(bar + 8 * (NS + s), (round - 1) & 1, flags, a.timeout_ns);
-                if (!__all_sync(FULL, w)) {
-                    if (lane == 0) {
-                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
-                        flags[0] = 1;
-                    }
-                    break;
-                }
-            }
+        uint32_t generic_k = 0, generic_v = 0;  // stages whose last fill had generic-proxy stores
+        bool ok = true;
+        // one tile of one tensor into one stage
+        auto load = [&](bool is_v, int j, uint32_t dst, uint32_t full, uint32_t &generic, int s) {
             const int row0 = j * BN, nr = min(BN, kend - row0);
-            const uint32_t full = bar + 8 * s;
-            const uint32_t kdst = st_s + uint32_t(s) * C::STAGE_BYTES, vdst = kdst + C::KT_BYTES;
-            // the stage's last fill had generic-proxy stores: order them
-            // before the TMA unit writes it again
-            if (generic_written & (1u << s)) dev::fence_proxy_async_smem();
+            const CUtensorMap *m128 = is_v ? &a.tm_v128 : &a.tm_k128;
+            const CUtensorMap *m32 = is_v ? &a.tm_v32 : &a.tm_k32;
+            const CUtensorMap *m8 = is_v ? &a.tm_v8 : &a.tm_k8;
+            // generic-proxy stores of the stage's last fill come before the
+            // TMA unit writes it again
+            if (generic & (1u << s)) dev::fence_proxy_async_smem();
             if (nr == BN) {
                 if (lane == 0) {
-                    dev::mbar_arrive_expect_tx(full, 2u * BN * C::ROW_BYTES);
+                    dev::mbar_arrive_expect_tx(full, uint32_t(BN) * C::ROW_BYTES);
+#pragma unroll
+                    for (int cb = 0; cb < CB; ++cb) dev::tma_load_3d(dst + cb * BLK, m128, cb * 64, row0, z, full);
+                }
+                generic &= ~(1u << s);
+                return;
+            }
+            // a partial tile: 32-row, then 8-row boxes over the live rows, the
+            // remaining live rows by 16-byte loads, zeros after them
+            const int n32 = nr >> 5, n8 = (nr >> 3) & 3, boxed = 32 * n32 + 8 * n8;
+            if (lane == 0) {
+                dev::mbar_expect_tx(full, uint32_t(boxed) * C::ROW_BYTES);
+                for (int g = 0; g < n32; ++g)
+#pragma unroll
+                    for (int cb = 0; cb < CB; ++cb)
+                        dev::tma_load_3d(dst + cb * BLK + g * 32 * 128, m32, cb * 64, row0 + 32 * g, z, full);
+                for (int g = 0; g < n8; ++g)
 #pragma unroll
                     for (int cb = 0; cb < CB; ++cb) {
-                        dev::tma_load_3d(kdst + cb * BLK, &a.tm_k128, cb * 64, row0, z, full);
-                        dev::tma_load_3d(vdst + cb * BLK, &a.tm_v128, cb * 64, row0, z, full);
+                        const int r = 32 * n32 + 8 * g;
+                        dev::tma_load_3d(dst + cb * BLK + r * 128, m8, cb * 64, row0 + r, z, full);
                     }
-                }
-                generic_written &= ~(1u << s);
-            } else {
-                // a partial tile: 32-row, then 8-row boxes over the live rows,
-                // the remaining live rows by 16-byte loads, zeros after them
-                const int n32 = nr >> 5, n8 = (nr >> 3) & 3, boxed = 32 * n32 + 8 * n8;
-                if (lane == 0) {
-                    dev::mbar_expect_tx(full, 2u * uint32_t(boxed) * C::ROW_BYTES);
-                    for (int g = 0; g < n32; ++g)
-#pragma unroll
-                        for (int cb = 0; cb < CB; ++cb) {
-                            const uint32_t off = cb * BLK + g * 32 * 128;
-                            dev::tma_load_3d(kdst + off, &a.tm_k32, cb * 64, row0 + 32 * g, z, full);
-                            dev::tma_load_3d(vdst + off, &a.tm_v32, cb * 64, row0 + 32 * g, z, full);
-                        }
-                    for (int g = 0; g < n8; ++g)
-#pragma unroll
-                        for (int cb = 0; cb < CB; ++cb) {
-                            const int r = 32 * n32 + 8 * g;
-                            const uint32_t off = cb * BLK + r * 128;
-                            dev::tma_load_3d(kdst + off, &a.tm_k8, cb * 64, row0 + r, z, full);
-                            dev::tma_load_3d(vdst + off, &a.tm_v8, cb * 64, row0 + r, z, full);
-                        }
-                }
-                const int per = (BN - boxed) * C::CHUNKS;  // 16-byte chunks per tensor after the boxes
-                for (int i = lane; i < 2 * per; i += 32) {
-                    const bool is_v = i >= per;
-                    const int jj = is_v ? i - per : i;
-                    const int r = boxed + jj / C::CHUNKS, c16 = jj % C::CHUNKS;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < nr)
-                        v = __ldg(reinterpret_cast<const uint4 *>((is_v ? vseg : kseg) +
-                                                                  int64_t(row0 + r) * C::ROW_BYTES) + c16);
-                    dev::st_shared_v4(C::swz(is_v ? vdst : kdst, r, c16), v);
-                }
-                dev::fence_proxy_async_smem();  // the tensor core reads these rows
-                generic_written |= 1u << s;
-                __syncwarp();
-                if (lane == 0) dev::mbar_arrive(full);
             }
-            issued = j + 1;
+            const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0) * C::ROW_BYTES;
+            for (int i = lane; i < (BN - boxed) * C::CHUNKS; i += 32) {
+                const int r = boxed + i / C::CHUNKS, c16 = i % C::CHUNKS;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (r < nr) v = __ldg(reinterpret_cast<const uint4 *>(src + int64_t(r) * C::ROW_BYTES) + c16);
+                dev::st_shared_v4(C::swz(dst, r, c16), v);
+            }
+            dev::fence_proxy_async_smem();  // the tensor core reads these rows
+            generic |= 1u << s;
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(full);
+        };
+        auto wait_free = [&](uint32_t empty, int j, int ns) {
+            if (j < ns) return true;
+            const bool w = dev::mbar_wait_bounded(empty, uint32_t(j / ns - 1) & 1, flags, a.timeout_ns);
+            if (__all_sync(FULL, w)) return true;
+            if (lane == 0) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            return false;
+        };
+        for (int j = 0; ok && j <= ntiles; ++j) {
+            if (j < ntiles) {
+                const int s = j % NSK;
+                ok = wait_free(kempty + 8 * s, j, NSK);
+                if (!ok) break;
+                load(false, j, k_s + uint32_t(s) * C::KT_BYTES, kfull + 8 * s, generic_k, s);
+                issued_k = j + 1;
+            }
+            if (j > 0) {
+                const int jv = j - 1, s = jv % NSV;
+                ok = wait_free(vempty + 8 * s, jv, NSV);
+                if (!ok) break;
+                load(true, jv, v_s + uint32_t(s) * C::KT_BYTES, vfull + 8 * s, generic_v, s);
+                issued_v = jv + 1;
+            }
         }
-    } else if (warp == 5) {
+    } else if (warp == ISSUER) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = dev::mbar_wait_bounded(q_full, 0, flags, a.timeout_ns);
@@ -233,11 +272,11 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                 if (j < ntiles) {
                     // S_j = Q . K_j^T into S buffer j % 2 (free: the softmax of
                     // tile j - 2 was waited for before P.V of tile j - 2)
-                    const int s = j % NS;
-                    ok = dev::mbar_wait_bounded(bar + 8 * s, uint32_t(j / NS) & 1, flags, a.timeout_ns);
+                    const int s = j % NSK;
+                    ok = dev::mbar_wait_bounded(kfull + 8 * s, uint32_t(j / NSK) & 1, flags, a.timeout_ns);
                     if (!ok) break;
                     tc::fence_after();
-                    const uint32_t kt = st_s + uint32_t(s) * C::STAGE_BYTES;
+                    const uint32_t kt = k_s + uint32_t(s) * C::KT_BYTES;
                     const uint32_t s_t = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
@@ -246,21 +285,23 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                                        tc::smem_desc_sw128(kt + off, 16, 1024), IDESC_S, ks > 0);
                     }
                     tc::commit(s_full + 8 * (j & 1));
+                    tc::commit(kempty + 8 * s);  // K stage free
                 }
                 if (j > 0) {
                     // O += P_{j-1} . V_{j-1}, once the softmax has written P
-                    const int jp = j - 1, sp = jp % NS;
-                    ok = dev::mbar_wait_bounded(p_full, uint32_t(jp) & 1, flags, a.timeout_ns);
+                    const int jp = j - 1, sp = jp % NSV;
+                    ok = dev::mbar_wait_bounded(p_full, uint32_t(jp) & 1, flags, a.timeout_ns) &&
+                         dev::mbar_wait_bounded(vfull + 8 * sp, uint32_t(jp / NSV) & 1, flags, a.timeout_ns);
                     if (!ok) break;
                     tc::fence_after();
-                    const uint32_t vt = st_s + uint32_t(sp) * C::STAGE_BYTES + C::KT_BYTES;
+                    const uint32_t vt = v_s + uint32_t(sp) * C::KT_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < BN / 16; ++ks) {
                         tc::mma_f16_ss(o_t, tc::smem_desc_sw128(p_s + (ks >> 2) * BLK + (ks & 3) * 32, 16, 1024),
                                        tc::smem_desc_sw128(vt + ks * 2048, BLK, 1024), IDESC_O, (jp > 0 || ks > 0));
                     }
-                    tc::commit(bar + 8 * (NS + sp));  // K/V stage free
-                    tc::commit(p_free);               // P buffer free, O up to date
+                    tc::commit(vempty + 8 * sp);  // V stage free
+                    tc::commit(p_free);           // P buffer free, O up to date
                 }
             }
             if (!ok) {
@@ -275,17 +316,24 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = threadIdx.x;              // query row = TMEM lane
+        // Two warps per TMEM lane quarter: thread (qd, hf) owns row r of the
+        // quarter and columns [64 hf, 64 hf + 64) of S (and half of O); the
+        // two threads of a row swap their maxima through shared memory under
+        // a bounded mbarrier of the pair.
+        const int qd = warp & 3, hf = warp >> 2;
+        const int r = 32 * qd + lane;           // query row = TMEM lane
         const int i = r / TB, tt = r - i * TB;  // head of the group, token of the block
         const bool row_ok = !bad && i < G && tt < ntok;
         const int t = t0 + tt;
         const int H = a.H_kv * G;
         const int64_t row_elem = ((int64_t(b) * H + kv * G + i) * a.T_new + t) * D;
+        const uint32_t pbar = pair_bar + 8 * qd;
+        constexpr int QC = C::CHUNKS / 2;       // 16-byte chunks of Q (and of O) per half row
         {
-            // Q row into shared memory (K-major, swizzled); unused rows zero
+            // this half of the Q row into shared memory (K-major, swizzled)
             const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.q) + row_elem);
 #pragma unroll
-            for (int c16 = 0; c16 < C::CHUNKS; ++c16) {
+            for (int c16 = hf * QC; c16 < (hf + 1) * QC; ++c16) {
                 const uint4 v = row_ok ? __ldg(qrow + c16) : make_uint4(0u, 0u, 0u, 0u);
                 dev::st_shared_v4(C::swz(q_s, r, c16), v);
             }
@@ -293,54 +341,75 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(q_full);
         }
+        // swap a value with the row's other thread: exchange k (0, 1, 2 ...)
+        auto swap = [&](float mine, int k, float &theirs) {
+            float *slot = xch + (k & 1) * 2 * BM;
+            slot[hf * BM + r] = mine;
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(pbar);
+            bool w = dev::mbar_wait_bounded(pbar, uint32_t(k) & 1, flags, a.timeout_ns);
+            w = __all_sync(FULL, w);
+            theirs = slot[(hf ^ 1) * BM + r];
+            return w;
+        };
         const int limit = row_ok ? c + t : c;  // last visible key (unused rows: any finite range)
         const int lim_min = c + t0;            // smallest limit of the CTA's rows
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        float m_run = -INFINITY, l_run = 0.f;
+        const uint32_t lane_base = uint32_t(qd * 32) << 16;
+        const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
+        float m_run = -INFINITY;
+        float2 l2 = make_float2(0.f, 0.f);     // this half's running sum, two partial lanes
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
+        int j = 0;
+        for (; j < ntiles; ++j) {
             ok = !flags[0] && dev::mbar_wait_bounded(s_full + 8 * (j & 1), uint32_t(j >> 1) & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc::fence_after();
-            uint32_t sr[4][32];
-            const uint32_t s_t = tmem + lane_base + ((j & 1) ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(s_t + 32 * q4, sr[q4]);
+            uint32_t sr[2][32];
+            const uint32_t s_t = tmem + lane_base + ((j & 1) ? C::S_COL1 : C::S_COL0) + 64 * hf;
+            tc::tmem_ld32(s_t, sr[0]);
+            tc::tmem_ld32(s_t + 32, sr[1]);
             tc::tmem_ld_wait();
+            tc::reg_fence(sr[0]);
+            tc::reg_fence(sr[1]);
+            const int key0 = j * BN + 64 * hf;
+            if (key0 + 63 > lim_min) {  // this half tile crosses some row's causal limit
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc::reg_fence(sr[q4]);
-            const int key0 = j * BN;
-            if (key0 + BN - 1 > lim_min) {  // the tile crosses some row's causal limit
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
+                for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        if (key0 + 32 * q4 + e > limit) sr[q4][e] = __float_as_uint(-INFINITY);
+                        if (key0 + 32 * h2 + e > limit) sr[h2][e] = __float_as_uint(-INFINITY);
             }
             float mx = -INFINITY;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[q4][e]));
-            const float m_tile = mx * a.scale_log2;
+                for (int e = 0; e < 32; e += 2)
+                    mx = fmax3(mx, __uint_as_float(sr[h2][e]), __uint_as_float(sr[h2][e + 1]));
+            float other;
+            ok = swap(mx, j, other);
+            if (!ok) break;
+            const float m_tile = fmaxf(mx, other) * a.scale_log2;
             // raise the reference max only when the tile's exceeds it by 2^8
+            // (both threads of the row take the same decision)
             const float m_new = m_tile > m_run + C::RESCALE_LOG2 ? m_tile : m_run;
-            const float corr = m_new == m_run ? 1.f : exp2f(m_run - m_new);
+            const float corr = m_new == m_run ? 1.f : ex2_approx(m_run - m_new);
             m_run = m_new;
-            const float neg = m_run == -INFINITY ? 0.f : -m_run;
-            float psum = 0.f;
-            uint32_t pk[64];
+            const float negm = m_run == -INFINITY ? 0.f : -m_run;
+            const float2 neg2 = make_float2(negm, negm);
+            float2 ps = make_float2(0.f, 0.f);
+            uint32_t pk[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = exp2f(fmaf(__uint_as_float(sr[q4][e]), a.scale_log2, neg));
-                    const float p1 = exp2f(fmaf(__uint_as_float(sr[q4][e + 1]), a.scale_log2, neg));
-                    psum += p0 + p1;
-                    pk[16 * q4 + e / 2] = Ops::pack(p0, p1);
+                    const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[h2][e]), __uint_as_float(sr[h2][e + 1])),
+                                                scale2, neg2);
+                    const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                    ps = __fadd2_rn(ps, make_float2(p0, p1));
+                    pk[16 * h2 + e / 2] = Ops::pack(p0, p1);
                 }
-            l_run = fmaf(l_run, corr, psum);
+            l2 = __ffma2_rn(l2, make_float2(corr, corr), ps);
             if (j > 0) {
                 // P.V of the previous tile has read P and written O
                 ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(j - 1) & 1, flags, a.timeout_ns);
@@ -348,25 +417,30 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                 if (!ok) break;
                 tc::fence_after();
                 if (__any_sync(FULL, corr != 1.f)) {
+                    const float2 c2 = make_float2(corr, corr);
 #pragma unroll
-                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                    for (int q4 = 0; q4 < D / 64; ++q4) {
                         uint32_t o[32];
-                        const uint32_t o_t = tmem + lane_base + C::O_COL + 32 * q4;
+                        const uint32_t o_t = tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q4;
                         tc::tmem_ld32(o_t, o);
                         tc::tmem_ld_wait();
                         tc::reg_fence(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2);
+                            o[e] = __float_as_uint(v.x);
+                            o[e + 1] = __float_as_uint(v.y);
+                        }
                         tc::tmem_st32(o_t, o);
                     }
                     tc::tmem_st_wait();
                 }
             }
-            // P row into shared memory: the A operand of O += P . V
+            // this half of the P row into shared memory: the A operand of O += P . V
 #pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16)
-                dev::st_shared_v4(C::swz(p_s, r, c16),
-                                  make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]));
+            for (int cc = 0; cc < 8; ++cc)
+                dev::st_shared_v4(C::swz(p_s, r, 8 * hf + cc),
+                                  make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]));
             dev::fence_proxy_async_smem();
             tc::fence_before();
             __syncwarp();
@@ -381,14 +455,16 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             // ---- epilogue: out = O / l, once the last P.V has completed
             ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(ntiles - 1) & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
+            float l_other = 0.f;
+            ok = ok && swap(l2.x + l2.y, ntiles, l_other);
             if (ok) {
                 tc::fence_after();
-                const float inv = 1.f / l_run;
-                uint4 *orow = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + row_elem);
+                const float inv = 1.f / (l2.x + l2.y + l_other);
+                uint4 *orow = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + row_elem) + hf * QC;
 #pragma unroll
-                for (int q4 = 0; q4 < D / 32; ++q4) {
+                for (int q4 = 0; q4 < D / 64; ++q4) {
                     uint32_t o[32];
-                    tc::tmem_ld32(tmem + lane_base + C::O_COL + 32 * q4, o);
+                    tc::tmem_ld32(tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q4, o);
                     tc::tmem_ld_wait();
                     tc::reg_fence(o);
 #pragma unroll
@@ -411,15 +487,17 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     // ---- teardown: every role is done; the MMAs have completed
     tc::fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == ISSUER) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (warp == 4 && lane == 0 && flags[0]) {
+    if (warp == PRODUCER && lane == 0 && flags[0]) {
         // after an abort, wait (bounded) for the copies that may still land
         const volatile int never = 0;
-        for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
-            dev::mbar_wait_bounded(bar + 8 * (j % NS), uint32_t(j / NS) & 1, &never, a.timeout_ns);
+        for (int j = issued_k > NSK ? issued_k - NSK : 0; j < issued_k; ++j)
+            dev::mbar_wait_bounded(kfull + 8 * (j % NSK), uint32_t(j / NSK) & 1, &never, a.timeout_ns);
+        for (int j = issued_v > NSV ? issued_v - NSV : 0; j < issued_v; ++j)
+            dev::mbar_wait_bounded(vfull + 8 * (j % NSV), uint32_t(j / NSV) & 1, &never, a.timeout_ns);
     }
 }
 
