@@ -18,20 +18,23 @@
 //                        A = Q and B = K_j K-major in shared memory, S in
 //                        tensor memory (two buffers, so S_{j+1} is computed
 //                        while the softmax works on S_j)
-//   softmax              two threads own row r (its TMEM lane), 64 columns
-//                        each: tcgen05.ld of the row, causal mask on the
-//                        tiles that cross a row's limit, running max and sum
-//                        in fp32 (log2 domain; the two halves' maxima are
-//                        swapped through shared memory); P rounded to the
-//                        cache type into shared memory (K-major, 128-byte
-//                        swizzle)
-//   O += P_j . V_j       tcgen05.mma, N = d_h; B = V_j as stored ([key][d]:
-//                        the N dimension contiguous, an MN-major operand); O
-//                        stays in tensor memory for the whole key range.
-// The running max is only raised when a tile's maximum exceeds it by more
-// than 2^8 (probabilities stay <= 256, no loss in fp32 or in P); only then
-// is the row of O in tensor memory rescaled (tcgen05.ld, multiply,
-// tcgen05.st), after the previous P.V has completed.  The final O / l is
+//   softmax              two threads own row r (its TMEM lane), one per half
+//                        of the key tile (64 keys): tcgen05.ld of that half
+//                        row, causal mask on the tiles that cross the row's
+//                        limit, a running max and sum in fp32 (log2 domain)
+//                        per half; P rounded to the cache type into shared
+//                        memory (K-major, 128-byte swizzle)
+//   O_h += P_h . V_h     tcgen05.mma per half h of the keys, N = d_h, into
+//                        one tensor-memory accumulator per half; B = V_j as
+//                        stored ([key][d]: the N dimension contiguous, an
+//                        MN-major operand).  O_0 and O_1 stay in tensor memory
+//                        for the whole key range.
+// Each half raises its reference max only when a tile's maximum exceeds it
+// by more than 2^8 (probabilities stay <= 256, no loss in fp32 or in P);
+// only then is its accumulator rescaled in tensor memory (tcgen05.ld,
+// multiply, tcgen05.st), after its previous P.V has completed.  The halves
+// never wait for each other: the epilogue swaps their (max, sum) once and
+// writes (O_0 e_0 + O_1 e_1) / (l_0 e_0 + l_1 e_1), e_h = 2^(m_h - max),
 // rounded once to the cache type.
 //
 // Warps: 0-7 softmax and epilogue (two per TMEM lane quarter), 8 producer
@@ -67,18 +70,20 @@ struct TcPrefillCfg {
     // after P.V: separate rings, the K ring the deeper
     static constexpr int NSK = D == 64 ? 4 : 2;
     static constexpr int NSV = D == 64 ? 4 : 2;
-    // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2], p_full,
-    // p_free, q_full, mma_done, pair[4]
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 10;
+    // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2],
+    // p_full[2], p_free[2], q_full, mma_done, pair[4]
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 12;
     static constexpr int BAR_OFF = Q_BYTES + P_BYTES + (NSK + NSV) * KT_BYTES;
-    // the two softmax threads of a row swap their halves' maxima (and at the
-    // end their sums) here: [tile parity][half][row]
+    // the two softmax threads of a row swap their halves' running maxima and
+    // sums here at the end: [2][half][row]
     static constexpr int XCH_OFF = BAR_OFF + 8 * NBAR + 32;  // after the TMEM address and the abort flag
     static constexpr int SMEM = 1024 + XCH_OFF + 2 * 2 * BM * 4;
     static constexpr int NSW = 8;                  // softmax warps: two per TMEM lane quarter
     static constexpr int THREADS = (NSW + 2) * 32;
     static constexpr uint32_t TMEM_COLS = 512;
+    // two S buffers, then one O accumulator per half of the key tile
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256;
+    static_assert(O_COL + 2 * D <= TMEM_COLS, "two S buffers and two O accumulators in tensor memory");
     static constexpr float RESCALE_LOG2 = 8.f;
 
     static_assert(D == 64 || D == 128, "head width 64 or 128");
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     const uint32_t q_s = sb, p_s = sb + C::Q_BYTES, k_s = p_s + C::P_BYTES, v_s = k_s + NSK * C::KT_BYTES;
     const uint32_t kfull = sb + C::BAR_OFF, kempty = kfull + 8 * NSK, vfull = kempty + 8 * NSK,
                    vempty = vfull + 8 * NSV;
-    const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 8, q_full = p_free + 8,
+    const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 16, q_full = p_free + 16,
                    mma_done = q_full + 8, pair_bar = mma_done + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + 8 * C::NBAR);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::BAR_OFF + 8 * C::NBAR + 16);
@@ -150,8 +155,10 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         }
         dev::mbar_init(s_full, 1);
         dev::mbar_init(s_full + 8, 1);
-        dev::mbar_init(p_full, C::NSW);  // one arrival per softmax warp
-        dev::mbar_init(p_free, 1);
+        for (int hf = 0; hf < 2; ++hf) {
+            dev::mbar_init(p_full + 8 * hf, C::NSW / 2);  // the four softmax warps of a half
+            dev::mbar_init(p_free + 8 * hf, 1);
+        }
         dev::mbar_init(q_full, C::NSW);
         dev::mbar_init(mma_done, 1);
         for (int qd = 0; qd < 4; ++qd) dev::mbar_init(pair_bar + 8 * qd, 2);  // the two warps of a lane quarter
@@ -267,7 +274,6 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         if (lane == 0) {
             bool ok = dev::mbar_wait_bounded(q_full, 0, flags, a.timeout_ns);
             tc::fence_after();
-            const uint32_t o_t = tmem + C::O_COL;
             for (int j = 0; ok && j <= ntiles; ++j) {
                 if (j < ntiles) {
                     // S_j = Q . K_j^T into S buffer j % 2 (free: the softmax of
@@ -288,20 +294,28 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                     tc::commit(kempty + 8 * s);  // K stage free
                 }
                 if (j > 0) {
-                    // O += P_{j-1} . V_{j-1}, once the softmax has written P
+                    // O_h += P_h . V_h for the two halves h of tile j - 1 (keys
+                    // [64 h, 64 h + 64)), each once its softmax warps have
+                    // written their half of P
                     const int jp = j - 1, sp = jp % NSV;
-                    ok = dev::mbar_wait_bounded(p_full, uint32_t(jp) & 1, flags, a.timeout_ns) &&
-                         dev::mbar_wait_bounded(vfull + 8 * sp, uint32_t(jp / NSV) & 1, flags, a.timeout_ns);
+                    ok = dev::mbar_wait_bounded(vfull + 8 * sp, uint32_t(jp / NSV) & 1, flags, a.timeout_ns);
                     if (!ok) break;
-                    tc::fence_after();
                     const uint32_t vt = v_s + uint32_t(sp) * C::KT_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks) {
-                        tc::mma_f16_ss(o_t, tc::smem_desc_sw128(p_s + (ks >> 2) * BLK + (ks & 3) * 32, 16, 1024),
-                                       tc::smem_desc_sw128(vt + ks * 2048, BLK, 1024), IDESC_O, (jp > 0 || ks > 0));
+                    for (int hf = 0; hf < 2; ++hf) {
+                        ok = dev::mbar_wait_bounded(p_full + 8 * hf, uint32_t(jp) & 1, flags, a.timeout_ns);
+                        if (!ok) break;
+                        tc::fence_after();
+                        const uint32_t o_t = tmem + C::O_COL + uint32_t(hf) * D;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc::mma_f16_ss(o_t, tc::smem_desc_sw128(p_s + hf * BLK + ks * 32, 16, 1024),
+                                           tc::smem_desc_sw128(vt + hf * 8192 + ks * 2048, BLK, 1024), IDESC_O,
+                                           (jp > 0 || ks > 0));
+                        tc::commit(p_free + 8 * hf);  // this half of P free, O_h up to date
                     }
+                    if (!ok) break;
                     tc::commit(vempty + 8 * sp);  // V stage free
-                    tc::commit(p_free);           // P buffer free, O up to date
                 }
             }
             if (!ok) {
@@ -317,9 +331,9 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     } else {
         // ------------------------------------------------------------ softmax
         // Two warps per TMEM lane quarter: thread (qd, hf) owns row r of the
-        // quarter and columns [64 hf, 64 hf + 64) of S (and half of O); the
-        // two threads of a row swap their maxima through shared memory under
-        // a bounded mbarrier of the pair.
+        // quarter and keys [64 hf, 64 hf + 64) of every tile, with its own
+        // running max and sum and its own accumulator O_hf in tensor memory.
+        // The halves never wait for each other; the epilogue combines them.
         const int qd = warp & 3, hf = warp >> 2;
         const int r = 32 * qd + lane;           // query row = TMEM lane
         const int i = r / TB, tt = r - i * TB;  // head of the group, token of the block
@@ -328,7 +342,7 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         const int H = a.H_kv * G;
         const int64_t row_elem = ((int64_t(b) * H + kv * G + i) * a.T_new + t) * D;
         const uint32_t pbar = pair_bar + 8 * qd;
-        constexpr int QC = C::CHUNKS / 2;       // 16-byte chunks of Q (and of O) per half row
+        constexpr int QC = C::CHUNKS / 2;       // 16-byte chunks of Q (and of the output) per half row
         {
             // this half of the Q row into shared memory (K-major, swizzled)
             const uint4 *qrow = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.q) + row_elem);
@@ -341,26 +355,16 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(q_full);
         }
-        // swap a value with the row's other thread: exchange k (0, 1, 2 ...)
-        auto swap = [&](float mine, int k, float &theirs) {
-            float *slot = xch + (k & 1) * 2 * BM;
-            slot[hf * BM + r] = mine;
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(pbar);
-            bool w = dev::mbar_wait_bounded(pbar, uint32_t(k) & 1, flags, a.timeout_ns);
-            w = __all_sync(FULL, w);
-            theirs = slot[(hf ^ 1) * BM + r];
-            return w;
-        };
         const int limit = row_ok ? c + t : c;  // last visible key (unused rows: any finite range)
         const int lim_min = c + t0;            // smallest limit of the CTA's rows
         const uint32_t lane_base = uint32_t(qd * 32) << 16;
+        const uint32_t o_t = tmem + lane_base + C::O_COL + uint32_t(hf) * D;  // this half's accumulator
+        const uint32_t pf = p_free + 8 * hf;
         const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
         float m_run = -INFINITY;
-        float2 l2 = make_float2(0.f, 0.f);     // this half's running sum, two partial lanes
+        float2 l2 = make_float2(0.f, 0.f);     // running sum, two partial lanes
         bool ok = true;
-        int j = 0;
-        for (; j < ntiles; ++j) {
+        for (int j = 0; j < ntiles; ++j) {
             ok = !flags[0] && dev::mbar_wait_bounded(s_full + 8 * (j & 1), uint32_t(j >> 1) & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
@@ -380,24 +384,21 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                     for (int e = 0; e < 32; ++e)
                         if (key0 + 32 * h2 + e > limit) sr[h2][e] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // maximum over four independent chains (no long dependency chain)
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
-                    mx = fmax3(mx, __uint_as_float(sr[h2][e]), __uint_as_float(sr[h2][e + 1]));
-            float other;
-            ok = swap(mx, j, other);
-            if (!ok) break;
-            const float m_tile = fmaxf(mx, other) * a.scale_log2;
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(sr[h2][e]), __uint_as_float(sr[h2][e + 1]));
+            const float m_tile = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * a.scale_log2;
             // raise the reference max only when the tile's exceeds it by 2^8
-            // (both threads of the row take the same decision)
             const float m_new = m_tile > m_run + C::RESCALE_LOG2 ? m_tile : m_run;
             const float corr = m_new == m_run ? 1.f : ex2_approx(m_run - m_new);
             m_run = m_new;
             const float negm = m_run == -INFINITY ? 0.f : -m_run;
             const float2 neg2 = make_float2(negm, negm);
-            float2 ps = make_float2(0.f, 0.f);
+            float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[32];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
@@ -406,23 +407,22 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                     const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[h2][e]), __uint_as_float(sr[h2][e + 1])),
                                                 scale2, neg2);
                     const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
-                    ps = __fadd2_rn(ps, make_float2(p0, p1));
+                    ps[(e >> 1) & 3] = __fadd2_rn(ps[(e >> 1) & 3], make_float2(p0, p1));
                     pk[16 * h2 + e / 2] = Ops::pack(p0, p1);
                 }
-            l2 = __ffma2_rn(l2, make_float2(corr, corr), ps);
+            l2 = __ffma2_rn(l2, make_float2(corr, corr), __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3])));
             if (j > 0) {
-                // P.V of the previous tile has read P and written O
-                ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(j - 1) & 1, flags, a.timeout_ns);
+                // this half's P.V of the previous tile has read P and written O_hf
+                ok = !flags[0] && dev::mbar_wait_bounded(pf, uint32_t(j - 1) & 1, flags, a.timeout_ns);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 tc::fence_after();
                 if (__any_sync(FULL, corr != 1.f)) {
                     const float2 c2 = make_float2(corr, corr);
 #pragma unroll
-                    for (int q4 = 0; q4 < D / 64; ++q4) {
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
                         uint32_t o[32];
-                        const uint32_t o_t = tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q4;
-                        tc::tmem_ld32(o_t, o);
+                        tc::tmem_ld32(o_t + 32 * q4, o);
                         tc::tmem_ld_wait();
                         tc::reg_fence(o);
 #pragma unroll
@@ -431,12 +431,13 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                             o[e] = __float_as_uint(v.x);
                             o[e + 1] = __float_as_uint(v.y);
                         }
-                        tc::tmem_st32(o_t, o);
+                        tc::tmem_st32(o_t + 32 * q4, o);
                     }
                     tc::tmem_st_wait();
                 }
             }
-            // this half of the P row into shared memory: the A operand of O += P . V
+            // this half of the P row into shared memory: the A operand of
+            // O_hf += P_hf . V_hf (P block hf, keys [64 hf, 64 hf + 64))
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc)
                 dev::st_shared_v4(C::swz(p_s, r, 8 * hf + cc),
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             dev::fence_proxy_async_smem();
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(p_full);
+            if (lane == 0) dev::mbar_arrive(p_full + 8 * hf);
         }
         if (!ok) {
             if (lane == 0) {
@@ -452,29 +453,50 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                 flags[0] = 1;
             }
         } else if (ntiles > 0) {
-            // ---- epilogue: out = O / l, once the last P.V has completed
-            ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(ntiles - 1) & 1, flags, a.timeout_ns);
+            // ---- epilogue: both halves' last P.V have completed; swap the
+            // halves' (max, sum), then out = (O_0 e_0 + O_1 e_1) / (l_0 e_0 +
+            // l_1 e_1) with e_h = 2^(m_h - max(m_0, m_1)), this thread taking
+            // output columns [hf D/2, (hf + 1) D/2)
+            ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(ntiles - 1) & 1, flags, a.timeout_ns) &&
+                 dev::mbar_wait_bounded(p_free + 8, uint32_t(ntiles - 1) & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
-            float l_other = 0.f;
-            ok = ok && swap(l2.x + l2.y, ntiles, l_other);
+            const float l_me = l2.x + l2.y;
+            if (ok) {
+                xch[hf * BM + r] = m_run;
+                xch[2 * BM + hf * BM + r] = l_me;
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(pbar);
+                ok = __all_sync(FULL, dev::mbar_wait_bounded(pbar, 0, flags, a.timeout_ns));
+            }
             if (ok) {
                 tc::fence_after();
-                const float inv = 1.f / (l2.x + l2.y + l_other);
+                const float m_ot = xch[(hf ^ 1) * BM + r], l_ot = xch[2 * BM + (hf ^ 1) * BM + r];
+                const float m0 = hf ? m_ot : m_run, m1 = hf ? m_run : m_ot;
+                const float l0 = hf ? l_ot : l_me, l1 = hf ? l_me : l_ot;
+                const float M = fmaxf(m0, m1);  // finite: key 0 is visible to every row
+                const float e0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
+                const float e1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+                const float inv = 1.f / (l0 * e0 + l1 * e1);
+                const float f0 = e0 * inv, f1 = e1 * inv;
                 uint4 *orow = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(a.out) + row_elem) + hf * QC;
+                const uint32_t oc = tmem + lane_base + C::O_COL + uint32_t(hf) * (D / 2);  // column hf D/2 of O_0
 #pragma unroll
                 for (int q4 = 0; q4 < D / 64; ++q4) {
-                    uint32_t o[32];
-                    tc::tmem_ld32(tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q4, o);
+                    uint32_t u[32], v[32];
+                    tc::tmem_ld32(oc + 32 * q4, u);
+                    tc::tmem_ld32(oc + D + 32 * q4, v);
                     tc::tmem_ld_wait();
-                    tc::reg_fence(o);
+                    tc::reg_fence(u);
+                    tc::reg_fence(v);
+                    float y[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        y[e] = fmaf(__uint_as_float(u[e]), f0, __uint_as_float(v[e]) * f1);
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
-                        const uint4 v = make_uint4(
-                            Ops::pack(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
-                            Ops::pack(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
-                            Ops::pack(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
-                            Ops::pack(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
-                        if (row_ok) orow[(32 * q4 + e) / 8] = v;
+                        const uint4 w = make_uint4(Ops::pack(y[e], y[e + 1]), Ops::pack(y[e + 2], y[e + 3]),
+                                                   Ops::pack(y[e + 4], y[e + 5]), Ops::pack(y[e + 6], y[e + 7]));
+                        if (row_ok) orow[(32 * q4 + e) / 8] = w;
                     }
                 }
             } else if (lane == 0) {
