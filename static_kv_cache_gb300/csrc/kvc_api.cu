@@ -569,10 +569,13 @@ kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const in
     if (!h->prefill) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(q)) return KVC_ERR_ALIGNMENT;
     const kvc_config &c = h->cfg;
-    const int64_t tokens_per_cta = h->prefill->rows / h->group;  // >= 1: find_prefill checked the group
-    const int64_t q_blocks = (T_new + tokens_per_cta - 1) / tokens_per_cta;
-    const int64_t grid = int64_t(c.batch) * c.n_kv_heads * q_blocks;
-    if (grid > 0x7fffffff) return KVC_ERR_UNSUPPORTED;
+    // work items of rows / g chunk tokens of one (sequence, KV head); the
+    // kernel is persistent, one CTA per SM (or per item when there are fewer)
+    const int64_t tokens_per_item = h->prefill->rows / h->group;  // >= 1: find_prefill checked the group
+    const int64_t q_blocks = (T_new + tokens_per_item - 1) / tokens_per_item;
+    const int64_t items = int64_t(c.batch) * c.n_kv_heads * q_blocks;
+    if (items > 0x7fffffff) return KVC_ERR_UNSUPPORTED;
+    const int64_t grid = items < h->num_sms ? items : h->num_sms;
     const uint64_t slab = layer_slab_bytes(h);
     kvc::PrefillArgs a{};
     a.K = h->k_base + slab * layer;

@@ -161,7 +161,7 @@ struct PrefillArgs {
 
 // One compiled prefill kernel.
 struct PrefillKernelInfo {
-    int rows;    // query rows per CTA: rows / g chunk tokens of the g heads of a KV head
+    int rows;    // query rows per work item: rows / g chunk tokens of the g heads of a KV head
     int smem;    // dynamic shared memory per CTA
     cudaError_t (*set_max_smem)(int bytes);
     cudaError_t (*launch)(const PrefillArgs &a, int grid, int smem, cudaStream_t s);
