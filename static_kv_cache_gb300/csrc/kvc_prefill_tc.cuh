@@ -39,16 +39,16 @@
 // The kernel is persistent: one CTA per SM walks its share of the items
 // (heaviest first, dealt out in a snake order so every CTA gets a similar
 // number of key tiles).  K and V tiles stream through their rings across
-// item boundaries; the next item's Q is copied into the second Q buffer
-// while the current item runs; its first S tiles are computed while the
+// item boundaries; the next item's Q is copied as soon as the current item's
+// last S has read the Q buffer; its first S tiles are computed while the
 // current item's epilogue reads the accumulators, which the next P.V only
 // overwrites once the epilogue has released them.
 //
-// Warps: 0-7 softmax and epilogue (two per TMEM lane quarter), 8 producer
-// (TMA boxes of 128 keys x 64 columns, 128-byte swizzle; a ring of K tiles,
-// released as soon as S has read them, and a ring of V tiles, released after
-// P.V), 9 and 10 MMA issuers (one thread each: S, and P.V), warp 9 also the
-// tensor-memory owner.  Rows past an
+// Warps: 0-7 softmax and epilogue (two per TMEM lane quarter); 8 and 11
+// producers of K and of V (TMA boxes of 128 keys x 64 columns, 128-byte
+// swizzle; a ring of K tiles, released as soon as S has read them, and a ring
+// of V tiles, released after P.V); 9 and 10 MMA issuers (one thread each: S,
+// and P.V), warp 9 also the tensor-memory owner.  Rows past an
 // item's last visible key are never read: a partial last tile is boxed in
 // 32- and 8-row groups, its remaining live rows copied by the producer's
 // lanes, the rest zeroed.  Every wait is bounded; a timeout records
@@ -72,20 +72,20 @@ struct TcPrefillCfg {
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int CHUNKS = ROW_BYTES / 16;  // 16-byte chunks of a row
     static constexpr int BLK = 128 * 128;          // one column block of a 128-row tile
-    static constexpr int Q_BYTES = CB * BLK;       // one Q buffer (two of them)
+    static constexpr int Q_BYTES = CB * BLK;
     static constexpr int P_BYTES = (BN / 64) * BLK;
     static constexpr int KT_BYTES = CB * BLK;      // one K (or V) tile
     // K tiles are released as soon as S = Q.K^T has used them, V tiles only
     // after P.V: separate rings
-    static constexpr int NSK = D == 64 ? 4 : 2;
+    static constexpr int NSK = D == 64 ? 4 : 3;
     static constexpr int NSV = D == 64 ? 4 : 2;
     // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2], p_full[2],
-    // p_free[2], q_full[2], q_empty[2], o_free, mma_done, pair[4], s_free[2]
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 18;
-    static constexpr int BAR_OFF = 2 * Q_BYTES + P_BYTES + (NSK + NSV) * KT_BYTES;
+    // p_free[2], q_full, q_empty, o_free, mma_done, pair[4], s_free[2]
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 16;
+    static constexpr int BAR_OFF = Q_BYTES + P_BYTES + (NSK + NSV) * KT_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * NBAR + 32;  // + TMEM address, abort flag
     static constexpr int NSW = 8;                  // softmax warps: two per TMEM lane quarter
-    static constexpr int THREADS = (NSW + 3) * 32; // + producer, S issuer, P.V issuer
+    static constexpr int THREADS = (NSW + 4) * 32; // + K producer, S issuer, P.V issuer, V producer
     static constexpr uint32_t TMEM_COLS = 512;
     // two S buffers, then one O accumulator per half of the key tile
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256;
@@ -159,16 +159,16 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     constexpr uint32_t IDESC_S = tc::idesc_f16_f32acc(BF16, BM, BN, false, false);
     constexpr uint32_t IDESC_O = tc::idesc_f16_f32acc(BF16, BM, D, false, true);
     // the single warps after the softmax warps
-    constexpr int PRODUCER = C::NSW, ISSUER = C::NSW + 1, PV_ISSUER = C::NSW + 2;
+    constexpr int PRODUCER = C::NSW, ISSUER = C::NSW + 1, PV_ISSUER = C::NSW + 2, V_PRODUCER = C::NSW + 3;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = dev::smem_addr(smem);
-    const uint32_t q_s = sb, p_s = sb + 2 * C::Q_BYTES, k_s = p_s + C::P_BYTES, v_s = k_s + NSK * C::KT_BYTES;
+    const uint32_t q_s = sb, p_s = sb + C::Q_BYTES, k_s = p_s + C::P_BYTES, v_s = k_s + NSK * C::KT_BYTES;
     const uint32_t kfull = sb + C::BAR_OFF, kempty = kfull + 8 * NSK, vfull = kempty + 8 * NSK,
                    vempty = vfull + 8 * NSV;
     const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 16, q_full = p_free + 16,
-                   q_empty = q_full + 16, o_free = q_empty + 16, mma_done = o_free + 8, pair_bar = mma_done + 8,
+                   q_empty = q_full + 8, o_free = q_empty + 8, mma_done = o_free + 8, pair_bar = mma_done + 8,
                    s_free = pair_bar + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + 8 * C::NBAR);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::BAR_OFF + 8 * C::NBAR + 16);
@@ -192,10 +192,10 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             dev::mbar_init(s_full + 8 * x, 1);
             dev::mbar_init(p_full + 8 * x, C::NSW / 2);  // the four softmax warps of a half
             dev::mbar_init(p_free + 8 * x, 1);
-            dev::mbar_init(q_full + 8 * x, C::NSW);      // every softmax warp copied its rows of Q
-            dev::mbar_init(q_empty + 8 * x, 1);          // the item's last S has read its Q
             dev::mbar_init(s_free + 8 * x, C::NSW);      // every softmax warp has loaded its part of S
         }
+        dev::mbar_init(q_full, C::NSW);                  // every softmax warp copied its rows of Q
+        dev::mbar_init(q_empty, 1);                      // the item's last S has read its Q
         dev::mbar_init(o_free, C::NSW);                  // the epilogue has read the accumulators
         dev::mbar_init(mma_done, 2);                     // one commit per issuing thread
         for (int qd = 0; qd < 4; ++qd) dev::mbar_init(pair_bar + 8 * qd, 2);  // the two warps of a lane quarter
@@ -216,16 +216,19 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     dev::grid_dependency_wait();
     dev::allow_dependents();
 
-    int issued_k = 0, issued_v = 0;  // tiles whose copies the producer issued
-    if (warp == PRODUCER) {
-        // ------------------------------------------------------------ producer
-        // K of tile j + 1 goes out before V of tile j: S needs K a whole
-        // softmax earlier than P.V needs V.
-        uint32_t generic_k = 0, generic_v = 0;  // stages whose last fill had generic-proxy stores
+    int issued = 0;  // tiles whose copies this producer issued
+    if (warp == PRODUCER || warp == V_PRODUCER) {
+        // ------------------------------------------------------------ producers
+        // One warp streams the K tiles, one the V tiles, each as far ahead as
+        // its ring allows (S needs K a whole softmax earlier than P.V needs V).
+        const bool is_v = warp == V_PRODUCER;
+        const int ns = is_v ? NSV : NSK;
+        const uint32_t ring = is_v ? v_s : k_s, full0 = is_v ? vfull : kfull, empty0 = is_v ? vempty : kempty;
+        uint32_t generic = 0;  // stages whose last fill had generic-proxy stores
         bool ok = true;
-        PrefillItem it;
-        // one tile of one tensor of the current item into one stage
-        auto load = [&](bool is_v, int j, uint32_t dst, uint32_t full, uint32_t &generic, int s) {
+        PrefillItem it{};
+        // one tile of this producer's tensor of the current item into one stage
+        auto load = [&](int j, uint32_t dst, uint32_t full, int s) {
             const int z = a.seg_base + it.seg;
             const int row0 = j * BN, nr = min(BN, it.kend - row0);
             const CUtensorMap *m128 = is_v ? &a.tm_v128 : &a.tm_k128;
@@ -284,21 +287,12 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             return false;
         };
         for (int k = 0; ok && prefill_item(a, k, TB, it); ++k) {
-            for (int j = 0; ok && it.ntiles > 0 && j <= it.ntiles; ++j) {
-                if (j < it.ntiles) {
-                    const int s = issued_k % NSK;
-                    ok = wait_free(kempty + 8 * s, issued_k, NSK);
-                    if (!ok) break;
-                    load(false, j, k_s + uint32_t(s) * C::KT_BYTES, kfull + 8 * s, generic_k, s);
-                    ++issued_k;
-                }
-                if (j > 0) {
-                    const int s = issued_v % NSV;
-                    ok = wait_free(vempty + 8 * s, issued_v, NSV);
-                    if (!ok) break;
-                    load(true, j - 1, v_s + uint32_t(s) * C::KT_BYTES, vfull + 8 * s, generic_v, s);
-                    ++issued_v;
-                }
+            for (int j = 0; ok && j < it.ntiles; ++j) {
+                const int s = issued % ns;
+                ok = wait_free(empty0 + 8 * s, issued, ns);
+                if (!ok) break;
+                load(j, ring + uint32_t(s) * C::KT_BYTES, full0 + 8 * s, s);
+                ++issued;
             }
         }
     } else if (warp == ISSUER || warp == PV_ISSUER) {
@@ -314,8 +308,8 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                 if (warp == ISSUER) {
                     // S = Q . K_j^T into S buffer gs % 2, once the softmax warps
                     // have loaded tile gs - 2 from that buffer
-                    const uint32_t qt = q_s + uint32_t(nk & 1) * C::Q_BYTES;
-                    ok = dev::mbar_wait_bounded(q_full + 8 * (nk & 1), uint32_t(nk >> 1) & 1, flags, a.timeout_ns);
+                    const uint32_t qt = q_s;
+                    ok = dev::mbar_wait_bounded(q_full, uint32_t(nk) & 1, flags, a.timeout_ns);
                     for (int j = 0; ok && j < it.ntiles; ++j, ++gs) {
                         const int s = gs % NSK;
                         ok = dev::mbar_wait_bounded(kfull + 8 * s, uint32_t(gs / NSK) & 1, flags, a.timeout_ns);
@@ -334,7 +328,7 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                         }
                         tc::commit(s_full + 8 * (gs & 1));
                         tc::commit(kempty + 8 * s);                                   // K stage free
-                        if (j == it.ntiles - 1) tc::commit(q_empty + 8 * (nk & 1));  // the item's Q read
+                        if (j == it.ntiles - 1) tc::commit(q_empty);  // the item's Q read
                     }
                 } else {
                     // O_h += P_h . V_h for the two halves h of every tile
@@ -392,13 +386,13 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         // The end-of-item swap of (max, sum) goes through the quarter's own
         // rows of P block 0 (free then: the item's last P.V has completed,
         // and only this pair of warps writes those rows before the next P.V).
-        float *xch = reinterpret_cast<float *>(smem + 2 * C::Q_BYTES) + qd * 32 * 32;
+        float *xch = reinterpret_cast<float *>(smem + C::Q_BYTES) + qd * 32 * 32;
         const uint32_t lane_base = uint32_t(qd * 32) << 16;
         const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-        // this thread's half of an item's Q row into Q buffer buf
-        auto copy_q = [&](const PrefillItem &x, int buf, bool async) {
+        // this thread's half of an item's Q row into the Q buffer
+        auto copy_q = [&](const PrefillItem &x, bool async) {
             const bool valid = x.ntiles > 0 && i < G && tt < x.ntok;
-            const uint32_t qt = q_s + uint32_t(buf) * C::Q_BYTES;
+            const uint32_t qt = q_s;
             const uint4 *qrow = reinterpret_cast<const uint4 *>(
                 reinterpret_cast<const T *>(a.q) + ((int64_t(x.b) * H + x.kv * G + i) * a.T_new + x.t0 + tt) * D);
 #pragma unroll
@@ -420,15 +414,16 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             have = prefill_item(a, kn++, TB, it);
         }
         if (have) {
-            copy_q(it, 0, false);
+            copy_q(it, false);
             dev::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(q_full);
         }
         while (have) {
-            // the next item with work (its enumeration index kx); its Q goes
-            // into the other buffer once the item before this one has
-            // finished reading that buffer
+            // the next item with work (its enumeration index kx); its Q is
+            // copied into the Q buffer as soon as this item's last S has read
+            // it -- polled between tiles, so the copy hides behind the
+            // item's last tiles
             int kx = -1;
             {
                 bool hn = prefill_item(a, kn, TB, nx);
@@ -436,19 +431,10 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                     if (threadIdx.x == 0 && nx.kv == 0 && nx.qb == 0) dev::record_error(a.err, ERR_DEVICE_INDEX);
                     hn = prefill_item(a, ++kn, TB, nx);
                 }
-                if (hn) {
-                    kx = kn++;
-                    const int buf = (nk + 1) & 1;
-                    if (nk >= 1) {
-                        ok = !flags[0] && dev::mbar_wait_bounded(q_empty + 8 * buf, uint32_t((nk - 1) >> 1) & 1,
-                                                                 flags, a.timeout_ns);
-                        ok = __all_sync(FULL, ok);
-                        if (!ok) break;
-                    }
-                    copy_q(nx, buf, true);
-                }
+                if (hn) kx = kn++;
             }
             const bool have_nx = kx >= 0;
+            bool q_copied = !have_nx;
             const bool row_ok = i < G && tt < it.ntok;
             const int limit = row_ok ? it.c + it.t0 + tt : it.c;  // last visible key (unused rows: any finite range)
             const int lim_min = it.c + it.t0;                     // smallest limit of the item's rows
@@ -457,6 +443,10 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             float m_run = -INFINITY;
             float2 l2 = make_float2(0.f, 0.f);  // running sum, two partial lanes
             for (int j = 0; j < it.ntiles; ++j, ++gt) {
+                if (!q_copied && __all_sync(FULL, dev::mbar_test_wait(q_empty, uint32_t(nk) & 1))) {
+                    copy_q(nx, true);
+                    q_copied = true;
+                }
                 ok = !flags[0] &&
                      dev::mbar_wait_bounded(s_full + 8 * (gt & 1), uint32_t(gt >> 1) & 1, flags, a.timeout_ns);
                 ok = __all_sync(FULL, ok);
@@ -550,11 +540,17 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             }
             if (!ok) break;
             if (have_nx) {
-                // the next item's Q has landed: hand it to the MMA issuer
+                if (!q_copied) {
+                    ok = __all_sync(FULL, !flags[0] && dev::mbar_wait_bounded(q_empty, uint32_t(nk) & 1, flags,
+                                                                               a.timeout_ns));
+                    if (!ok) break;
+                    copy_q(nx, true);
+                }
+                // the next item's Q has landed: hand it to the S issuer
                 cp_async_wait_all();
                 dev::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(q_full + 8 * ((nk + 1) & 1));
+                if (lane == 0) dev::mbar_arrive(q_full);
             }
             // ---- epilogue: both halves' last P.V have completed; swap the
             // halves' (max, sum), then out = (O_0 e_0 + O_1 e_1) / (l_0 e_0 +
@@ -630,13 +626,13 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         tc::fence_after();
         tc::tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (warp == PRODUCER && lane == 0 && flags[0]) {
+    if ((warp == PRODUCER || warp == V_PRODUCER) && lane == 0 && flags[0]) {
         // after an abort, wait (bounded) for the copies that may still land
         const volatile int never = 0;
-        for (int j = issued_k > NSK ? issued_k - NSK : 0; j < issued_k; ++j)
-            dev::mbar_wait_bounded(kfull + 8 * (j % NSK), uint32_t(j / NSK) & 1, &never, a.timeout_ns);
-        for (int j = issued_v > NSV ? issued_v - NSV : 0; j < issued_v; ++j)
-            dev::mbar_wait_bounded(vfull + 8 * (j % NSV), uint32_t(j / NSV) & 1, &never, a.timeout_ns);
+        const int ns = warp == V_PRODUCER ? NSV : NSK;
+        const uint32_t full0 = warp == V_PRODUCER ? vfull : kfull;
+        for (int j = issued > ns ? issued - ns : 0; j < issued; ++j)
+            dev::mbar_wait_bounded(full0 + 8 * (j % ns), uint32_t(j / ns) & 1, &never, a.timeout_ns);
     }
     if (warp < C::NSW) cp_async_wait_all();  // no copy of this thread lands after the CTA exits
 }

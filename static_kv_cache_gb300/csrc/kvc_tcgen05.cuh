@@ -81,6 +81,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] = A * B (+ D when `accumulate`) with A in tensor memory (row m of
+// A in lane m, consecutive K elements along the columns, two 16-bit elements
+// per 32-bit column, the lower-indexed one in the low half) and B in shared
+// memory by descriptor; issued by one thread, asynchronous.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on the mbarrier when every tcgen05.mma this thread issued so
 // far has completed.
 __device__ __forceinline__ void commit(uint32_t mbar) {
