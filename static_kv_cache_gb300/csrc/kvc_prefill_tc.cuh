@@ -22,12 +22,13 @@
 //                        of the key tile (64 keys): tcgen05.ld of that half
 //                        row, causal mask on the tiles that cross the row's
 //                        limit, a running max and sum in fp32 (log2 domain)
-//                        per half; P rounded to the cache type into shared
-//                        memory (K-major, 128-byte swizzle)
-//   O_h += P_h . V_h     tcgen05.mma per half h of the keys, N = d_h, into
-//                        one tensor-memory accumulator per half; B = V_j as
-//                        stored ([key][d]: the N dimension contiguous, an
-//                        MN-major operand).
+//                        per half; P rounded to the cache type and stored
+//                        back into tensor memory over the S columns already
+//                        read (tcgen05.st)
+//   O_h += P_h . V_h     tcgen05.mma per half h of the keys, N = d_h, A = P_h
+//                        from tensor memory, into one tensor-memory
+//                        accumulator per half; B = V_j as stored ([key][d]:
+//                        the N dimension contiguous, an MN-major operand).
 // Each half raises its reference max only when a tile's maximum exceeds it
 // by more than 2^8 (probabilities stay <= 256, no loss in fp32 or in P);
 // only then is its accumulator rescaled in tensor memory (tcgen05.ld,
@@ -73,21 +74,29 @@ struct TcPrefillCfg {
     static constexpr int CHUNKS = ROW_BYTES / 16;  // 16-byte chunks of a row
     static constexpr int BLK = 128 * 128;          // one column block of a 128-row tile
     static constexpr int Q_BYTES = CB * BLK;
-    static constexpr int P_BYTES = (BN / 64) * BLK;
     static constexpr int KT_BYTES = CB * BLK;      // one K (or V) tile
     // K tiles are released as soon as S = Q.K^T has used them, V tiles only
     // after P.V: separate rings
     static constexpr int NSK = D == 64 ? 4 : 3;
     static constexpr int NSV = D == 64 ? 4 : 2;
-    // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2], p_full[2],
-    // p_free[2], q_full, q_empty, o_free, mma_done, pair[4], s_free[2]
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 16;
-    static constexpr int BAR_OFF = Q_BYTES + P_BYTES + (NSK + NSV) * KT_BYTES;
-    static constexpr int SMEM = 1024 + BAR_OFF + 8 * NBAR + 32;  // + TMEM address, abort flag
+    // kfull[NSK], kempty[NSK], vfull[NSV], vempty[NSV], s_full[2],
+    // p_full[2 buffers][2 halves], p_free[2 buffers][2 halves], q_full,
+    // q_empty, o_free, mma_done, pair[4], s_free[2].  Every barrier whose
+    // phases follow the key tiles is kept per S buffer, so that no waiter is
+    // ever two phases away from it (the softmax may run two tiles ahead of
+    // P.V).
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 20;
+    static constexpr int BAR_OFF = Q_BYTES + (NSK + NSV) * KT_BYTES;
+    // the two softmax threads of a row swap their halves' running maxima and
+    // sums here at the end of an item: per lane quarter [half][max, sum][32]
+    static constexpr int XCH_OFF = BAR_OFF + 8 * NBAR + 32;  // after the TMEM address and the abort flag
+    static constexpr int SMEM = 1024 + XCH_OFF + 4 * 2 * 2 * 32 * 4;
     static constexpr int NSW = 8;                  // softmax warps: two per TMEM lane quarter
     static constexpr int THREADS = (NSW + 4) * 32; // + K producer, S issuer, P.V issuer, V producer
     static constexpr uint32_t TMEM_COLS = 512;
-    // two S buffers, then one O accumulator per half of the key tile
+    // two S buffers, then one O accumulator per half of the key tile; the
+    // probabilities P of a tile overwrite the first 32 columns of each half
+    // of its S buffer (64 keys as 16-bit pairs)
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256;
     static_assert(O_COL + 2 * D <= TMEM_COLS, "two S buffers and two O accumulators in tensor memory");
     static constexpr float RESCALE_LOG2 = 8.f;
@@ -164,10 +173,10 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = dev::smem_addr(smem);
-    const uint32_t q_s = sb, p_s = sb + C::Q_BYTES, k_s = p_s + C::P_BYTES, v_s = k_s + NSK * C::KT_BYTES;
+    const uint32_t q_s = sb, k_s = sb + C::Q_BYTES, v_s = k_s + NSK * C::KT_BYTES;
     const uint32_t kfull = sb + C::BAR_OFF, kempty = kfull + 8 * NSK, vfull = kempty + 8 * NSK,
                    vempty = vfull + 8 * NSV;
-    const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 16, q_full = p_free + 16,
+    const uint32_t s_full = vempty + 8 * NSV, p_full = s_full + 16, p_free = p_full + 32, q_full = p_free + 32,
                    q_empty = q_full + 8, o_free = q_empty + 8, mma_done = o_free + 8, pair_bar = mma_done + 8,
                    s_free = pair_bar + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + 8 * C::NBAR);
@@ -190,9 +199,11 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         }
         for (int x = 0; x < 2; ++x) {
             dev::mbar_init(s_full + 8 * x, 1);
-            dev::mbar_init(p_full + 8 * x, C::NSW / 2);  // the four softmax warps of a half
-            dev::mbar_init(p_free + 8 * x, 1);
-            dev::mbar_init(s_free + 8 * x, C::NSW);      // every softmax warp has loaded its part of S
+            dev::mbar_init(s_free + 8 * x, 1);           // the P.V of the buffer's tile has completed
+        }
+        for (int x = 0; x < 4; ++x) {                    // [buffer][half]
+            dev::mbar_init(p_full + 8 * x, C::NSW / 2);  // the half's four softmax warps
+            dev::mbar_init(p_free + 8 * x, 1);           // the half's P.V has completed
         }
         dev::mbar_init(q_full, C::NSW);                  // every softmax warp copied its rows of Q
         dev::mbar_init(q_empty, 1);                      // the item's last S has read its Q
@@ -306,8 +317,8 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             for (int k = 0; ok && prefill_item(a, k, TB, it); ++k) {
                 if (it.ntiles == 0) continue;
                 if (warp == ISSUER) {
-                    // S = Q . K_j^T into S buffer gs % 2, once the softmax warps
-                    // have loaded tile gs - 2 from that buffer
+                    // S = Q . K_j^T into S buffer gs % 2, once the P.V of tile
+                    // gs - 2 has read its probabilities from that buffer
                     const uint32_t qt = q_s;
                     ok = dev::mbar_wait_bounded(q_full, uint32_t(nk) & 1, flags, a.timeout_ns);
                     for (int j = 0; ok && j < it.ntiles; ++j, ++gs) {
@@ -343,19 +354,24 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                             ok = dev::mbar_wait_bounded(o_free, uint32_t(nk - 1) & 1, flags, a.timeout_ns);
                         if (!ok) break;
                         const uint32_t vt = v_s + uint32_t(s) * C::KT_BYTES;
+                        const int buf = gs & 1;
+                        const uint32_t pt = tmem + (buf ? C::S_COL1 : C::S_COL0);  // P in the tile's S buffer
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
-                            ok = dev::mbar_wait_bounded(p_full + 8 * hf, uint32_t(gs) & 1, flags, a.timeout_ns);
+                            ok = dev::mbar_wait_bounded(p_full + 8 * (2 * buf + hf), uint32_t(gs >> 1) & 1, flags,
+                                                        a.timeout_ns);
                             if (!ok) break;
                             tc::fence_after();
                             const uint32_t o_t = tmem + C::O_COL + uint32_t(hf) * D;
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
-                                tc::mma_f16_ss(o_t, tc::smem_desc_sw128(p_s + hf * BLK + ks * 32, 16, 1024),
+                                tc::mma_f16_ts(o_t, pt + 64 * hf + 8 * ks,
                                                tc::smem_desc_sw128(vt + hf * 8192 + ks * 2048, BLK, 1024), IDESC_O,
                                                (j > 0 || ks > 0));
-                            tc::commit(p_free + 8 * hf);  // this half of P free, O_h up to date
+                            tc::commit(p_free + 8 * (2 * buf + hf));  // O_h up to date
                         }
+                        if (!ok) break;
+                        tc::commit(s_free + 8 * buf);  // the S buffer (and its P) free
                         if (!ok) break;
                         tc::commit(vempty + 8 * s);  // V stage free
                     }
@@ -383,10 +399,7 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
         const int H = a.H_kv * G;
         const uint32_t pbar = pair_bar + 8 * qd;
         constexpr int QC = C::CHUNKS / 2;       // 16-byte chunks of Q (and of the output) per half row
-        // The end-of-item swap of (max, sum) goes through the quarter's own
-        // rows of P block 0 (free then: the item's last P.V has completed,
-        // and only this pair of warps writes those rows before the next P.V).
-        float *xch = reinterpret_cast<float *>(smem + C::Q_BYTES) + qd * 32 * 32;
+        float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF) + qd * 4 * 32;  // this lane quarter's slots
         const uint32_t lane_base = uint32_t(qd * 32) << 16;
         const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
         // this thread's half of an item's Q row into the Q buffer
@@ -459,10 +472,6 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                 tc::tmem_ld_wait();
                 tc::reg_fence(sr[0]);
                 tc::reg_fence(sr[1]);
-                // S is in registers: the buffer may take tile gt + 2
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) dev::mbar_arrive(s_free + 8 * (gt & 1));
                 const int key0 = j * BN + 64 * hf;
                 if (key0 + 63 > lim_min) {  // this half tile crosses some row's causal limit
 #pragma unroll
@@ -501,42 +510,38 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
                     }
                 l2 = __ffma2_rn(l2, make_float2(corr, corr),
                                 __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3])));
-                if (j > 0) {
-                    // this half's P.V of the previous tile has read P and written O_hf
-                    ok = !flags[0] && dev::mbar_wait_bounded(pf, uint32_t(gt - 1) & 1, flags, a.timeout_ns);
+                if (j > 0 && __any_sync(FULL, corr != 1.f)) {
+                    // rescale O_hf once this half's P.V of the previous tile has
+                    // completed (its next P.V waits for this tile's P)
+                    ok = !flags[0] && dev::mbar_wait_bounded(pf + 16 * ((gt - 1) & 1), uint32_t((gt - 1) >> 1) & 1,
+                                                             flags, a.timeout_ns);
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
                     tc::fence_after();
-                    if (__any_sync(FULL, corr != 1.f)) {
-                        const float2 c2 = make_float2(corr, corr);
+                    const float2 c2 = make_float2(corr, corr);
 #pragma unroll 1
-                        for (int q4 = 0; q4 < D / 32; ++q4) {
-                            uint32_t o[32];
-                            tc::tmem_ld32(o_t + 32 * q4, o);
-                            tc::tmem_ld_wait();
-                            tc::reg_fence(o);
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(o_t + 32 * q4, o);
+                        tc::tmem_ld_wait();
+                        tc::reg_fence(o);
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const float2 v =
-                                    __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2);
-                                o[e] = __float_as_uint(v.x);
-                                o[e + 1] = __float_as_uint(v.y);
-                            }
-                            tc::tmem_st32(o_t + 32 * q4, o);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v =
+                                __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2);
+                            o[e] = __float_as_uint(v.x);
+                            o[e + 1] = __float_as_uint(v.y);
                         }
-                        tc::tmem_st_wait();
+                        tc::tmem_st32(o_t + 32 * q4, o);
                     }
                 }
-                // this half of the P row into shared memory: the A operand of
-                // O_hf += P_hf . V_hf (P block hf, keys [64 hf, 64 hf + 64))
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    dev::st_shared_v4(C::swz(p_s, r, 8 * hf + cc),
-                                      make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]));
-                dev::fence_proxy_async_smem();
+                // this half of the P row into the tile's S buffer (columns
+                // [64 hf, 64 hf + 32)): the A operand of O_hf += P_hf . V_hf
+                tc::tmem_st32(s_t, pk);
+                tc::tmem_st_wait();
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(p_full + 8 * hf);
+                if (lane == 0) dev::mbar_arrive(p_full + 8 * (2 * (gt & 1) + hf));
             }
             if (!ok) break;
             if (have_nx) {
@@ -556,8 +561,9 @@ __global__ void __launch_bounds__(TcPrefillCfg<T, D>::THREADS, 1)
             // halves' (max, sum), then out = (O_0 e_0 + O_1 e_1) / (l_0 e_0 +
             // l_1 e_1) with e_h = 2^(m_h - max(m_0, m_1)), this thread taking
             // output columns [hf D/2, (hf + 1) D/2)
-            ok = !flags[0] && dev::mbar_wait_bounded(p_free, uint32_t(gt - 1) & 1, flags, a.timeout_ns) &&
-                 dev::mbar_wait_bounded(p_free + 8, uint32_t(gt - 1) & 1, flags, a.timeout_ns);
+            const uint32_t pl = p_free + 16 * ((gt - 1) & 1);  // the last tile's buffer
+            ok = !flags[0] && dev::mbar_wait_bounded(pl, uint32_t((gt - 1) >> 1) & 1, flags, a.timeout_ns) &&
+                 dev::mbar_wait_bounded(pl + 8, uint32_t((gt - 1) >> 1) & 1, flags, a.timeout_ns);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             const float l_me = l2.x + l2.y;
