@@ -26,6 +26,7 @@ struct kvc_cache {
     uint8_t *v_scale;
     const int32_t *block_table;  // paged caches: [B, max_blocks]; else null
     int32_t num_blocks;          // paged: physical blocks per layer pool
+    int32_t kv_pair;             // paged: KV heads read per tile (1, or 2 with the pair kernel)
     uint8_t *ws;
     uint64_t ws_bytes;
     kvc::WorkspaceLayout wl;
@@ -60,12 +61,27 @@ const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
     return kvc::find_decode_kernel(c->dtype, c->d_head, c->n_heads / c->n_kv_heads);
 }
 
+// Paged pools with 2 or 4 query heads per KV head and an even number of KV
+// heads (16-bit, d_h 64 or 128) are read two KV heads per tile: a block
+// stores the heads' rows one after another, so one box brings both.
+bool paged_pair_ok(const kvc_config *c) {
+    const int G = c->n_heads / c->n_kv_heads;
+    return (c->dtype == KVC_BF16 || c->dtype == KVC_FP16) && (c->d_head == 64 || c->d_head == 128) &&
+           (G == 2 || G == 4) && c->n_kv_heads % 2 == 0;
+}
+
 // Kernel for a paged pool: the tensor-core kernel (16-bit, 2 to 8 query heads
-// per KV head); for d_h = 128 the variant whose consumers read the half-row
-// tile layout the paged producer writes, for d_h = 64 the contiguous cache's
+// per KV head, or 16, 32, 64); the pair kernel where paged_pair_ok holds;
+// else for d_h = 128 the variant whose consumers read the half-row tile
+// layout the paged producer writes, for d_h = 64 the contiguous cache's
 // kernel (the layouts coincide).  Null otherwise.
 const kvc::DecodeKernelInfo *find_decode_paged(const kvc_config *c) {
     const int G = c->n_heads / c->n_kv_heads;
+    if (paged_pair_ok(c)) {
+        const bool bf = c->dtype == KVC_BF16;
+        if (c->d_head == 128) return bf ? kvc::decode_kernel_pair_bf16_128(2 * G) : kvc::decode_kernel_pair_f16_128(2 * G);
+        return bf ? kvc::decode_kernel_pair_bf16_64(2 * G) : kvc::decode_kernel_pair_f16_64(2 * G);
+    }
     if (G < 2 || (G > 8 && G != 16 && G != 32 && G != 64)) return nullptr;
     if (c->d_head == 128) {
         if (c->dtype == KVC_BF16) return kvc::decode_kernel_paged_bf16_128(G);
@@ -252,6 +268,31 @@ bool kvc::encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const v
     return true;
 }
 
+bool kvc::encode_pool_pair_maps(int32_t dtype, int D, int H_kv, int64_t blocks_total, const void *k_pool,
+                                const void *v_pool, CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16,
+                                CUtensorMap *v8) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16) || D % 64 != 0 || H_kv < 2) return false;
+    const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t row = cuuint64_t(D) * 2;  // bytes of one row
+    // (64 columns, 16 rows, column blocks, heads, blocks): a column block is
+    // 128 bytes further along the row, so a box lands block after block
+    const cuuint64_t dims[5] = {64, 16, cuuint64_t(D / 64), cuuint64_t(H_kv), cuuint64_t(blocks_total)};
+    const cuuint64_t strides[4] = {row, 128, 16 * row, cuuint64_t(H_kv) * 16 * row};
+    const cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+    const cuuint32_t pair_box[5] = {64, 16, cuuint32_t(D / 64), 2, 1};
+    const cuuint32_t half_box[5] = {64, 8, 1, 1, 1};
+    struct Job { const void *base; const cuuint32_t *box; CUtensorMap *out; };
+    const Job jobs[4] = {{k_pool, pair_box, k16}, {k_pool, half_box, k8}, {v_pool, pair_box, v16}, {v_pool, half_box, v8}};
+    for (const Job &j : jobs) {
+        if (encode(j.out, dt, 5, const_cast<void *>(j.base), dims, strides, j.box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 extern "C" {
 
 int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
@@ -291,7 +332,12 @@ uint64_t kvc_bytes_per_token(const kvc_config *c) {
 
 uint64_t kvc_workspace_bytes(const kvc_config *c) {
     if (!shape_ok(c)) return 0;
-    return kvc::workspace_layout(c->batch, c->n_kv_heads, c->n_heads / c->n_kv_heads, c->d_head).total;
+    const int G = c->n_heads / c->n_kv_heads;
+    const uint64_t one = kvc::workspace_layout(c->batch, c->n_kv_heads, G, c->d_head).total;
+    // a paged pool read two KV heads per tile: half the segments, twice the heads each
+    const uint64_t pair =
+        paged_pair_ok(c) ? kvc::workspace_layout(c->batch, c->n_kv_heads / 2, 2 * G, c->d_head).total : 0;
+    return one > pair ? one : pair;
 }
 
 uint64_t kvc_scale_bytes(const kvc_config *c) {
@@ -351,17 +397,24 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     h->v_scale = static_cast<uint8_t *>(v_scale);
     h->block_table = block_table;
     h->num_blocks = num_blocks;
+    h->kv_pair = block_table && paged_pair_ok(cfg) ? 2 : 1;
     h->ws = static_cast<uint8_t *>(workspace);
     h->ws_bytes = ws_bytes;
-    h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads, h->group, cfg->d_head);
+    h->wl = kvc::workspace_layout(cfg->batch, cfg->n_kv_heads / h->kv_pair, h->group * h->kv_pair, cfg->d_head);
     h->decode = info;
     h->prefill = pinfo;
     h->n_stages = n_stages;
     h->smem_bytes = smem_bytes;
     if (block_table) {
         h->prefill = nullptr;  // chunked prefill reads contiguous caches only
-        if (!kvc::encode_pool_maps(cfg->dtype, cfg->d_head, int64_t(cfg->n_layers) * num_blocks * cfg->n_kv_heads,
-                                   k_base, v_base, &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8)) {
+        const bool maps_ok =
+            h->kv_pair == 2
+                ? kvc::encode_pool_pair_maps(cfg->dtype, cfg->d_head, cfg->n_kv_heads,
+                                             int64_t(cfg->n_layers) * num_blocks, k_base, v_base, &h->tm_k32,
+                                             &h->tm_k8, &h->tm_v32, &h->tm_v8)
+                : kvc::encode_pool_maps(cfg->dtype, cfg->d_head, int64_t(cfg->n_layers) * num_blocks * cfg->n_kv_heads,
+                                        k_base, v_base, &h->tm_k32, &h->tm_k8, &h->tm_v32, &h->tm_v8);
+        if (!maps_ok) {
             delete h;
             return KVC_ERR_CUDA;
         }
@@ -475,8 +528,10 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
                          const void *v_new) {
     const kvc_config &c = h->cfg;
 
-    const int grid = kvc::decode_grid(h->decode, c.batch, c.n_kv_heads, c.d_head, h->elem_bytes, c.max_context,
-                                      max_valid_hint, h->num_sms, h->num_splits);
+    // a pair kernel's segment is (sequence, KV-head pair): half the segments, twice the row bytes
+    const int kp = h->kv_pair;
+    const int grid = kvc::decode_grid(h->decode, c.batch, c.n_kv_heads / kp, c.d_head * kp, h->elem_bytes,
+                                      c.max_context, max_valid_hint, h->num_sms, h->num_splits);
 
     const uint64_t slab = layer_slab_bytes(h);
     kvc::DecodeArgs a{};
@@ -507,6 +562,10 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
     a.num_blocks = h->num_blocks;
     a.gran = h->block_table ? 16 : 1;
     if (h->block_table) a.seg_base = layer * h->num_blocks * c.n_kv_heads;
+    if (kp == 2) {  // segments are head pairs; the pair maps address blocks
+        a.H_kv = c.n_kv_heads / 2;
+        a.seg_base = layer * h->num_blocks;
+    }
     if (h->decode->tensor_maps) {
         a.tm_k32 = h->tm_k32;
         a.tm_k8 = h->tm_k8;

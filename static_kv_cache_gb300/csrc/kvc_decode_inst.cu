@@ -40,11 +40,23 @@ namespace kvc {
 #endif
 
 #if defined(KVC_INST_PAGED)
-// Kernels for paged pools with d_h = 128 (tiles in the half-row layout); the
-// build compiles this variant once per 16-bit type.
-#if KVC_INST_D != 128 || KVC_INST_TYPE == 2
-#error "the paged variant is built for 16-bit caches with d_h = 128"
+// Kernels for paged pools, built once per 16-bit type and d_h of 64 or 128:
+// the kernels that read a block two KV heads at a time (2 or 4 query heads
+// per KV head; G2 counts the query heads of both), and for d_h = 128 the
+// kernels that read one KV head per block in the half-row tile layout.
+#if (KVC_INST_D != 128 && KVC_INST_D != 64) || KVC_INST_TYPE == 2
+#error "the paged variant is built for 16-bit caches with d_h = 64 or 128"
 #endif
+#define KVC_PAIR2(a, d) decode_kernel_pair_##a##_##d
+#define KVC_PAIR(a, d) KVC_PAIR2(a, d)
+const DecodeKernelInfo *KVC_PAIR(KVC_TAG, KVC_INST_D)(int G2) {
+    switch (G2) {
+        case 4: return mma_decode_info<KVC_ELEM, KVC_INST_D, 4, true, true>();
+        case 8: return mma_decode_info<KVC_ELEM, KVC_INST_D, 8, true, true>();
+        default: return nullptr;
+    }
+}
+#if KVC_INST_D == 128
 #define KVC_PCAT2(a) decode_kernel_paged_##a##_128
 #define KVC_PCAT(a) KVC_PCAT2(a)
 const DecodeKernelInfo *KVC_PCAT(KVC_TAG)(int G) {
@@ -62,6 +74,7 @@ const DecodeKernelInfo *KVC_PCAT(KVC_TAG)(int G) {
         default: return nullptr;
     }
 }
+#endif
 #else
 const DecodeKernelInfo *KVC_TABLE_FN(int G) {
     switch (G) {

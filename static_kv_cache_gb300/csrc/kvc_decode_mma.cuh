@@ -349,6 +349,126 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
     return issued;
 }
 
+// The producer for a paged pool read two KV heads at a time.  One block of
+// the pool holds the 16 rows of every KV head of a sequence, head after head
+// ([H_kv, 16, D]), so the rows of KV heads 2j and 2j + 1 are one contiguous
+// run of 2 x 16 rows: one box of each tensor brings both (8 KB at d_h = 128,
+// the size of the contiguous cache's tile boxes), where one head per box
+// takes twice the boxes for the same bytes.  A segment is (sequence, head
+// pair) and a tile is one block: stage rows [16 z, 16 z + 16) hold head
+// 2j + z, laid out [head][64-column block][16 rows][128 bytes] with the
+// 128-byte swizzle (the 5-D box of the pair maps writes exactly that).  A
+// partial last block is boxed in 8 rows per (head, column block) and
+// finished with 16-byte cp.async copies; the new row of a fused step comes
+// from k_new / v_new.  A table entry outside [0, num_blocks) is recorded as a
+// device-index error and its block is not copied.  a.H_kv counts head pairs,
+// a.seg_base is the layer's first block in the pools.
+template <typename C>
+__device__ __forceinline__ uint32_t produce_tiles_paged_pair(const DecodeArgs &a, Walker walk, uint32_t stage0,
+                                                             uint32_t bar0, int ns, volatile int *flags,
+                                                             int lane) {
+    constexpr int BS = 16, CB = C::ROW_BYTES / 128;
+    constexpr int HEAD_BYTES = BS * C::ROW_BYTES;  // one head's rows of a stage tile
+    static_assert(C::TILE_BYTES == 2 * HEAD_BYTES, "a tile is one block of two heads");
+    constexpr unsigned FULL = 0xffffffffu;
+    const int H_all = 2 * a.H_kv;  // KV heads of the pool
+    uint32_t issued = 0, generic_written = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    Piece pc;
+    while (ok && walk.next(a, pc)) {
+        const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
+        const int new_row = a.k_new ? pc.n - 1 : -1;
+        // table entries in windows of 32 (lane l: logical block base + l), the
+        // next window loaded when one comes into use
+        const int first = pc.lo / BS;
+        auto load_window = [&](int base) { return base + lane < a.max_blocks ? __ldg(trow + base + lane) : -1; };
+        int32_t cached = load_window(first);
+        int32_t ahead = load_window(first + 32);
+        int cached_base = first;
+        for (int row0 = pc.lo; row0 < pc.hi; row0 += BS) {
+            const int nr = min(BS, pc.hi - row0);
+            const int blk = row0 / BS;
+            if (blk >= cached_base + 32) {
+                cached_base += 32;
+                cached = ahead;
+                ahead = load_window(cached_base + 32);
+            }
+            const int phys = __shfl_sync(FULL, cached, blk - cached_base);
+            const int nb = (new_row >= row0 && new_row < row0 + nr) ? new_row - row0 : nr;
+            int rows = nr;
+            int boxed = nb == BS ? BS : (nb >= 8 ? 8 : 0);
+            if (phys < 0 || phys >= a.num_blocks) {
+                if (lane == 0) dev::record_error(a.err, ERR_DEVICE_INDEX);
+                rows = boxed = 0;  // not copied: its rows stay stale
+            }
+            if (round > 0) {
+                const bool w =
+                    dev::mbar_wait_bounded(bar0 + 8 * (ns + stage), (round - 1) & 1, flags, a.timeout_ns);
+                if (!__all_sync(FULL, w)) {
+                    if (lane == 0) {
+                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                        flags[0] = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+            }
+            const uint32_t full = bar0 + 8 * stage;
+            const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
+            const uint32_t vdst = kdst + C::TILE_BYTES;
+            if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();  // every issuing lane
+            if (lane == 0) dev::mbar_expect_tx(full, 4u * uint32_t(boxed) * C::ROW_BYTES);
+            __syncwarp();
+            const int wblk = a.seg_base + phys;
+            if (boxed == BS) {
+                // lane 0: K, lane 1: V, both heads in one box each
+                if (lane < 2)
+                    dev::tma_load_5d(lane ? vdst : kdst, lane ? &a.tm_v32 : &a.tm_k32, 0, 0, 0, 2 * pc.kv, wblk,
+                                     full);
+            } else if (boxed == 8 && lane < 4 * CB) {
+                // one 8-row box per (tensor, head, column block)
+                const bool is_v = lane & 1;
+                const int z = (lane >> 1) & 1, cb = lane >> 2;
+                dev::tma_load_5d((is_v ? vdst : kdst) + z * HEAD_BYTES + cb * 2048, is_v ? &a.tm_v8 : &a.tm_k8, 0, 0,
+                                 cb, 2 * pc.kv + z, wblk, full);
+            }
+            const int rem = rows - boxed;
+            if (rem > 0) {
+                // rows no box covers: (tensor, head, row, 16-byte chunk) per lane
+                const int per = rem * C::CHUNKS;
+                for (int i = lane; i < 4 * per; i += 32) {
+                    const bool is_v = i >= 2 * per;
+                    const int j = is_v ? i - 2 * per : i;
+                    const int z = j / per, jj = j - z * per;
+                    const int r = boxed + jj / C::CHUNKS, c16 = jj % C::CHUNKS;
+                    const int kvh = 2 * pc.kv + z;
+                    const uint8_t *src =
+                        row0 + r == new_row
+                            ? (is_v ? a.v_new : a.k_new) + (int64_t(pc.b) * H_all + kvh) * C::ROW_BYTES + c16 * 16
+                            : (is_v ? a.V : a.K) + ((int64_t(phys) * H_all + kvh) * BS + r) * C::ROW_BYTES + c16 * 16;
+                    const uint32_t dst = (is_v ? vdst : kdst) + uint32_t(z * HEAD_BYTES + (c16 >> 3) * 2048 + r * 128) +
+                                         (uint32_t((c16 & 7) ^ (r & 7)) << 4);
+                    dev::cp_async_16(dst, src);
+                }
+                dev::cp_async_arrive(full);
+                generic_written |= 1u << stage;
+            } else {
+                generic_written &= ~(1u << stage);
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(full);
+            ++issued;
+            if (++stage == ns) {
+                stage = 0;
+                ++round;
+            }
+        }
+    }
+    return issued;
+}
+
 // Zero the halves of a 32-bit pair of keys (k, k + 1) that are not live.
 __device__ __forceinline__ uint32_t live_pair(uint32_t r, int k, int nr) {
     return r & ((k < nr ? 0x0000ffffu : 0u) | (k + 1 < nr ? 0xffff0000u : 0u));
@@ -551,7 +671,7 @@ struct FinalCombine {
 // piece and the segment has more than HELP_MIN_OTHERS other splits, the fold
 // is left to the whole CTA: the function returns true with the job in `job`
 // and the CTA's own partial in `st`.
-template <typename T, int D, int G, int NW>
+template <typename T, int D, int G, int NW, int KH = 1>
 __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &plan, Walker walk,
                                              const float *scr_acc, const float *scr_ml, uint32_t scr_full,
                                              uint32_t scr_free, volatile int *flags, int lane,
@@ -569,22 +689,27 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
         const bool final_piece = !peek.next(a, next_pc);
         if (a.k_new && pc.hi == pc.n && lane < 2 * CHUNKS) {
             // fused step: this CTA holds the segment's last row; store the
-            // new K and V rows into the cache (nobody in this launch reads
-            // them back from there)
-            const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
+            // new K and V rows of its KH KV heads into the cache (nobody in
+            // this launch reads them back from there)
             const bool is_v = lane >= CHUNKS;
             const int c16 = is_v ? lane - CHUNKS : lane;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) + seg * ROW_BYTES) + c16);
             uint8_t *cache = const_cast<uint8_t *>(is_v ? a.V : a.K);  // the caller's writable cache
-            int64_t row_off = seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES;
-            if (a.block_table) {  // paged: the row's slot in its physical block
-                const int p = pc.n - 1;
-                const int phys = __ldg(a.block_table + int64_t(pc.b) * a.max_blocks + p / 16);
-                row_off = phys >= 0 && phys < a.num_blocks
-                              ? ((int64_t(phys) * a.H_kv + pc.kv) * 16 + p % 16) * ROW_BYTES
-                              : -1;  // reported by the producer
+#pragma unroll
+            for (int z = 0; z < KH; ++z) {
+                const int kvh = pc.kv * KH + z;  // KV head
+                const int64_t seg = int64_t(pc.b) * a.H_kv * KH + kvh;
+                const uint4 v =
+                    __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) + seg * ROW_BYTES) + c16);
+                int64_t row_off = seg * kv_slab + int64_t(pc.n - 1) * ROW_BYTES;
+                if (a.block_table) {  // paged: the row's slot in its physical block
+                    const int p = pc.n - 1;
+                    const int phys = __ldg(a.block_table + int64_t(pc.b) * a.max_blocks + p / 16);
+                    row_off = phys >= 0 && phys < a.num_blocks
+                                  ? ((int64_t(phys) * a.H_kv * KH + kvh) * 16 + p % 16) * ROW_BYTES
+                                  : -1;  // reported by the producer
+                }
+                if (row_off >= 0) reinterpret_cast<uint4 *>(cache + row_off)[c16] = v;
             }
-            if (row_off >= 0) reinterpret_cast<uint4 *>(cache + row_off)[c16] = v;
         }
         bool ok = !flags[0] && dev::mbar_wait_bounded(scr_full, piece & 1, flags, a.timeout_ns);
         ok = __all_sync(FULL, ok);
@@ -743,15 +868,27 @@ __device__ __forceinline__ void merge_pieces_chunked(const DecodeArgs &a, const 
 
 // PG: the tiles come from a paged pool in the half-row layout (MmaCfg::swz_pg);
 // only the d_h = 128 kernels need it (for d_h = 64 the layouts coincide).
-template <typename T, int D, int G, bool PG = false>
+// PAIR: the tiles come from a paged pool two KV heads at a time
+// (produce_tiles_paged_pair): a segment is (sequence, head pair), G counts
+// the query heads of both KV heads (query head c belongs to KV head
+// c / (G / 2)), a tile is 16 keys of each head, stage rows [16 z, 16 z + 16)
+// hold head z; the products of one head's keys with the other head's
+// queries are masked out of the softmax.
+template <typename T, int D, int G, bool PG = false, bool PAIR = false>
 __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
     using C = MmaCfg<T, D, G>;
     constexpr bool PAGED_OK = PG || D == 64;         // the paged producer's layout is this kernel's
-    constexpr bool PGL = PG && D != 64;              // consumers address the half-row layout
+    constexpr bool PGL = PG && D != 64 && !PAIR;     // consumers address the half-row layout
     using Ops = MmaOps<T>;
     constexpr int NW = C::NW, TILE = C::TILE, KSTEPS = C::KSTEPS;
     constexpr unsigned FULL = 0xffffffffu;
+    static_assert(!PAIR || (G == 4 || G == 8), "head pairs of 2 or 4 query heads per KV head");
+    constexpr int TK = PAIR ? 16 : TILE;  // keys of a segment per tile
+    constexpr int KH = PAIR ? 2 : 1;      // KV heads per segment
+    // tile addressing: the 16-row m-tile and the 64-column block strides
+    constexpr uint32_t MT_STRIDE = PAIR ? 16u * C::ROW_BYTES : 2048u;
+    constexpr uint32_t CB_STRIDE = PAIR ? 2048u : uint32_t(C::BLOCK_BYTES);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -801,7 +938,9 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
         uint32_t issued;
-        if constexpr (PAGED_OK)
+        if constexpr (PAIR)
+            issued = produce_tiles_paged_pair<C>(a, walk, stage0, bar0, ns, flags, lane);
+        else if constexpr (PAGED_OK)
             issued = a.block_table ? produce_tiles_paged<C>(a, walk, stage0, bar0, ns, flags, lane)
                                    : produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         else
@@ -830,7 +969,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     } else if (warp == 1) {
         LaneState<D, G> st;
         FinalCombine job;
-        const bool help = merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
+        const bool help = merge_pieces<T, D, G, NW, KH>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
                                                     lane, st, job);
         if (lane == 0) {
             flags[1] = help;
@@ -914,7 +1053,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             l0 = l1 = 0.f;
         }
 
-        for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE, ++t) {
+        for (int row0 = pc.lo; row0 < pc.hi; row0 += TK, ++t) {
             const int cur_stage = stage;
             const uint32_t cur_round = round;
             if (++stage == ns) {
@@ -922,7 +1061,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                 ++round;
             }
             if (int(t % NSTREAM) != strm) continue;
-            const int nr = min(TILE, pc.hi - row0);
+            const int nr = min(TK, pc.hi - row0);
             // Wait for the previous release of this stage first, then for its
             // data: the reasoning is the one in decode_split_kernel, with a
             // stream's NC warps in place of one warp (tile t - ns needs all of
@@ -956,19 +1095,28 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                     if constexpr (PGL)
                         dev::ldsm_x4(ks_base + mt * 16 * C::ROW_BYTES + koffp[ks >> 2][ks & 3], r);
                     else
-                        dev::ldsm_x4(ks_base + (ks >> 2) * C::BLOCK_BYTES + mt * 2048 + koff[ks & 3], r);
+                        dev::ldsm_x4(ks_base + (ks >> 2) * CB_STRIDE + mt * MT_STRIDE + koff[ks & 3], r);
                     Ops::mma(s[mt], r, qb[ks][0], qb[ks][1]);
                 }
             }
 
             // ---- online softmax per head column (keys along the rows)
-            if (nr < TILE) {
+            if (nr < TK) {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    const int k = 16 * mt + gq;
+                    const int k = (PAIR ? 0 : 16 * mt) + gq;  // key of the rows gq, gq + 8
                     if (k >= nr) s[mt][0] = s[mt][1] = -INFINITY;
                     if (k + 8 >= nr) s[mt][2] = s[mt][3] = -INFINITY;
                 }
+            }
+            if constexpr (PAIR) {
+                // m-tile z holds KV head z's keys: only its own query heads
+                // (columns [z G/2, (z + 1) G/2)) see them; padding columns
+                // past G keep their zero products
+                const int cz = (2 * tq) / (G / 2);  // KV head of this lane's two columns
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+                    if (cz < 2 && cz != mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = -INFINITY;
             }
             float x0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
             float x1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
@@ -1020,9 +1168,9 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                     if constexpr (PGL)
                         dev::ldsm_x4_trans(vs_base + kst * 16 * C::ROW_BYTES + voffp[mt >> 2][mt & 3], r);
                     else
-                        dev::ldsm_x4_trans(vs_base + (mt >> 2) * C::BLOCK_BYTES + kst * 2048 + voff[mt & 3], r);
-                    if (nr < TILE) {  // stale rows past the copied ones
-                        const int k0 = kst * 16 + 2 * tq;
+                        dev::ldsm_x4_trans(vs_base + (mt >> 2) * CB_STRIDE + kst * MT_STRIDE + voff[mt & 3], r);
+                    if (nr < TK) {  // stale rows past the copied ones
+                        const int k0 = (PAIR ? 0 : kst * 16) + 2 * tq;
                         r[0] = live_pair(r[0], k0, nr);
                         r[1] = live_pair(r[1], k0, nr);
                         r[2] = live_pair(r[2], k0 + 8, nr);
@@ -1092,24 +1240,26 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     dev::named_barrier_sync(2, C::THREADS);
 }
 
-template <typename T, int D, int G, bool PG>
+template <typename T, int D, int G, bool PG, bool PAIR>
 cudaError_t set_mma_max_smem(int bytes) {
-    return cudaFuncSetAttribute(decode_mma_kernel<T, D, G, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(decode_mma_kernel<T, D, G, PG, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 bytes);
 }
 
-template <typename T, int D, int G, bool PG>
+template <typename T, int D, int G, bool PG, bool PAIR>
 cudaError_t launch_mma(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
-    return launch_pdl(decode_mma_kernel<T, D, G, PG>, dim3(grid), dim3(MmaCfg<T, D, G>::THREADS), smem, s, a);
+    return launch_pdl(decode_mma_kernel<T, D, G, PG, PAIR>, dim3(grid), dim3(MmaCfg<T, D, G>::THREADS), smem, s, a);
 }
 
 // PG: the kernel for paged pools with d_h = 128 (the half-row tile layout).
-template <typename T, int D, int G, bool PG = false>
+// PAIR: the kernel for paged pools read two KV heads per tile (G counts the
+// query heads of both); a tile is 16 keys of each head.
+template <typename T, int D, int G, bool PG = false, bool PAIR = false>
 const DecodeKernelInfo *mma_decode_info() {
     using C = MmaCfg<T, D, G>;
-    static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
-                                          &set_mma_max_smem<T, D, G, PG>, &launch_mma<T, D, G, PG>, true,
-                                          true};
+    static const DecodeKernelInfo info = {PAIR ? 16 : C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
+                                          &set_mma_max_smem<T, D, G, PG, PAIR>, &launch_mma<T, D, G, PG, PAIR>,
+                                          true, true};
     return &info;
 }
 

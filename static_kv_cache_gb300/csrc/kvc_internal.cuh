@@ -126,6 +126,11 @@ KVC_DECLARE_DECODE_TABLE(q8, 128)
 // paged pools with d_h = 128: the tensor-core kernel in the half-row tile layout
 const DecodeKernelInfo *decode_kernel_paged_bf16_128(int G);
 const DecodeKernelInfo *decode_kernel_paged_f16_128(int G);
+// paged pools read two KV heads per tile (G2 = query heads of both: 4 or 8)
+const DecodeKernelInfo *decode_kernel_pair_bf16_64(int G2);
+const DecodeKernelInfo *decode_kernel_pair_bf16_128(int G2);
+const DecodeKernelInfo *decode_kernel_pair_f16_64(int G2);
+const DecodeKernelInfo *decode_kernel_pair_f16_128(int G2);
 
 // Launch planning shared by every decode entry point (kvc_api.cu).
 // The kernel for a contiguous cache of this element type, head width and
@@ -236,6 +241,12 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, int smem, cudaStrea
 // them (its first 8 rows), 128-byte swizzle.  Host only.
 bool encode_pool_maps(int32_t dtype, int D, int64_t n_blocks_total, const void *k_pool, const void *v_pool,
                       CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8);
+// Tensor maps of paged pools read two KV heads at a time: the pools as 5-D
+// arrays (64 columns, 16 rows, D/64 column blocks, H_kv heads, blocks_total =
+// L * num_blocks blocks), boxes of (64, 16, D/64, 2, 1) -- a block's rows of
+// two heads -- and of (64, 8, 1, 1, 1), 128-byte swizzle.  Host only.
+bool encode_pool_pair_maps(int32_t dtype, int D, int H_kv, int64_t blocks_total, const void *k_pool,
+                           const void *v_pool, CUtensorMap *k16, CUtensorMap *k8, CUtensorMap *v16, CUtensorMap *v8);
 
 }  // namespace kvc
 
@@ -442,6 +453,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+// The same for a 5-D tensor map.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w, int u,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(u), "r"(bar)
         : "memory");
 }
 

@@ -89,6 +89,11 @@ CASES = [
     ("bf16", 64, 8, 1, 1, 2048, [2048]),
     ("bf16", 128, 32, 1, 3, 800, [800, 17, 401]),
     ("fp16", 64, 32, 2, 2, 512, [512, 100]),
+    # 2 or 4 query heads per KV head and an even H_kv: the kernel that reads a
+    # block two KV heads at a time; an odd H_kv keeps one head per tile
+    ("fp16", 64, 8, 4, 3, 512, [512, 31, 257]),
+    ("bf16", 128, 12, 6, 2, 400, [17, 400]),
+    ("bf16", 128, 12, 3, 3, 320, [320, 1, 129]),
 ]
 
 
@@ -132,7 +137,7 @@ def test_blocks_shared_between_sequences():
     assert np.array_equal(Kd[1, :, :48], Kd[0, :, :48])
 
 
-@pytest.mark.parametrize("dtype,D,H,H_kv", [("bf16", 128, 16, 4), ("fp16", 64, 6, 2)])
+@pytest.mark.parametrize("dtype,D,H,H_kv", [("bf16", 128, 16, 4), ("fp16", 64, 6, 2), ("fp16", 64, 8, 4)])
 def test_paged_decode_steps_and_append_through_the_table(dtype, D, H, H_kv):
     B, T, L = 3, 256, 2
     hn = PagedHarness(L, B, H, H_kv, D, T, dtype, num_blocks=B * (T // 16) + 3, seed=3300 + D)
