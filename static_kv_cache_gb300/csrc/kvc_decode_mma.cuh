@@ -380,22 +380,15 @@ __device__ __forceinline__ uint32_t produce_tiles_paged_pair(const DecodeArgs &a
     while (ok && walk.next(a, pc)) {
         const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
         const int new_row = a.k_new ? pc.n - 1 : -1;
-        // table entries in windows of 32 (lane l: logical block base + l), the
-        // next window loaded when one comes into use
         const int first = pc.lo / BS;
-        auto load_window = [&](int base) { return base + lane < a.max_blocks ? __ldg(trow + base + lane) : -1; };
-        int32_t cached = load_window(first);
-        int32_t ahead = load_window(first + 32);
-        int cached_base = first;
+        // the tile's table entry, loaded one tile ahead (a warp-uniform load
+        // from the table's cached lines) so that its latency hides behind
+        // the previous tile's copies
+        int phys_next = __ldg(trow + first);
         for (int row0 = pc.lo; row0 < pc.hi; row0 += BS) {
             const int nr = min(BS, pc.hi - row0);
             const int blk = row0 / BS;
-            if (blk >= cached_base + 32) {
-                cached_base += 32;
-                cached = ahead;
-                ahead = load_window(cached_base + 32);
-            }
-            const int phys = __shfl_sync(FULL, cached, blk - cached_base);
+            const int phys = phys_next;
             const int nb = (new_row >= row0 && new_row < row0 + nr) ? new_row - row0 : nr;
             int rows = nr;
             int boxed = nb == BS ? BS : (nb >= 8 ? 8 : 0);
@@ -415,6 +408,7 @@ __device__ __forceinline__ uint32_t produce_tiles_paged_pair(const DecodeArgs &a
                     break;
                 }
             }
+            phys_next = blk + 1 < a.max_blocks ? __ldg(trow + blk + 1) : -1;
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             const uint32_t vdst = kdst + C::TILE_BYTES;
