@@ -94,7 +94,13 @@ struct MmaCfg {
     static constexpr int CHUNKS = ROW_BYTES / 16;       // 16-byte chunks of a row
     static constexpr int KSTEPS = D / 16;               // k-steps of S^T, m-tiles of O^T
     static constexpr int NW = 8;                        // consumer warps (+ producer + merger)
-    static constexpr int THREADS = (NW + 2) * 32;
+    // Warps: 0 issues the copies, 4 merges, 8 only takes part in the
+    // set-up, the other eight compute.  A warp runs on scheduler (SMSP)
+    // warp mod 4, so the copy-issuing warp shares its scheduler with no
+    // consumer: consumers there delay its issue and, with it, the stream.
+    static constexpr int THREADS = (NW + 3) * 32;
+    static constexpr int ACTIVE_THREADS = (NW + 2) * 32;  // all but the idle warp
+    static constexpr int PRODUCER_WARP = 0, MERGER_WARP = 4, IDLE_WARP = 8;
     static constexpr int NC = (G + 7) / 8;              // 8-head chunks of the group
     static constexpr int GW = G < 8 ? G : 8;            // heads of one consumer warp
     static constexpr int NSTREAM = NW / NC;             // streams of NC warps taking tiles round robin
@@ -922,6 +928,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
     __syncthreads();
 
+    if (warp == C::IDLE_WARP) return;
     const Plan plan = make_plan(a, vl, lane);
     if (plan.r0 >= plan.r1 || plan.b >= a.B) return;  // uniform over the CTA
 
@@ -930,7 +937,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     const int64_t kv_slab = int64_t(a.max_ctx) * C::ROW_BYTES;
 
     // ---------------------------------------------------------------- producer
-    if (warp == 0) {
+    if (warp == C::PRODUCER_WARP) {
         uint32_t issued;
         if constexpr (PAIR)
             issued = produce_tiles_paged_pair<C>(a, walk, stage0, bar0, ns, flags, lane);
@@ -940,7 +947,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
         else
             issued = produce_tiles_tma<C>(a, walk, stage0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
-        dev::named_barrier_sync(2, C::THREADS);  // every warp is done
+        dev::named_barrier_sync(2, C::ACTIVE_THREADS);  // every warp is done
         if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);
         __syncwarp();
         return;
@@ -954,13 +961,13 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
     // ---------------------------------------------------------------- merger
     if constexpr (NC > 1) {
-        if (warp == 1) {
+        if (warp == C::MERGER_WARP) {
             merge_pieces_chunked<T, D, G, NSTREAM>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
             __syncwarp();
-            dev::named_barrier_sync(2, C::THREADS);
+            dev::named_barrier_sync(2, C::ACTIVE_THREADS);
             return;
         }
-    } else if (warp == 1) {
+    } else if (warp == C::MERGER_WARP) {
         LaneState<D, G> st;
         FinalCombine job;
         const bool help = merge_pieces<T, D, G, NW, KH>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
@@ -986,12 +993,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             if (lane == 0) a.tickets[job.seg] = 0;
         }
         __syncwarp();
-        dev::named_barrier_sync(2, C::THREADS);
+        dev::named_barrier_sync(2, C::ACTIVE_THREADS);
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int cw = warp - 2;
+    const int cw = warp - 1 - (warp > C::MERGER_WARP) - (warp > C::IDLE_WARP);  // 0 .. NW - 1
     const int strm = cw / NC;  // this warp's stream: tiles strm, strm + NSTREAM, ...
     const int h0 = (cw % NC) * 8;  // first head of this warp's chunk (0 for groups up to 8)
     const int gq = lane >> 2;  // fragment row group: query head of B / C columns
@@ -1231,7 +1238,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             dev::named_barrier_sync(3, (NW + 1) * 32);
         }
     }
-    dev::named_barrier_sync(2, C::THREADS);
+    dev::named_barrier_sync(2, C::ACTIVE_THREADS);
 }
 
 template <typename T, int D, int G, bool PG, bool PAIR>

@@ -44,13 +44,26 @@ struct Q8Cfg {
     // 32 int8 rows would halve the bytes in flight per tile and cap the
     // stream well below the memory's rate.
     static constexpr int TILE = 64;
-    static constexpr int MT = TILE / 16;                 // 16-key m-tiles of S^T = k-steps of P.V
+    static constexpr int MT = TILE / 16;                 // 16-key m-tiles of a tile
+    // Two consumer warps share each tile, one per half of its keys, each with
+    // its own softmax state: a warp's work per tile (and the time the tile's
+    // stage stays occupied) is halved.  The warps form NW / WPT streams that
+    // take the tiles round robin.
+    static constexpr int WPT = 2;                        // consumer warps per tile
+    static constexpr int KW = TILE / WPT;                // keys of a tile per warp
+    static constexpr int MTW = KW / 16;                  // m-tiles of S^T = k-steps of P.V per warp
     static constexpr int TILE_BYTES = TILE * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K codes, V codes
     static constexpr int CHUNKS = ROW_BYTES / 16;
     static constexpr int CPAIRS = D / 32;                // 32-code blocks of a row
     static constexpr int NW = 8;
-    static constexpr int THREADS = (NW + 2) * 32;
+    // Warps: 0 issues the copies, 4 merges, 8 only takes part in the
+    // set-up, the other eight compute.  A warp runs on scheduler (SMSP)
+    // warp mod 4, so the copy-issuing warp shares its scheduler with no
+    // consumer: consumers there delay its issue and, with it, the stream.
+    static constexpr int THREADS = (NW + 3) * 32;
+    static constexpr int ACTIVE_THREADS = (NW + 2) * 32;  // all but the idle warp
+    static constexpr int PRODUCER_WARP = 0, MERGER_WARP = 4, IDLE_WARP = 8;
     static constexpr int SCR_ACC_FLOATS = NW * G * D;
     static constexpr int SCR_ML_FLOATS = NW * G * 2;
     static constexpr int VL_CACHE = 256;
@@ -182,7 +195,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(const __grid_constant__ DecodeArgs a) {
     using C = Q8Cfg<D, G>;
     using T = __nv_bfloat16;  // q and output
-    constexpr int NW = C::NW, TILE = C::TILE, CPAIRS = C::CPAIRS, MT = C::MT;
+    constexpr int NW = C::NW, TILE = C::TILE, CPAIRS = C::CPAIRS, MT = C::MTW, NSTREAM = NW / C::WPT;
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
         dev::prefetch_tensormap(&a.tm_v32);
         for (int s = 0; s < ns; ++s) {
             dev::mbar_init(bar0 + 8 * s, 1);
-            dev::mbar_init(bar0 + 8 * (ns + s), 1);
+            dev::mbar_init(bar0 + 8 * (ns + s), C::WPT);  // released by both warps of a stream
         }
         dev::mbar_init(scr_full, NW);
         dev::mbar_init(scr_free, 1);
@@ -221,6 +234,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
         for (int b = threadIdx.x; b < a.B; b += C::THREADS) vl_cache[b] = __ldg(a.valid_len + b);
     __syncthreads();
 
+    if (warp == C::IDLE_WARP) return;
     const Plan plan = make_plan(a, vl, lane);
     if (plan.r0 >= plan.r1 || plan.b >= a.B) return;  // uniform over the CTA
     Walker walk;
@@ -232,16 +246,16 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
     constexpr int FOLD_U = fold_batch<D, G>();
 
     // ---------------------------------------------------------------- producer
-    if (warp == 0) {
+    if (warp == C::PRODUCER_WARP) {
         const uint32_t issued = produce_tiles_q8<C>(a, walk, stage0, scale0, bar0, ns, kv_slab, flags, lane);
         __syncwarp();
-        dev::named_barrier_sync(2, C::THREADS);
+        dev::named_barrier_sync(2, C::ACTIVE_THREADS);
         if (lane == 0 && flags[0]) drain_copies(bar0, ns, issued, a.timeout_ns);
         __syncwarp();
         return;
     }
     // ---------------------------------------------------------------- merger
-    if (warp == 1) {
+    if (warp == C::MERGER_WARP) {
         LaneState<D, G> st;
         FinalCombine job;
         const bool help = merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
@@ -266,12 +280,14 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             if (lane == 0) a.tickets[job.seg] = 0;
         }
         __syncwarp();
-        dev::named_barrier_sync(2, C::THREADS);
+        dev::named_barrier_sync(2, C::ACTIVE_THREADS);
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int cw = warp - 2;
+    const int cw = warp - 1 - (warp > C::MERGER_WARP) - (warp > C::IDLE_WARP);  // 0 .. NW - 1
+    const int strm = cw / C::WPT;            // tiles strm, strm + NSTREAM, ...
+    const int kofs = (cw % C::WPT) * C::KW;  // this warp's keys of a tile: [kofs, kofs + KW)
     const int gq = lane >> 2, tq = lane & 3;
     const int H = a.H_kv * G;
     // ldmatrix lanes.  K (non-.trans): matrices (keys 0-7, chunk c) (keys 8-15,
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
                 stage = 0;
                 ++round;
             }
-            if (int(t % NW) != cw) continue;
+            if (int(t % NSTREAM) != strm) continue;
             const int nr = min(TILE, pc.hi - row0);
             const uint32_t full_bar = bar0 + 8 * cur_stage;
             const uint32_t empty_bar = bar0 + 8 * (ns + cur_stage);
@@ -335,6 +351,11 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             const uint32_t ks_base = stage0 + uint32_t(cur_stage) * C::STAGE_BYTES;
             const uint32_t vs_base = ks_base + C::TILE_BYTES;
             const float *ksc = scales + cur_stage * 2 * TILE, *vsc = ksc + TILE;
+            if (kofs >= nr) {  // a tail tile with no live key in this warp's half
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(empty_bar);
+                continue;
+            }
 
             // ---- S^T = K . Q^T on the codes, then the K row scales
             float s[MT][4];
@@ -345,7 +366,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
 #pragma unroll
                 for (int cp = 0; cp < CPAIRS; ++cp) {
                     uint32_t r[4];
-                    dev::ldsm_x4(C::swz(ks_base, mt * 16 + k_row, 2 * cp + k_chunk), r);
+                    dev::ldsm_x4(C::swz(ks_base, kofs + mt * 16 + k_row, 2 * cp + k_chunk), r);
                     uint32_t lo[4], hi[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -358,7 +379,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
                 }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const int k = 16 * mt + gq;
+                const int k = kofs + 16 * mt + gq;
                 const float sa = ksc[k], sb = ksc[k + 8];   // rows past nr hold stale scales
                 s[mt][0] = k < nr ? s[mt][0] * sa : -INFINITY;
                 s[mt][1] = k < nr ? s[mt][1] * sa : -INFINITY;
@@ -410,7 +431,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
             uint32_t pb[MT][2];
 #pragma unroll
             for (int kst = 0; kst < MT; ++kst) {
-                const int k = 16 * kst + gq;
+                const int k = kofs + 16 * kst + gq;
                 const float va = k < nr ? vsc[k] : 0.f, vb = k + 8 < nr ? vsc[k + 8] : 0.f;
                 pb[kst][0] = dev::movmatrix_trans(q8::pack_f16(p[kst][0] * va, p[kst][1] * va));
                 pb[kst][1] = dev::movmatrix_trans(q8::pack_f16(p[kst][2] * vb, p[kst][3] * vb));
@@ -421,7 +442,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
 #pragma unroll
                 for (int cp = 0; cp < CPAIRS; ++cp) {
                     uint32_t r[4];
-                    dev::ldsm_x4_trans(C::swz(vs_base, kst * 16 + v_row, 2 * cp + v_chunk), r);
+                    dev::ldsm_x4_trans(C::swz(vs_base, kofs + kst * 16 + v_row, 2 * cp + v_chunk), r);
                     uint32_t ev[4], od[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -490,7 +511,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
         st.store_slot(fin_acc, fin_ml, cw, lane);
         dev::named_barrier_sync(3, (NW + 1) * 32);
     }
-    dev::named_barrier_sync(2, C::THREADS);
+    dev::named_barrier_sync(2, C::ACTIVE_THREADS);
 }
 
 template <int D, int G>
