@@ -43,13 +43,13 @@
 // split partial (and, for the last CTA of a segment, combines the partials)
 // while the consumers keep the stage ring draining.
 //
-// Groups of more than 8 query heads (G = 8 * NC, NC = 2, 4 or 8) take the
-// heads in chunks of 8, one chunk per consumer warp: the NW consumers form
-// NW / NC streams of NC warps, the streams take the tiles round robin, and
-// the NC warps of a stream all read the same tile, each for its own 8 heads
-// (the tile's empty barrier completes after NC arrivals).  Every K/V byte is
-// still read from HBM once for the whole group; each warp's registers hold
-// the same state as for an 8-head group.  The merge warp combines the
+// Groups of 16, 32 or 64 query heads take the heads in chunks of 16, one
+// chunk per consumer warp, as two N = 8 column tiles that share every K and
+// V fragment the warp loads: the NW consumers form NW / NC streams of
+// NC = G / 16 warps, the streams take the tiles round robin, and the NC
+// warps of a stream all read the same tile, each for its own 16 heads (the
+// tile's empty barrier completes after NC arrivals).  Every K/V byte is still
+// read from HBM once for the whole group.  The merge warp combines the
 // streams' states one 8-head chunk at a time.
 #pragma once
 
@@ -97,12 +97,19 @@ struct MmaCfg {
     // Warps: 0 issues the copies, 4 merges, 8 only takes part in the
     // set-up, the other eight compute.  A warp runs on scheduler (SMSP)
     // warp mod 4, so the copy-issuing warp shares its scheduler with no
-    // consumer: consumers there delay its issue and, with it, the stream.
+    // consumer: consumers there delay its issue and, with it, the stream
+    // (measured so for every group size, the compute-heavy 32-head group
+    // included).
+    static constexpr int PRODUCER_WARP = 0, MERGER_WARP = 4, IDLE_WARP = 8;
     static constexpr int THREADS = (NW + 3) * 32;
     static constexpr int ACTIVE_THREADS = (NW + 2) * 32;  // all but the idle warp
-    static constexpr int PRODUCER_WARP = 0, MERGER_WARP = 4, IDLE_WARP = 8;
-    static constexpr int NC = (G + 7) / 8;              // 8-head chunks of the group
-    static constexpr int GW = G < 8 ? G : 8;            // heads of one consumer warp
+    // Groups of 16 or more heads: each consumer warp takes 16 heads (two
+    // N = 8 column tiles, so every K and V fragment it loads serves both), and
+    // the NC = G / 16 warps of a stream share each tile.
+    static constexpr int NT = G >= 16 ? 2 : 1;          // 8-head column tiles per consumer warp
+    static constexpr int GW = G >= 16 ? 16 : G;         // heads of one consumer warp
+    static constexpr int NC = G >= 16 ? G / 16 : 1;     // warps sharing a tile
+    static constexpr bool CHUNKED = G > 8;              // merged 8 heads at a time
     static constexpr int NSTREAM = NW / NC;             // streams of NC warps taking tiles round robin
     static constexpr int SCR_ACC_FLOATS = NSTREAM * G * D;
     static constexpr int SCR_ML_FLOATS = NSTREAM * G * 2;
@@ -117,8 +124,8 @@ struct MmaCfg {
     static constexpr int HELP_MIN_OTHERS = 4;
 
     static_assert(sizeof(T) == 2, "the tensor-core path takes 16-bit caches");
-    static_assert(G >= 1 && (G <= 8 || (G % 8 == 0 && NW % NC == 0)),
-                  "a group of more than 8 heads is taken in whole 8-head chunks, one per consumer warp");
+    static_assert(G >= 1 && (G <= 8 || (G % 16 == 0 && NW % NC == 0)),
+                  "a group of more than 8 heads is taken in whole 16-head chunks, one per consumer warp");
     static_assert(D % 64 == 0, "head width must be a multiple of 64 (128-byte swizzle blocks)");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the swizzle-atom alignment");
 
@@ -957,10 +964,10 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     float *fin_acc = reinterpret_cast<float *>(smem);
     float *fin_ml = fin_acc + (NW + 1) * G * D;
     constexpr int FOLD_U = fold_batch<D, G>();
-    constexpr int NC = C::NC, NSTREAM = C::NSTREAM;
+    constexpr int NC = C::NC, NSTREAM = C::NSTREAM, NT = C::NT;
 
     // ---------------------------------------------------------------- merger
-    if constexpr (NC > 1) {
+    if constexpr (C::CHUNKED) {
         if (warp == C::MERGER_WARP) {
             merge_pieces_chunked<T, D, G, NSTREAM>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
             __syncwarp();
@@ -1000,7 +1007,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     // ---------------------------------------------------------------- consumers
     const int cw = warp - 1 - (warp > C::MERGER_WARP) - (warp > C::IDLE_WARP);  // 0 .. NW - 1
     const int strm = cw / NC;  // this warp's stream: tiles strm, strm + NSTREAM, ...
-    const int h0 = (cw % NC) * 8;  // first head of this warp's chunk (0 for groups up to 8)
+    const int h0 = (cw % NC) * C::GW;  // first head of this warp's chunk (0 for groups up to 8)
     const int gq = lane >> 2;  // fragment row group: query head of B / C columns
     const int tq = lane & 3;   // quad lane
     const int H = a.H_kv * G;
@@ -1032,26 +1039,32 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             }
     }
 
-    uint32_t qb[KSTEPS][2];
-    float o[KSTEPS][4];
-    float m0, m1, l0, l1;  // heads 2tq and 2tq + 1
+    // Per 8-head column tile nt of this warp: Q^T fragments, O^T, and the
+    // running max / sum of the lane's two heads h0 + 8 nt + 2 tq (+ 1).
+    uint32_t qb[KSTEPS][NT][2];
+    float o[KSTEPS][NT][4];
+    float mx[NT][2], lx[NT][2];
     uint32_t t = 0, piece = 0;
     int stage = 0;
     uint32_t round = 0;
     Piece pc;
     while (walk.next(a, pc)) {
         {
-            const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + h0 + gq) * D;
-            const bool qv = h0 + gq < G;
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                qb[ks][0] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
-                qb[ks][1] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hq = h0 + 8 * nt + gq;
+                const T *qrow = reinterpret_cast<const T *>(a.q) + (int64_t(pc.b) * H + pc.kv * G + hq) * D;
+                const bool qv = hq < G;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    qb[ks][nt][0] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * tq)) : 0u;
+                    qb[ks][nt][1] = qv ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * tq)) : 0u;
+                }
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+                mx[nt][0] = mx[nt][1] = -INFINITY;
+                lx[nt][0] = lx[nt][1] = 0.f;
             }
-#pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
         }
 
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TK, ++t) {
@@ -1084,10 +1097,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
             const uint32_t ks_base = stage0 + uint32_t(cur_stage) * C::STAGE_BYTES;
             const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
-            // ---- S^T = K . Q^T for 32 keys (2 m-tiles of 16)
-            float s[2][4];
+            // ---- S^T = K . Q^T for 32 keys (2 m-tiles of 16), NT column tiles
+            float s[2][NT][4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) s[mt][nt][0] = s[mt][nt][1] = s[mt][nt][2] = s[mt][nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
@@ -1097,7 +1112,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                         dev::ldsm_x4(ks_base + mt * 16 * C::ROW_BYTES + koffp[ks >> 2][ks & 3], r);
                     else
                         dev::ldsm_x4(ks_base + (ks >> 2) * CB_STRIDE + mt * MT_STRIDE + koff[ks & 3], r);
-                    Ops::mma(s[mt], r, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) Ops::mma(s[mt][nt], r, qb[ks][nt][0], qb[ks][nt][1]);
                 }
             }
 
@@ -1106,8 +1122,11 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     const int k = (PAIR ? 0 : 16 * mt) + gq;  // key of the rows gq, gq + 8
-                    if (k >= nr) s[mt][0] = s[mt][1] = -INFINITY;
-                    if (k + 8 >= nr) s[mt][2] = s[mt][3] = -INFINITY;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (k >= nr) s[mt][nt][0] = s[mt][nt][1] = -INFINITY;
+                        if (k + 8 >= nr) s[mt][nt][2] = s[mt][nt][3] = -INFINITY;
+                    }
                 }
             }
             if constexpr (PAIR) {
@@ -1117,48 +1136,60 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                 const int cz = (2 * tq) / (G / 2);  // KV head of this lane's two columns
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt)
-                    if (cz < 2 && cz != mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = -INFINITY;
+                    if (cz < 2 && cz != mt) s[mt][0][0] = s[mt][0][1] = s[mt][0][2] = s[mt][0][3] = -INFINITY;
             }
-            float x0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-            float x1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+            float corr[NT][2];
+            float p[2][NT][4];
+            bool any_corr = false;
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
-                x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, off));
+            for (int nt = 0; nt < NT; ++nt) {
+                float x0 = fmaxf(fmaxf(s[0][nt][0], s[0][nt][2]), fmaxf(s[1][nt][0], s[1][nt][2]));
+                float x1 = fmaxf(fmaxf(s[0][nt][1], s[0][nt][3]), fmaxf(s[1][nt][1], s[1][nt][3]));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
+                    x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, off));
+                }
+                const float mn0 = fmaxf(mx[nt][0], x0 * a.scale_log2), mn1 = fmaxf(mx[nt][1], x1 * a.scale_log2);
+                corr[nt][0] = exp2f(mx[nt][0] - mn0);
+                corr[nt][1] = exp2f(mx[nt][1] - mn1);
+                mx[nt][0] = mn0;
+                mx[nt][1] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    p[mt][nt][0] = exp2f(fmaf(s[mt][nt][0], a.scale_log2, -mn0));
+                    p[mt][nt][1] = exp2f(fmaf(s[mt][nt][1], a.scale_log2, -mn1));
+                    p[mt][nt][2] = exp2f(fmaf(s[mt][nt][2], a.scale_log2, -mn0));
+                    p[mt][nt][3] = exp2f(fmaf(s[mt][nt][3], a.scale_log2, -mn1));
+                }
+                lx[nt][0] = fmaf(lx[nt][0], corr[nt][0], (p[0][nt][0] + p[0][nt][2]) + (p[1][nt][0] + p[1][nt][2]));
+                lx[nt][1] = fmaf(lx[nt][1], corr[nt][1], (p[0][nt][1] + p[0][nt][3]) + (p[1][nt][1] + p[1][nt][3]));
+                any_corr = any_corr || (corr[nt][0] != 1.f) || (corr[nt][1] != 1.f);
             }
-            const float mn0 = fmaxf(m0, x0 * a.scale_log2), mn1 = fmaxf(m1, x1 * a.scale_log2);
-            const float corr0 = exp2f(m0 - mn0), corr1 = exp2f(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            float p[2][4];
+            if (__any_sync(FULL, any_corr)) {
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                p[mt][0] = exp2f(fmaf(s[mt][0], a.scale_log2, -mn0));
-                p[mt][1] = exp2f(fmaf(s[mt][1], a.scale_log2, -mn1));
-                p[mt][2] = exp2f(fmaf(s[mt][2], a.scale_log2, -mn0));
-                p[mt][3] = exp2f(fmaf(s[mt][3], a.scale_log2, -mn1));
-            }
-            l0 = fmaf(l0, corr0, (p[0][0] + p[0][2]) + (p[1][0] + p[1][2]));
-            l1 = fmaf(l1, corr1, (p[0][1] + p[0][3]) + (p[1][1] + p[1][3]));
-            if (__any_sync(FULL, (corr0 != 1.f) || (corr1 != 1.f))) {
-                const float2 cc = make_float2(corr0, corr1);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 cc = make_float2(corr[nt][0], corr[nt][1]);
 #pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    const float2 lo = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), cc);
-                    const float2 hi = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), cc);
-                    o[mt][0] = lo.x;
-                    o[mt][1] = lo.y;
-                    o[mt][2] = hi.x;
-                    o[mt][3] = hi.y;
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        const float2 lo = __fmul2_rn(make_float2(o[mt][nt][0], o[mt][nt][1]), cc);
+                        const float2 hi = __fmul2_rn(make_float2(o[mt][nt][2], o[mt][nt][3]), cc);
+                        o[mt][nt][0] = lo.x;
+                        o[mt][nt][1] = lo.y;
+                        o[mt][nt][2] = hi.x;
+                        o[mt][nt][3] = hi.y;
+                    }
                 }
             }
             // P^T blocks (keys x heads) -> B fragments (keys along k)
-            uint32_t pb[2][2];
+            uint32_t pb[2][NT][2];
 #pragma unroll
-            for (int kst = 0; kst < 2; ++kst) {
-                pb[kst][0] = dev::movmatrix_trans(Ops::pack(p[kst][0], p[kst][1]));
-                pb[kst][1] = dev::movmatrix_trans(Ops::pack(p[kst][2], p[kst][3]));
-            }
+            for (int kst = 0; kst < 2; ++kst)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    pb[kst][nt][0] = dev::movmatrix_trans(Ops::pack(p[kst][nt][0], p[kst][nt][1]));
+                    pb[kst][nt][1] = dev::movmatrix_trans(Ops::pack(p[kst][nt][2], p[kst][nt][3]));
+                }
 
             // ---- O^T += V^T . P^T over the tile's two 16-key steps
 #pragma unroll
@@ -1177,7 +1208,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
                         r[2] = live_pair(r[2], k0 + 8, nr);
                         r[3] = live_pair(r[3], k0 + 8, nr);
                     }
-                    Ops::mma(o[mt], r, pb[kst][0], pb[kst][1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) Ops::mma(o[mt][nt], r, pb[kst][nt][0], pb[kst][nt][1]);
                 }
             }
             __syncwarp();
@@ -1186,35 +1218,40 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
 
         // ---- end of piece: hand this warp's state to the merge warp
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(FULL, l0, off);
-            l1 += __shfl_xor_sync(FULL, l1, off);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                lx[nt][0] += __shfl_xor_sync(FULL, lx[nt][0], off);
+                lx[nt][1] += __shfl_xor_sync(FULL, lx[nt][1], off);
+            }
         bool ok = !flags[0] &&
                   (piece == 0 || dev::mbar_wait_bounded(scr_free, (piece - 1) & 1, flags, a.timeout_ns));
         ok = __all_sync(FULL, ok);
         if (ok) {
-            const int ha = h0 + 2 * tq, hb = h0 + 2 * tq + 1;  // heads of this lane's two columns
 #pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) {
-                const int d = 16 * mt + gq;
-                if (ha < G) {
-                    scr_acc[(strm * G + ha) * D + d] = o[mt][0];
-                    scr_acc[(strm * G + ha) * D + d + 8] = o[mt][2];
+            for (int nt = 0; nt < NT; ++nt) {
+                const int ha = h0 + 8 * nt + 2 * tq, hb = ha + 1;  // heads of this lane's two columns
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int d = 16 * mt + gq;
+                    if (ha < G) {
+                        scr_acc[(strm * G + ha) * D + d] = o[mt][nt][0];
+                        scr_acc[(strm * G + ha) * D + d + 8] = o[mt][nt][2];
+                    }
+                    if (hb < G) {
+                        scr_acc[(strm * G + hb) * D + d] = o[mt][nt][1];
+                        scr_acc[(strm * G + hb) * D + d + 8] = o[mt][nt][3];
+                    }
                 }
-                if (hb < G) {
-                    scr_acc[(strm * G + hb) * D + d] = o[mt][1];
-                    scr_acc[(strm * G + hb) * D + d + 8] = o[mt][3];
-                }
-            }
-            if (gq == 0) {
-                if (ha < G) {
-                    scr_ml[(strm * G + ha) * 2] = m0;
-                    scr_ml[(strm * G + ha) * 2 + 1] = l0;
-                }
-                if (hb < G) {
-                    scr_ml[(strm * G + hb) * 2] = m1;
-                    scr_ml[(strm * G + hb) * 2 + 1] = l1;
+                if (gq == 0) {
+                    if (ha < G) {
+                        scr_ml[(strm * G + ha) * 2] = mx[nt][0];
+                        scr_ml[(strm * G + ha) * 2 + 1] = lx[nt][0];
+                    }
+                    if (hb < G) {
+                        scr_ml[(strm * G + hb) * 2] = mx[nt][1];
+                        scr_ml[(strm * G + hb) * 2 + 1] = lx[nt][1];
+                    }
                 }
             }
         } else if (lane == 0) {
@@ -1227,7 +1264,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::THREADS, 1)
     }
 
     // ---- the final combine, when the merger asks for it (groups up to 8 heads)
-    if constexpr (NC == 1) {
+    if constexpr (!C::CHUNKED) {
         dev::named_barrier_sync(3, (NW + 1) * 32);
         if (flags[1]) {
             const int seg = flags[2], c0 = flags[3], c1 = flags[4], me = flags[5];
