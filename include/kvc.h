@@ -401,9 +401,11 @@ kvc_status kvc_get_error(kvc_cache *h, void *stream);
  * the tensor-core product) -- reading every latent row once for all heads.
  * Size: n_layers * d_latent * max_context * batch * p bytes ("10.3" §4.3).
  *
- * Shapes the kernels take: KVC_BF16 or KVC_FP16, n_heads 8 or 16, d_latent
- * 128, 256 or 512, d_head 16..256 in multiples of 16; others are
- * KVC_ERR_UNSUPPORTED.  Conventions (ownership, streams, device error word)
+ * Shapes the kernels take: KVC_BF16 or KVC_FP16, n_heads 8, 16, or a
+ * multiple of 16 up to 128 (taken 16 heads per CTA, the head groups of one
+ * split side by side in the grid so that they read its latent rows from
+ * memory once between them), d_latent 128, 256 or 512, d_head 16..256 in
+ * multiples of 16; others are KVC_ERR_UNSUPPORTED.  Conventions (ownership, streams, device error word)
  * as for the calls above. */
 typedef struct {
     int32_t n_layers;

@@ -179,8 +179,10 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
 template <class A>
 __device__ __forceinline__ int round_len(const A &a, int n) { return (n + a.gran - 1) / a.gran * a.gran; }
 
+// The CTA's range as split `split` of `nsplit` (by default the CTA's index
+// in the grid and the grid's size).
 template <class A>
-__device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lane) {
+__device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lane, int split, int nsplit) {
     Plan p;
     int64_t total = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -193,9 +195,9 @@ __device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lan
         total += warp_sum_i64(round_len(a, n));
     }
     const int64_t R = total * a.H_kv;
-    p.chunk = (R + gridDim.x - 1) / gridDim.x;
+    p.chunk = (R + nsplit - 1) / nsplit;
     p.chunk = (p.chunk + a.gran - 1) / a.gran * a.gran;  // split points fall on multiples of gran
-    p.r0 = min(R, int64_t(blockIdx.x) * p.chunk);
+    p.r0 = min(R, int64_t(split) * p.chunk);
     p.r1 = min(R, p.r0 + p.chunk);
     p.b = a.B;
     p.pb = 0;
@@ -225,6 +227,11 @@ __device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lan
         base += __shfl_sync(0xffffffffu, incl, 31);
     }
     return p;
+}
+
+template <class A>
+__device__ __forceinline__ Plan make_plan(const A &a, const int32_t *vl, int lane) {
+    return make_plan(a, vl, lane, int(blockIdx.x), int(gridDim.x));
 }
 
 // One maximal run of rows of one segment inside the CTA's range: live rows

@@ -47,9 +47,15 @@ struct MlaArgs {
     int32_t B, H_kv, max_ctx, gran;
     int32_t *err;
     const int32_t *valid_len;  // [B]
-    const void *qt;            // absorbed queries [B, H, d_c], prescaled by log2(e) / sqrt(d_h)
-    float *part_ml;            // [slots, H, 2]: running max (log2 domain) and sum
-    float *part_acc;           // [slots, H, d_c]: unnormalised attended latent
+    const void *qt;            // absorbed queries [B, H_all, d_c], prescaled by log2(e) / sqrt(d_h)
+    float *part_ml;            // [slots, H_all, 2]: running max (log2 domain) and sum
+    float *part_acc;           // [slots, H_all, d_c]: unnormalised attended latent
+    // More heads than one kernel instance takes: the grid is nsplit splits
+    // x groups head groups of the kernel's H heads, CTA c taking split
+    // c / groups for heads [(c % groups) H, (c % groups + 1) H) -- the
+    // groups of one split are neighbours in the grid, so they run at the same
+    // time and read the split's latent rows once from memory between them.
+    int32_t H_all, groups;
     int32_t n_stages;
     int32_t seg_base;          // layer * B: the layer's first row block in the tensor maps
     unsigned long long timeout_ns;
@@ -263,7 +269,8 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
     dev::allow_dependents();
     __syncthreads();
 
-    const Plan plan = make_plan(a, a.valid_len, lane);
+    const int split = int(blockIdx.x) / a.groups, head0 = (int(blockIdx.x) % a.groups) * H;
+    const Plan plan = make_plan(a, a.valid_len, lane, split, int(gridDim.x) / a.groups);
     if (plan.r0 >= plan.r1 || plan.b >= a.B) return;  // uniform over the CTA
     Walker walk;
     walk.init(a, plan, a.valid_len);
@@ -348,7 +355,8 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
         // the sequence's absorbed queries into shared memory
         dev::named_barrier_sync(1, NW * 32);
         {
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.qt) + int64_t(pc.b) * H * DC);
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(static_cast<const T *>(a.qt) + (int64_t(pc.b) * a.H_all + head0) * DC);
             for (int i = ctid; i < H * DC / 8; i += NW * 32) {
                 const int h = i / (DC / 8), c = i - h * (DC / 8);
                 *reinterpret_cast<uint4 *>(q_s + h * C::QS + c * 8) = __ldg(src + i);
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
             }
         }
         dev::named_barrier_sync(1, NW * 32);
-        const int64_t slot = int64_t(blockIdx.x) + pc.b;
+        const int64_t slot = int64_t(split) + pc.b;
         if (cw == 0 && lane < 4) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -540,11 +548,11 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
                     float L = 0.f;
 #pragma unroll
                     for (int w = 0; w < NW; ++w) L += lsum[w * H + head];
-                    a.part_ml[(slot * H + head) * 2] = m_run[nt][e];
-                    a.part_ml[(slot * H + head) * 2 + 1] = L;
+                    a.part_ml[(slot * a.H_all + head0 + head) * 2] = m_run[nt][e];
+                    a.part_ml[(slot * a.H_all + head0 + head) * 2 + 1] = L;
                 }
         }
-        float *acc = a.part_acc + slot * H * DC;
+        float *acc = a.part_acc + (slot * a.H_all + head0) * DC;
 #pragma unroll
         for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll

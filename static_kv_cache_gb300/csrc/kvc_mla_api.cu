@@ -38,8 +38,11 @@ bool mla_shape_ok(const kvc_mla_config *c) {
 
 const kvc::MlaKernelInfo *find_mla(const kvc_mla_config *c) {
     if (c->d_head % 16 != 0 || c->d_head < 16 || c->d_head > 256) return nullptr;
-    if (c->dtype == KVC_BF16) return kvc::mla_kernel_bf16(c->d_latent, c->n_heads);
-    if (c->dtype == KVC_FP16) return kvc::mla_kernel_f16(c->d_latent, c->n_heads);
+    // 8 or 16 heads: one kernel instance; 32 to 128 heads (a multiple of 16):
+    // the 16-head kernel over head groups
+    const int Hk = c->n_heads <= 16 ? c->n_heads : (c->n_heads % 16 == 0 && c->n_heads <= 128 ? 16 : 0);
+    if (c->dtype == KVC_BF16) return kvc::mla_kernel_bf16(c->d_latent, Hk);
+    if (c->dtype == KVC_FP16) return kvc::mla_kernel_f16(c->d_latent, Hk);
     return nullptr;
 }
 
@@ -118,15 +121,19 @@ kvc_status mla_launch(kvc_mla_cache *h, int32_t layer, const void *q, const void
 
     // 2. attention over the latents: the same even split of the flattened
     // rows as the GQA decode, at most one CTA per SM
+    // Head groups of one split run side by side: nsplit splits x groups CTAs.
+    const int groups = c.n_heads > 16 ? c.n_heads / 16 : 1;
     int64_t grid = h->num_splits;
     if (grid == 0) {
         const int64_t upper = int64_t(c.batch) * (hint > 0 ? hint : c.max_context);
         grid = (upper + 4 * 64 - 1) / (4 * 64);
-        if (grid > h->num_sms) grid = h->num_sms;
+        if (grid > h->num_sms / groups) grid = h->num_sms / groups;
     }
     if (grid > kvc::MLA_MAX_CTAS) grid = kvc::MLA_MAX_CTAS;
     if (grid < 1) grid = 1;
     kvc::MlaArgs a;
+    a.H_all = c.n_heads;
+    a.groups = groups;
     a.B = c.batch;
     a.H_kv = 1;
     a.max_ctx = c.max_context;
@@ -141,7 +148,7 @@ kvc_status mla_launch(kvc_mla_cache *h, int32_t layer, const void *q, const void
     a.timeout_ns = kvc::WAIT_TIMEOUT_NS;
     a.tm64 = h->tm64;
     a.tm16 = h->tm16;
-    if (h->info->launch(a, int(grid), h->smem_bytes, s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (h->info->launch(a, int(grid * groups), h->smem_bytes, s) != cudaSuccess) return KVC_ERR_CUDA;
 
     // 3. fold the splits, apply W_UV
     kvc::MlaCombineArgs cb;

@@ -95,6 +95,10 @@ WORKLOADS = {
     # against 16 heads x 128), B=64, ragged live lengths U{1024..8192}.
     "mla_dsv2": Workload("mla_dsv2", 32, 64, 16, 1, 128, 8192, "bf16", steps=1,
                          ragged=(1024, 8192), seed=1030, d_latent=512),
+    # The same latent cache read by 128 query heads (DeepSeek-V2's full head
+    # count): every latent row feeds eight 16-head groups.
+    "mla_dsv2_128h": Workload("mla_dsv2_128h", 32, 64, 128, 1, 128, 8192, "bf16", steps=1,
+                              ragged=(1024, 8192), seed=1031, d_latent=512),
     "llama2_70b_b1": Workload("llama2_70b_b1", 1, 1, 64, 64, 128, 32768, "bf16",
                               steps=1, prefill=32767, seed=1004),
     "llama2_70b_b4": Workload("llama2_70b_b4", 1, 4, 64, 64, 128, 32768, "bf16",

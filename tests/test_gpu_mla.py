@@ -99,6 +99,9 @@ class MlaHarness:
 SHAPES = [  # dtype, H, d_h, d_c
     ("bf16", 16, 128, 512), ("fp16", 16, 128, 512), ("bf16", 8, 64, 512),
     ("bf16", 16, 64, 256), ("fp16", 8, 128, 256), ("bf16", 16, 128, 128), ("bf16", 8, 32, 128),
+    # more than 16 heads: the 16-head kernel over head groups ("10.3" §4.3:
+    # every head attends over the same latent rows)
+    ("bf16", 32, 128, 512), ("fp16", 48, 64, 256), ("bf16", 128, 128, 512),
 ]
 
 
@@ -248,7 +251,8 @@ def test_mla_host_errors():
         cfg = kvc.make_mla_config(*shape)
         return kvc.kvc_mla_alloc(cfg, buf, ws, ws.numel())[0]
     assert alloc(1, 2, 16, 128, 96, 64, "bf16") == kvc.KVC_ERR_UNSUPPORTED     # d_c not compiled
-    assert alloc(1, 2, 32, 128, 512, 64, "bf16") == kvc.KVC_ERR_UNSUPPORTED    # H not compiled
+    assert alloc(1, 2, 24, 128, 512, 64, "bf16") == kvc.KVC_ERR_UNSUPPORTED    # H not a multiple of 16
+    assert alloc(1, 2, 144, 128, 512, 64, "bf16") == kvc.KVC_ERR_UNSUPPORTED   # H above 128
     assert alloc(1, 2, 16, 128, 512, 64, "fp32") == kvc.KVC_ERR_UNSUPPORTED
     assert alloc(1, 2, 16, 0, 512, 64, "bf16") == kvc.KVC_ERR_INVALID
     cfg = kvc.make_mla_config(1, 2, 16, 128, 512, 64, "bf16")
