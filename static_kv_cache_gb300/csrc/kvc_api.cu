@@ -199,8 +199,8 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
     const cuuint64_t strides[2] = {cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
     const cuuint32_t elem[4] = {1, 1, 1, 1};
     struct Job { const void *base; cuuint32_t rows; CUtensorMap *out; };
-    // the larger box covers a whole decode tile (int8: 64 rows; 16-bit: 32)
-    const cuuint32_t r32 = q8 ? 64 : 32;
+    // the larger box covers a whole decode tile (int8: 128 rows; 16-bit: 32)
+    const cuuint32_t r32 = q8 ? 128 : 32;
     if (tile_box) {
         // (64 columns, rows, column blocks, segments); a block is 128 bytes
         // further along the row, so the box lands block after block

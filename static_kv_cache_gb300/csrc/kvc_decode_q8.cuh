@@ -5,7 +5,7 @@
 // x_hat = code * scale; q and the output are bf16.
 //
 // Same decomposition, stage ring, merge warp and split combine as
-// decode_mma_kernel; the tiles hold int8 codes (64 rows of d_h bytes, TMA
+// decode_mma_kernel; the tiles hold int8 codes (128 rows of d_h bytes, TMA
 // boxes with the 128-byte swizzle) and the row scales arrive by 4-byte
 // cp.async beside them.  The per-row scale factors out of both products
 // exactly:
@@ -39,11 +39,12 @@ namespace kvc {
 template <int D, int G>
 struct Q8Cfg {
     static constexpr int ROW_BYTES = D;                 // one int8 code per element
-    // 64 keys per tile: a stage (K and V codes) is 16 KB.  The stage ring
-    // moves a bounded number of tiles per microsecond, so tiles as small as
-    // 32 int8 rows would halve the bytes in flight per tile and cap the
-    // stream well below the memory's rate.
-    static constexpr int TILE = 64;
+    // 128 keys per tile: a stage (K and V codes) is 32 KB, one 16 KB box
+    // per tensor.  The copy issue costs about the same per box whatever its
+    // size, so the largest tiles that leave enough stages (six here, for
+    // four streams) carry the most bytes per box (64-row tiles: 41.9 us per
+    // layer call, 128-row tiles: 40.3 us).
+    static constexpr int TILE = 128;
     static constexpr int MT = TILE / 16;                 // 16-key m-tiles of a tile
     // Two consumer warps share each tile, one per half of its keys, each with
     // its own softmax state: a warp's work per tile (and the time the tile's
@@ -105,7 +106,7 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 }  // namespace q8
 
-// Producer: codes through the tensor maps (one box of 128 codes x 64 rows
+// Producer: codes through the tensor maps (one box of 128 codes x 128 rows
 // for a whole tile, boxes of x 8 rows in a tail tile), the tail's last rows
 // and every row scale by cp.async.
 template <typename C>
@@ -527,7 +528,8 @@ cudaError_t launch_q8(const DecodeArgs &a, int grid, int smem, cudaStream_t s) {
 template <int D, int G>
 const DecodeKernelInfo *q8_decode_info() {
     using C = Q8Cfg<D, G>;
-    static const DecodeKernelInfo info = {C::TILE, C::NW, C::STAGE_BYTES + 16 + C::SCALE_BYTES, C::FIXED_SMEM,
+    // one stage per stream in use, one more being filled
+    static const DecodeKernelInfo info = {C::TILE, C::NW / C::WPT, C::STAGE_BYTES + 16 + C::SCALE_BYTES, C::FIXED_SMEM,
                                           &set_q8_max_smem<D, G>, &launch_q8<D, G>, true};
     return &info;
 }
