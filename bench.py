@@ -41,6 +41,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_mma.cuh",
+                  "static_kv_cache_gb300/csrc/kvc_decode_tc.cuh",
                   "static_kv_cache_gb300/csrc/kvc_decode_q8.cuh",
                   "static_kv_cache_gb300/csrc/kvc_mla.cuh",
                   "static_kv_cache_gb300/csrc/kvc_internal.cuh",
@@ -49,13 +50,16 @@ KERNEL_SOURCES = ("static_kv_cache_gb300/csrc/kvc_decode.cuh",
 
 
 def decode_kernel_name(w: synth.Workload) -> str:
-    """The decode kernel the library picks for a workload: the tensor-core
-    kernel for 16-bit caches with head groups of 2 to 8, 16, 32 or 64 and d_h of 64 or 128,
-    the CUDA-core kernel otherwise."""
+    """The decode kernel the library picks for a workload: the tcgen05 kernel
+    for contiguous 16-bit caches with 16- or 32-head groups at d_h 128, the
+    mma.sync tensor-core kernel for 16-bit caches with head groups of 2 to 8,
+    16, 32 or 64 and d_h of 64 or 128, the CUDA-core kernel otherwise."""
     if w.d_latent:
         return "mla_decode_kernel"
     if w.dtype == "int8":
         return "decode_q8_kernel"
+    if w.dtype in ("bf16", "fp16") and w.group in (16, 32) and w.d_head == 128 and not w.paged:
+        return "decode_tc_kernel"
     if w.dtype in ("bf16", "fp16") and (2 <= w.group <= 8 or w.group in (16, 32, 64)) and w.d_head in (64, 128):
         return "decode_mma_kernel"
     return "decode_split_kernel"

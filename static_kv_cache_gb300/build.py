@@ -48,6 +48,8 @@ def _units():
         for d in (64, 128):
             units.append((inst, os.path.join(BUILD, f"kvc_decode_paged_{tag}_{d}.o"),
                           [f"-DKVC_INST_TYPE={code}", f"-DKVC_INST_D={d}", "-DKVC_INST_PAGED"]))
+        units.append((inst, os.path.join(BUILD, f"kvc_decode_tc_{tag}_128.o"),
+                      [f"-DKVC_INST_TYPE={code}", "-DKVC_INST_D=128", "-DKVC_INST_TC"]))
     units.append((os.path.join(CSRC, "kvc_decode_q8_inst.cu"), os.path.join(BUILD, "kvc_decode_q8_128.o"), []))
     pre = os.path.join(CSRC, "kvc_prefill_inst.cu")
     for code, tag in ((0, "bf16"), (1, "f16")):

@@ -57,8 +57,16 @@ bool shape_ok(const kvc_config *c) {
            elem_bytes_of(c->dtype) > 0;
 }
 
+// Kernel for a contiguous cache bound to a handle: 16- and 32-head groups of
+// 16-bit caches at d_h = 128 take the tcgen05 kernel, which reads its tiles
+// through the handle's 128-row tensor maps; the rest the kernel table.
 const kvc::DecodeKernelInfo *find_decode(const kvc_config *c) {
-    return kvc::find_decode_kernel(c->dtype, c->d_head, c->n_heads / c->n_kv_heads);
+    const int G = c->n_heads / c->n_kv_heads;
+    if (c->d_head == 128 && (G == 16 || G == 32)) {
+        if (c->dtype == KVC_BF16) return kvc::decode_kernel_tc_bf16_128(G);
+        if (c->dtype == KVC_FP16) return kvc::decode_kernel_tc_f16_128(G);
+    }
+    return kvc::find_decode_kernel(c->dtype, c->d_head, G);
 }
 
 // Paged pools with 2 or 4 query heads per KV head and an even number of KV
@@ -356,6 +364,10 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return KVC_ERR_ALIGNMENT;
     const kvc::DecodeKernelInfo *info = block_table ? find_decode_paged(cfg) : find_decode(cfg);
     if (!info) return KVC_ERR_UNSUPPORTED;
+    // the 128- and 32-row maps are encoded with the chunked prefill's
+    const kvc::PrefillKernelInfo *pinfo = block_table ? nullptr : find_prefill(cfg);
+    if (info->row_box_maps && !pinfo) info = kvc::find_decode_kernel(cfg->dtype, cfg->d_head, cfg->n_heads / cfg->n_kv_heads);
+    if (!info) return KVC_ERR_UNSUPPORTED;
     if (!aligned16(k_base) || !aligned16(v_base) || (workspace && !aligned16(workspace)))
         return KVC_ERR_ALIGNMENT;
     const uint64_t need = kvc_workspace_bytes(cfg);
@@ -374,7 +386,6 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
     if (n_stages == 0) return KVC_ERR_UNSUPPORTED;
     const int smem_bytes = info->fixed_smem + n_stages * info->stage_bytes;
     if (info->set_max_smem(smem_bytes) != cudaSuccess) return KVC_ERR_CUDA;
-    const kvc::PrefillKernelInfo *pinfo = find_prefill(cfg);
     if (pinfo && pinfo->set_max_smem(pinfo->smem) != cudaSuccess) return KVC_ERR_CUDA;
 
     // Zero the workspace: error word and per-segment counters start at 0.
@@ -571,6 +582,10 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
         a.tm_k8 = h->tm_k8;
         a.tm_v32 = h->tm_v32;
         a.tm_v8 = h->tm_v8;
+        a.tm_k128 = h->pf_k128;  // encoded with the chunked prefill's maps
+        a.tm_v128 = h->pf_v128;
+        a.tm_kr32 = h->pf_k32;
+        a.tm_vr32 = h->pf_v32;
     }
     const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;

@@ -2,6 +2,9 @@
 // width), selected at compile time by KVC_INST_TYPE (0 bf16, 1 fp16, 2 fp32)
 // and KVC_INST_D.  The build compiles this file once per pair, in parallel.
 #include "kvc_decode_mma.cuh"
+#if defined(KVC_INST_TC)
+#include "kvc_decode_tc.cuh"
+#endif
 
 #ifndef KVC_INST_TYPE
 #error "KVC_INST_TYPE must be defined"
@@ -39,7 +42,23 @@ namespace kvc {
 #define KVC_LARGE_GROUP(G) nullptr
 #endif
 
-#if defined(KVC_INST_PAGED)
+#if defined(KVC_INST_TC)
+// The tcgen05 kernel of 16- and 32-head groups at d_h = 128 (contiguous
+// caches bound to a handle); the build compiles this variant once per 16-bit
+// type.
+#if KVC_INST_D != 128 || KVC_INST_TYPE == 2
+#error "the tcgen05 decode variant is built for 16-bit caches with d_h = 128"
+#endif
+#define KVC_TCAT2(a) decode_kernel_tc_##a##_128
+#define KVC_TCAT(a) KVC_TCAT2(a)
+const DecodeKernelInfo *KVC_TCAT(KVC_TAG)(int G) {
+    switch (G) {
+        case 16: return tc_decode_info<KVC_ELEM, 16>();
+        case 32: return tc_decode_info<KVC_ELEM, 32>();
+        default: return nullptr;
+    }
+}
+#elif defined(KVC_INST_PAGED)
 // Kernels for paged pools, built once per 16-bit type and d_h of 64 or 128:
 // the kernels that read a block two KV heads at a time (2 or 4 query heads
 // per KV head; G2 counts the query heads of both), and for d_h = 128 the

@@ -91,6 +91,10 @@ struct DecodeArgs {
     // x 8 rows with the 128-byte swizzle.  seg_base = layer * B * H_kv.
     int32_t seg_base;
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // the type carries its own alignment
+    // The tcgen05 kernel of large head groups: boxes of 64 columns x 128 and
+    // x 32 rows over the same caches (one column block per box); it takes
+    // its 8-row boxes from tm_k8 / tm_v8.
+    CUtensorMap tm_k128, tm_v128, tm_kr32, tm_vr32;
 };
 
 // One compiled decode kernel and what the host needs to launch it.
@@ -103,6 +107,7 @@ struct DecodeKernelInfo {
     cudaError_t (*launch)(const DecodeArgs &a, int grid, int smem, cudaStream_t s);
     bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
     bool tile_box;       // its full-tile map is the 4-D one of encode_cache_maps
+    bool row_box_maps;   // also reads through the 128- and 32-row maps (tm_k128 ...)
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -126,6 +131,10 @@ KVC_DECLARE_DECODE_TABLE(q8, 128)
 // paged pools with d_h = 128: the tensor-core kernel in the half-row tile layout
 const DecodeKernelInfo *decode_kernel_paged_bf16_128(int G);
 const DecodeKernelInfo *decode_kernel_paged_f16_128(int G);
+// contiguous caches with 16 or 32 query heads per KV head at d_h = 128: the
+// tcgen05 kernel (keys on M = 128, the group's heads on N)
+const DecodeKernelInfo *decode_kernel_tc_bf16_128(int G);
+const DecodeKernelInfo *decode_kernel_tc_f16_128(int G);
 // paged pools read two KV heads per tile (G2 = query heads of both: 4 or 8)
 const DecodeKernelInfo *decode_kernel_pair_bf16_64(int G2);
 const DecodeKernelInfo *decode_kernel_pair_bf16_128(int G2);
