@@ -25,17 +25,18 @@
 // it by more than 2^8 (P stays <= 256); O^T and the partial sums are then
 // rescaled, after the previous P.V has completed.
 //
-// The split of the live rows over the CTAs, the pieces, the merge warp and the
-// ticket-first split combine are those of decode_mma_kernel (one consumer
-// stream); a piece's state -- O^T, each head's max and sum -- is handed to the
-// merge warp through shared memory.
+// The split of the live rows over the CTAs, the pieces and the ticket-first
+// split combine are those of decode_mma_kernel; the softmax warps run the
+// combine themselves at the end of a piece, on O^T read straight from tensor
+// memory, so no shared-memory copy of the state is needed and the K and V
+// rings get that space.
 //
 // Warps: 0 and 1 copy the K and V tiles (TMA boxes of 64 columns x 128, 32 or
 // 8 rows with the 128-byte swizzle; rows past a box-aligned range and the
 // step's new row by 16-byte loads; rows past the piece's end zeroed); 2 issues
 // S (and owns tensor memory), 3 issues P.V (one thread each); 4-11 softmax
-// and the piece epilogue, two per TMEM lane quarter (one per half of the
-// heads); 12 merges.  Every wait is bounded; a timeout records
+// and the piece epilogue (split combine included), two per TMEM lane quarter
+// (one per half of the heads).  Every wait is bounded; a timeout records
 // KVC_ERR_TIMEOUT, every role leaves its loop, the issuers wait for their MMAs
 // and tensor memory is freed before the CTA exits.
 #pragma once
@@ -57,17 +58,17 @@ struct TcDecodeCfg {
     static constexpr int BLK = TK * 128;           // one column block of a tile
     static constexpr int KT_BYTES = CB * BLK;      // a K (or V) tile
     // K tiles are released after S, V tiles only after P.V: the deeper V ring
-    static constexpr int NSK = 2, NSV = 3;
+    static constexpr int NSK = 2, NSV = 4;
     static constexpr int QB = G * 128;             // one 64-column block of Q^T (G rows)
     static constexpr int Q_BYTES = CB * QB;
     static constexpr int P_BYTES = (TK / 64) * G * 128;  // P^T of one tile: two 64-key blocks of G rows
     static constexpr int K_OFF = 0, V_OFF = NSK * KT_BYTES, Q_OFF = V_OFF + NSV * KT_BYTES,
-                         P_OFF = Q_OFF + Q_BYTES, SCR_OFF = P_OFF + 2 * P_BYTES;
-    static constexpr int SCR_BYTES = 4 * (G * D + G * 2);    // the piece's O and (max, sum) for the merger
-    static constexpr int RED_OFF = SCR_OFF + SCR_BYTES;      // [2][2][4][32] tile maxima, [2][4][32] sums
-    static constexpr int RED_BYTES = 4 * (2 * 2 * 4 * 32 + 2 * 4 * 32);
+                         P_OFF = Q_OFF + Q_BYTES, RED_OFF = P_OFF + 2 * P_BYTES;
+    // the softmax warps' exchange slots, [2 phases][2 halves][4 quarters][32]:
+    // tile maxima, or at a piece's end the partial sums
+    static constexpr int RED_BYTES = 4 * (2 * 2 * 4 * 32);
     // kfull[NSK] kempty[NSK] vfull[NSV] vempty[NSV] s_full[2] s_free[2] p_full[2]
-    // p_free[2] q_full q_empty o_free scr_full scr_free mx mma_done
+    // p_free[2] q_full q_empty o_free mx st_full st_free mma_done
     static constexpr int NBAR = 2 * NSK + 2 * NSV + 15;
     static constexpr int BAR_OFF = RED_OFF + RED_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * NBAR + 32;  // + the TMEM address and the flags
@@ -189,6 +190,109 @@ __device__ __forceinline__ uint16_t bits16<__half>(float x) {
 
 }  // namespace tcd
 
+// The merge warp of decode_tc_kernel: for each split piece of the CTA, once
+// the softmax warps have written its state to its partial slot (CTA +
+// segment), the split combine of merge_pieces_chunked on that global state:
+// a split takes its ticket -- every split but the last publishes (fence,
+// ready flag), the last waits for the others' flags, folds all the segment's
+// partials (eight heads at a time, every split's loads in flight together)
+// and writes the output, then resets the counter and the flags.  (A piece
+// that is a whole segment was written by the softmax warps.)
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_pieces_tc(const DecodeArgs &a, const Plan &plan, Walker walk, uint32_t st_full,
+                                                uint32_t st_free, volatile int *flags, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    static_assert(D == 128, "four output columns per lane");
+    const int H = a.H_kv * G;
+    const int me = int(blockIdx.x);
+    uint32_t piece = 0;
+    Piece pc;
+    while (walk.next(a, pc)) {
+        bool ok = !flags[0] && dev::mbar_wait_bounded(st_full, piece & 1, flags, a.timeout_ns);
+        ok = __all_sync(FULL, ok);
+        if (!ok) {
+            if (lane == 0) {
+                if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            return;
+        }
+        const int seg = pc.b * a.H_kv + pc.kv;
+        const int c0 = int(pc.seg_start / plan.chunk), c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
+        if (c0 != c1) {  // whole segments were written by the softmax warps
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(a.tickets + seg, 1);
+            ticket = __shfl_sync(FULL, ticket, 0);
+            if (ticket < c1 - c0) {
+                // not the last split: publish the partial
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) dev::flag_store(a.ready + me + seg, 1);
+            } else {
+                // the last split: wait for the others' flags, then fold every
+                // split's partial (this CTA's included)
+                bool pub = true;
+                for (int c = c0 + lane; c <= c1; c += 32)
+                    if (c != me) pub = pub && dev::flag_wait_bounded(a.ready + c + seg, flags, a.flag_timeout_ns);
+                pub = __all_sync(FULL, pub);
+                if (!pub) {
+                    if (lane == 0) {
+                        if (!flags[0]) dev::record_error(a.err, ERR_TIMEOUT);
+                        flags[0] = 1;
+                    }
+                    return;
+                }
+                __threadfence();
+                // lane h < G: head h's max and sum over the splits
+                const float *mlp = a.part_ml + (int64_t(c0) + seg) * G * 2;
+                float Mh = -INFINITY, Lh = 0.f;
+                if (lane < G) {
+                    for (int c = 0; c <= c1 - c0; ++c) Mh = fmaxf(Mh, __ldcg(mlp + (c * G + lane) * 2));
+                    for (int c = 0; c <= c1 - c0; ++c)
+                        Lh = fmaf(__ldcg(mlp + (c * G + lane) * 2 + 1), tcd::ex2(__ldcg(mlp + (c * G + lane) * 2) - Mh), Lh);
+                }
+                const float invh = lane < G ? 1.f / Lh : 0.f;
+                // eight heads at a time, lane l: output columns [4 l, 4 l + 4)
+#pragma unroll 1
+                for (int h0 = 0; h0 < G; h0 += 8) {
+                    float4 acc[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = 0; c <= c1 - c0; ++c) {
+                        const float e_lane = lane < G ? tcd::ex2(__ldcg(mlp + (c * G + lane) * 2) - Mh) : 0.f;
+                        const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + ((int64_t(c0) + c + seg) * G + h0) * D) + lane;
+                        float4 v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) v[k] = __ldcg(src + k * (D / 4));
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float e = __shfl_sync(FULL, e_lane, h0 + k);
+                            acc[k].x = fmaf(v[k].x, e, acc[k].x);
+                            acc[k].y = fmaf(v[k].y, e, acc[k].y);
+                            acc[k].z = fmaf(v[k].z, e, acc[k].z);
+                            acc[k].w = fmaf(v[k].w, e, acc[k].w);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float inv = __shfl_sync(FULL, invh, h0 + k);
+                        uint16_t *ob = reinterpret_cast<uint16_t *>(a.out) + (int64_t(pc.b) * H + pc.kv * G + h0 + k) * D + 4 * lane;
+                        const uint32_t lo = uint32_t(tcd::bits16<T>(acc[k].x * inv)) | (uint32_t(tcd::bits16<T>(acc[k].y * inv)) << 16);
+                        const uint32_t hi = uint32_t(tcd::bits16<T>(acc[k].z * inv)) | (uint32_t(tcd::bits16<T>(acc[k].w * inv)) << 16);
+                        *reinterpret_cast<uint2 *>(ob) = make_uint2(lo, hi);
+                    }
+                }
+                for (int c = c0 + lane; c <= c1; c += 32)  // ready for the next launch
+                    if (c != me) dev::flag_store(a.ready + c + seg, 0);
+                if (lane == 0) a.tickets[seg] = 0;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(st_free);
+        ++piece;
+    }
+}
+
 template <typename T, int G>
 // 13 warps: four run on one scheduler, whose 16,384 registers cap them at 128
 __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ DecodeArgs a) {
@@ -203,14 +307,11 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = dev::smem_addr(smem);
     const uint32_t k_s = sb + C::K_OFF, v_s = sb + C::V_OFF, q_s = sb + C::Q_OFF, p_s = sb + C::P_OFF;
-    float *scr_acc = reinterpret_cast<float *>(smem + C::SCR_OFF);  // [G][D]
-    float *scr_ml = scr_acc + G * D;                                   // [G][2]
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);        // [2 phases][2 halves][4 quarters][32]
-    float *lred = red + 2 * 2 * 4 * 32;                                // [2 halves][4 quarters][32]
     const uint32_t kfull = sb + C::BAR_OFF, kempty = kfull + 8 * NSK, vfull = kempty + 8 * NSK,
                    vempty = vfull + 8 * NSV, s_full = vempty + 8 * NSV, s_free = s_full + 16, p_full = s_free + 16,
                    p_free = p_full + 16, q_full = p_free + 16, q_empty = q_full + 8, o_free = q_empty + 8,
-                   scr_full = o_free + 8, scr_free = scr_full + 8, mx_bar = scr_free + 8, mma_done = mx_bar + 8;
+                   mx_bar = o_free + 8, st_full = mx_bar + 8, st_free = st_full + 8, mma_done = st_free + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + 8 * C::NBAR);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::BAR_OFF + 8 * C::NBAR + 16);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,8 +336,8 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
         dev::mbar_init(q_full, C::NSOFT);    // the piece's queries are in shared memory
         dev::mbar_init(q_empty, 1);          // the piece's last S has read them
         dev::mbar_init(o_free, C::NSOFT);    // the piece's O^T has been read
-        dev::mbar_init(scr_full, C::NSOFT);  // the piece's state is in the scratch
-        dev::mbar_init(scr_free, 1);         // the merger has read it
+        dev::mbar_init(st_full, C::NSOFT);   // the piece's state is in its partial slot
+        dev::mbar_init(st_free, 1);          // the merge warp is done with it
         dev::mbar_init(mx_bar, C::NSOFT);    // the four softmax warps' tile maxima
         dev::mbar_init(mma_done, 2);         // one commit per issuing thread
         flags[0] = 0;
@@ -418,7 +519,7 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
         __syncwarp();
     } else if (warp == C::MERGER) {
         // ------------------------------------------------------------ merger
-        merge_pieces_chunked<T, D, G, 1>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags, lane);
+        merge_pieces_tc<T, D, G>(a, plan, walk, st_full, st_free, flags, lane);
     } else {
         // ------------------------------------------------------------ softmax
         // Thread (w, hh, lane) owns key 32 w + lane of every tile (S^T lane)
@@ -543,18 +644,25 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
                 if (lane == 0) dev::mbar_arrive(p_full + 8 * (t & 1));
             }
             if (!ok) break;
-            // ---- piece epilogue: every head's sum over the 128 keys, then
-            // the state into the scratch once the merger has read the last one
+            // ---- piece epilogue: every head's sum over the piece's keys; a
+            // whole segment's output, or a split's state (O^T from tensor
+            // memory, each head's max and sum) into its partial slot (CTA +
+            // segment) for the merge warp, which runs the split combine.  The
+            // previous piece's combine must be done first: the two barriers
+            // between these warps and the merge warp then never run more than
+            // one phase apart.
             tcd::transpose_reduce<GH, true>(lsum, lane);
-            lred[(hh * 4 + w) * 32 + lane] = lsum[0];
+            float *lr = red + (mxp & 1) * 256;  // this phase's slots: [2 halves][4 quarters][32]
+            lr[(hh * 4 + w) * 32 + lane] = lsum[0];
+            const int seg = pc.b * a.H_kv + pc.kv;
             ok = !flags[0] &&
                  dev::mbar_wait_bounded(p_free + 8 * ((t - 1) & 1), uint32_t((t - 1) >> 1) & 1, flags, a.timeout_ns) &&
-                 (np == 0 || dev::mbar_wait_bounded(scr_free, uint32_t(np - 1) & 1, flags, a.timeout_ns));
+                 (np == 0 || dev::mbar_wait_bounded(st_free, uint32_t(np - 1) & 1, flags, a.timeout_ns));
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             tc::fence_after();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(mx_bar);  // partial sums written (one more phase of mx)
+            if (lane == 0) dev::mbar_arrive(mx_bar);  // sums written (one more phase of mx)
             ok = __all_sync(FULL, dev::mbar_wait_bounded(mx_bar, uint32_t(mxp) & 1, flags, a.timeout_ns));
             ++mxp;
             if (!ok) break;
@@ -566,16 +674,41 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) dev::mbar_arrive(o_free);  // O^T read: the next piece may overwrite it
+                const float *lh = lr + hh * 4 * 32;
+                const float l_lane = (lh[lane] + lh[32 + lane]) + (lh[64 + lane] + lh[96 + lane]);  // head hh GH + lane mod GH
+                const int c0 = int(pc.seg_start / plan.chunk), c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
+                if (c0 == c1) {
+                    // the piece is the whole segment: its output, normalised
+                    uint16_t *ob = reinterpret_cast<uint16_t *>(a.out) + (int64_t(pc.b) * H + pc.kv * G + hh * GH) * D + key;
 #pragma unroll
-                for (int h = 0; h < GH; ++h) scr_acc[(hh * GH + h) * D + key] = __uint_as_float(o[h]);
+                    for (int h = 0; h < GH; ++h)
+                        ob[h * D] = tcd::bits16<T>(__uint_as_float(o[h]) / __shfl_sync(FULL, l_lane, h));
+                } else {
+                    // a split: its partial, combined by the merge warp
+                    const int64_t slot = int64_t(blockIdx.x) + seg;
+                    float *pa = a.part_acc + (slot * G + hh * GH) * D + key;
+#pragma unroll
+                    for (int h = 0; h < GH; ++h) pa[h * D] = __uint_as_float(o[h]);
+                    if (w == 0 && lane < GH) {
+                        a.part_ml[(slot * G + hh * GH + lane) * 2] = m_run;
+                        a.part_ml[(slot * G + hh * GH + lane) * 2 + 1] = l_lane;
+                    }
+                    __threadfence();
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(st_full);
             }
-            if (w == 0 && lane < GH) {
-                const float *lr = lred + hh * 4 * 32;
-                scr_ml[(hh * GH + lane) * 2] = m_run;
-                scr_ml[(hh * GH + lane) * 2 + 1] = (lr[lane] + lr[32 + lane]) + (lr[64 + lane] + lr[96 + lane]);
+            // fused step: the CTA holding the segment's last row stores the
+            // step's new K and V rows into the cache (nobody in this launch
+            // reads them back from there)
+            if (a.k_new && pc.hi == pc.n && sid < 2 * C::CHUNKS) {
+                const bool is_v = sid >= C::CHUNKS;
+                const int c16 = is_v ? sid - C::CHUNKS : sid;
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) +
+                                                                       int64_t(seg) * C::ROW_BYTES) + c16);
+                uint8_t *cache = const_cast<uint8_t *>(is_v ? a.V : a.K);  // the caller's writable cache
+                reinterpret_cast<uint4 *>(cache + int64_t(seg) * kv_slab + int64_t(pc.n - 1) * C::ROW_BYTES)[c16] = v;
             }
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(scr_full);
             ++np;
         }
         if (!ok && lane == 0) {
