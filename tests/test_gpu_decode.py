@@ -178,6 +178,10 @@ CASES = [
     ("fp16", 64, 16, 1, 5, 1200, 15),
     ("bf16", 128, 64, 1, 2, 1300, 16),
     ("fp16", 128, 64, 2, 2, 900, 17),
+    # 16 and 32 heads at d_h 128 run the tcgen05 kernel: fp16, and 16 heads
+    ("fp16", 128, 32, 1, 3, 2100, 18),
+    ("fp16", 128, 16, 2, 4, 1500, 19),
+    ("bf16", 128, 16, 1, 5, 700, 20),
 ]
 
 

@@ -70,6 +70,7 @@ SEQ = [
     ("bf16_g8_d128", "bf16", 128, 8, 1, 2, 520, [1, 480]),
     ("bf16_g32_d128_mqa", "bf16", 128, 32, 1, 3, 600, [0, 33, 590]),
     ("fp16_g16_d64", "fp16", 64, 32, 2, 2, 400, [64, 391]),
+    ("fp16_g16_d128_tc", "fp16", 128, 32, 2, 3, 400, [0, 127, 383]),
     ("fp32_g6_d128_two_launches", "fp32", 128, 12, 2, 3, 300, [0, 40, 290]),
     ("bf16_g1_d128_two_launches", "bf16", 128, 4, 4, 2, 300, [5, 100]),
 ]
