@@ -611,18 +611,7 @@ kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q, const voi
     if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
     const uint64_t slab = layer_slab_bytes(h);
-    if (h->cfg.dtype == KVC_INT8) {  // the quantising append, then the attention
-        const uint64_t ss = layer_scale_bytes(h);
-        const cudaError_t e = kvc::launch_append_q8(
-            h->k_base + slab * layer, h->v_base + slab * layer, reinterpret_cast<float *>(h->k_scale + ss * layer),
-            reinterpret_cast<float *>(h->v_scale + ss * layer), static_cast<const uint8_t *>(k_new),
-            static_cast<const uint8_t *>(v_new), valid_len, -1, h->cfg.batch, h->cfg.n_kv_heads, 1,
-            h->cfg.max_context, h->cfg.d_head, reinterpret_cast<int32_t *>(h->ws), h->num_sms,
-            static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return KVC_ERR_CUDA;
-        return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
-    }
-    if (h->decode->tensor_maps)  // one launch: the kernel appends as it streams
+    if (h->decode->tensor_maps)  // one launch: the kernel appends (an int8 cache: quantises) as it streams
         return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, k_new, v_new);
     // the CUDA-core kernel: the append, then the attention, on the same stream
     const cudaError_t e = kvc::launch_append(

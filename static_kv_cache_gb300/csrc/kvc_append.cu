@@ -93,23 +93,10 @@ __global__ void __launch_bounds__(256) append_q8_kernel(uint8_t *__restrict__ K,
         }
         const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(is_v ? v_new : k_new) + r * D + lane * EPL;
         float x[EPL];
-        float am = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            x[e] = __bfloat162float(src[e]);
-            am = fmaxf(am, fabsf(x[e]));
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        const float scale = am / 127.0f;
-        const float inv = am > 0.f ? 127.0f / am : 0.f;
-        uint32_t packed = 0;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            int c = __float2int_rn(x[e] * inv);
-            c = c > 127 ? 127 : (c < -127 ? -127 : c);
-            packed |= (uint32_t(c) & 0xffu) << (8 * e);
-        }
+        for (int e = 0; e < EPL; ++e) x[e] = __bfloat162float(src[e]);
+        float scale;
+        const uint32_t packed = dev::quantise_row_q8<EPL>(x, scale);
         const int64_t row = seg * max_ctx + ci + t;          // cache row within the layer
         uint8_t *dst = (is_v ? V : K) + row * D + lane * EPL;
         if constexpr (EPL == 4)

@@ -677,8 +677,10 @@ struct FinalCombine {
 // and the flags for the next launch.  When that last split is the CTA's final
 // piece and the segment has more than HELP_MIN_OTHERS other splits, the fold
 // is left to the whole CTA: the function returns true with the job in `job`
-// and the CTA's own partial in `st`.
-template <typename T, int D, int G, int NW, int KH = 1>
+// and the CTA's own partial in `st`.  In a fused step it also stores the new
+// 16-bit K and V rows into the cache (NEW_ROWS false: the caller's producer
+// stores them itself, as the int8 cache's quantising producer does).
+template <typename T, int D, int G, int NW, int KH = 1, bool NEW_ROWS = true>
 __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &plan, Walker walk,
                                              const float *scr_acc, const float *scr_ml, uint32_t scr_full,
                                              uint32_t scr_free, volatile int *flags, int lane,
@@ -694,7 +696,7 @@ __device__ __forceinline__ bool merge_pieces(const DecodeArgs &a, const Plan &pl
         Walker peek = walk;
         Piece next_pc;
         const bool final_piece = !peek.next(a, next_pc);
-        if (a.k_new && pc.hi == pc.n && lane < 2 * CHUNKS) {
+        if (NEW_ROWS && a.k_new && pc.hi == pc.n && lane < 2 * CHUNKS) {
             // fused step: this CTA holds the segment's last row; store the
             // new K and V rows of its KH KV heads into the cache (nobody in
             // this launch reads them back from there)

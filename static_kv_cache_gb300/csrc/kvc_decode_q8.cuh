@@ -108,7 +108,8 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 // Producer: codes through the tensor maps (one box of 128 codes x 128 rows
 // for a whole tile, boxes of x 8 rows in a tail tile), the tail's last rows
-// and every row scale by cp.async.
+// and every row scale by cp.async; in a fused step the new row is quantised
+// by the warp itself (the append's own quantise_row_q8).
 template <typename C>
 __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker walk, uint32_t stage0,
                                                      uint32_t scale0, uint32_t bar0, int ns, int64_t kv_slab,
@@ -126,6 +127,10 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
         const uint8_t *vseg = a.V + int64_t(seg) * kv_slab;
         const float *kss = a.k_scale + int64_t(seg) * a.max_ctx;
         const float *vss = a.v_scale + int64_t(seg) * a.max_ctx;
+        // In a fused step the segment's last row is this step's new row: the
+        // warp quantises it from k_new / v_new into the stage and the cache;
+        // no box or copy reads it from the stale cache.
+        const int new_row = a.k_new ? pc.n - 1 : -1;
         for (int row0 = pc.lo; row0 < pc.hi; row0 += TILE) {
             const int nr = min(TILE, pc.hi - row0);
             if (round > 0) {
@@ -143,7 +148,9 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
             const uint32_t sdst = scale0 + uint32_t(stage) * C::SCALE_BYTES;
-            const int q = nr >> 3, rem = nr & 7;  // 8-row groups (boxes), rows after them
+            // rows boxes may cover: all but a new row (always the tile's last)
+            const int nb = (new_row >= row0 && new_row < row0 + nr) ? new_row - row0 : nr;
+            const int q = nb >> 3, rem = nr - 8 * q;  // 8-row groups (boxes), rows after them
             if (lane == 0) {
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
@@ -161,19 +168,43 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
 #pragma unroll
             for (int h = 0; h < TILE / 32; ++h) {
                 const int r = lane + 32 * h;
-                if (r < nr) {
+                if (r < nb) {
                     dev::cp_async_4(sdst + 4 * r, kss + row0 + r);
                     dev::cp_async_4(sdst + 4 * (TILE + r), vss + row0 + r);
                 }
             }
             if (rem) {
-                const int per = rem * C::CHUNKS;
+                const int per = (nb - 8 * q) * C::CHUNKS;  // the rows before a new row
                 for (int i = lane; i < 2 * per; i += 32) {
                     const bool is_v = i >= per;
                     const int j = is_v ? i - per : i;
                     const int r = 8 * q + j / C::CHUNKS, c16 = j % C::CHUNKS;
                     const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
                     dev::cp_async_16(C::swz(is_v ? vdst : kdst, r, c16), src);
+                }
+                if (nb < nr) {
+                    // the new row, K then V: lane l quantises elements
+                    // [4l, 4l + 4) and stores their codes in the stage (16-byte
+                    // chunk l / 4 of the swizzled row) and in the cache, with
+                    // the row's scale beside them
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint8_t *src = (t ? a.v_new : a.k_new) + int64_t(seg) * (2 * C::ROW_BYTES) + 8 * lane;
+                        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src));
+                        const float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                                            __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
+                        float scale;
+                        const uint32_t codes = dev::quantise_row_q8<4>(x, scale);
+                        dev::st_shared_u32(C::swz(t ? vdst : kdst, nb, lane >> 2) + 4 * (lane & 3), codes);
+                        uint8_t *cache = const_cast<uint8_t *>(t ? a.V : a.K);  // the caller's writable cache
+                        reinterpret_cast<uint32_t *>(cache + int64_t(seg) * kv_slab +
+                                                     int64_t(new_row) * C::ROW_BYTES)[lane] = codes;
+                        if (lane == 0) {
+                            dev::st_shared_f32(sdst + 4 * (t * TILE + nb), scale);
+                            const_cast<float *>(t ? a.v_scale : a.k_scale)[int64_t(seg) * a.max_ctx + new_row] =
+                                scale;
+                        }
+                    }
                 }
                 generic_written |= 1u << stage;
             } else {
@@ -227,8 +258,8 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
         flags[0] = 0;
         dev::fence_mbar_init();
     }
-    // the set-up above overlaps the previous kernel on the stream (the
-    // quantising append); nothing below runs before it has completed
+    // the set-up above overlaps the previous kernel on the stream; nothing
+    // below runs before it has completed
     dev::grid_dependency_wait();
     dev::allow_dependents();
     if (a.B <= C::VL_CACHE)
@@ -259,8 +290,8 @@ __global__ void __launch_bounds__(Q8Cfg<D, G>::THREADS, 1) decode_q8_kernel(cons
     if (warp == C::MERGER_WARP) {
         LaneState<D, G> st;
         FinalCombine job;
-        const bool help = merge_pieces<T, D, G, NW>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free, flags,
-                                                    lane, st, job);
+        const bool help = merge_pieces<T, D, G, NW, 1, false>(a, plan, walk, scr_acc, scr_ml, scr_full, scr_free,
+                                                              flags, lane, st, job);
         if (lane == 0) {
             flags[1] = help;
             flags[2] = job.seg;

@@ -439,6 +439,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -502,6 +508,33 @@ __device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
 // next such kernel be scheduled once every CTA of this grid has issued it.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The int8 cache's quantisation of one row ("10.3 -- KV cache implementation
+// details", section 4.4: the cache stored as int8, p = 1), taken by a whole
+// warp: lane l holds elements [l * EPL, (l + 1) * EPL) of the row in fp32.
+// scale = absmax / 127 and code = rint(x * (127 / absmax)) in fp32 (IEEE
+// division and product, round half to even), codes clamped to [-127, 127]; a
+// row of zeros gets scale 0.  Returns the lane's EPL codes packed little-end
+// first; every caller (the append and the fused decode step) goes through
+// this one function, so their codes agree bit for bit.
+template <int EPL>
+__device__ __forceinline__ uint32_t quantise_row_q8(const float (&x)[EPL], float &scale) {
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) am = fmaxf(am, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    scale = am / 127.0f;
+    const float inv = am > 0.f ? 127.0f / am : 0.f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        int c = __float2int_rn(x[e] * inv);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        packed |= (uint32_t(c) & 0xffu) << (8 * e);
+    }
+    return packed;
+}
 
 }  // namespace dev
 }  // namespace kvc

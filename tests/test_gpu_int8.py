@@ -168,6 +168,81 @@ def test_decode_steps_on_int8_cache():
     assert hn.canaries_intact()
 
 
+# New rows at the interesting offsets of the int8 kernel's 128-row tiles:
+# the first row, ends and starts of 8-row box groups and of tiles, the two
+# 64-key halves of a tile, the last row of the buffer.
+Q8_EDGE_LENGTHS = [1, 2, 8, 9, 63, 64, 65, 127, 128, 129, 136, 257, 511, 700]
+
+
+def _fill_prefixes(hn, layer, pre, *tags):
+    k, v = hn.rows(max(max(pre), 1), *tags)
+    for b, n in enumerate(pre):
+        if n:
+            ci = torch.full((hn.B,), hn.T + 1, dtype=torch.int32, device="cuda")
+            ci[b] = 0
+            assert hn.kvc.kvc_append(hn.h, layer, k[:, :, :n].contiguous(), v[:, :, :n].contiguous(), ci, n,
+                                     None) == 0
+    hn.kvc.kvc_get_error(hn.h, None)   # the skipped sequences' index errors
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 13, 152])
+def test_int8_fused_step_equals_append_then_decode(splits):
+    """kvc_decode_step on an int8 cache quantises the new row inside the
+    attention launch: the cache (codes and scales, padded rows included)
+    equals kvc_append then kvc_decode_attn byte for byte, the new rows equal
+    the oracle's quantisation, and the output matches the oracle."""
+    B, T = len(Q8_EDGE_LENGTHS), 700
+    lengths = np.array(Q8_EDGE_LENGTHS)
+    fused, twice = Q8Harness(1, B, 16, 4, 128, T, seed=2700), Q8Harness(1, B, 16, 4, 128, T, seed=2700)
+    for hn in (fused, twice):
+        _fill_prefixes(hn, 0, (lengths - 1).tolist(), "pre")
+        if splits:
+            assert hn.kvc.kvc_set_num_splits(hn.h, splits) == 0
+    kn, vn = fused.rows(1, "step")
+    q = fused.query("step")
+    vl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    out_f = torch.empty((B, 16, 128), dtype=torch.bfloat16, device="cuda")
+    out_t = torch.empty_like(out_f)
+    assert fused.kvc.kvc_decode_step(fused.h, 0, q, kn, vn, vl, T, out_f, None) == 0
+    assert twice.kvc.kvc_append(twice.h, 0, kn, vn, vl - 1, 1, None) == 0
+    assert twice.kvc.kvc_decode_attn(twice.h, 0, q, vl, T, out_t, None) == 0
+    torch.cuda.synchronize()
+    assert fused.kvc.kvc_get_error(fused.h, None) == 0 and twice.kvc.kvc_get_error(twice.h, None) == 0
+    for a, b in ((fused.K, twice.K), (fused.V, twice.V), (fused.KS, twice.KS), (fused.VS, twice.VS)):
+        assert torch.equal(a, b)
+    kc, ks = quantize_rows(_gpu.bits(kn), "bf16")
+    vc, vs = quantize_rows(_gpu.bits(vn), "bf16")
+    for b, n in enumerate(lengths):
+        assert np.array_equal(fused.K[0, b, :, n - 1].cpu().numpy(), kc[b, :, 0])
+        assert np.array_equal(fused.V[0, b, :, n - 1].cpu().numpy(), vc[b, :, 0])
+        assert np.array_equal(fused.KS[0, b, :, n - 1].cpu().numpy().view(np.float32), ks[b, :, 0])
+        assert np.array_equal(fused.VS[0, b, :, n - 1].cpu().numpy().view(np.float32), vs[b, :, 0])
+    ref = _decode_ref(fused, 0, q, lengths)
+    _gpu.compare(out_f, ref, "bf16", "int8 fused step")
+    _gpu.compare(out_t, ref, "bf16", "int8 append + decode")
+    assert fused.canaries_intact() and twice.canaries_intact()
+
+
+def test_int8_step_bad_valid_len_skips_append_and_output():
+    hn = Q8Harness(1, 3, 8, 2, 128, 100, seed=2800)
+    _fill_prefixes(hn, 0, [49, 10, 99], "bad")
+    before = [t.clone() for t in (hn.K, hn.V, hn.KS, hn.VS)]
+    kn, vn = hn.rows(1, "bad-step")
+    q = hn.query("bad-step")
+    for bad in (0, 101, -3):
+        vl = torch.tensor([50, bad, 100], dtype=torch.int32, device="cuda")
+        out = torch.full((3, 8, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+        assert hn.kvc.kvc_decode_step(hn.h, 0, q, kn, vn, vl, 100, out, None) == 0
+        torch.cuda.synchronize()
+        assert hn.kvc.kvc_get_error(hn.h, None) == hn.kvc.KVC_ERR_DEVICE_INDEX
+        assert (out[1].float() == 7.0).all(), "a skipped sequence's output must stay unwritten"
+        for t, t0 in zip((hn.K, hn.V, hn.KS, hn.VS), before):
+            assert torch.equal(t[0, 1], t0[0, 1])
+    ref = _decode_ref(hn, 0, q, np.array([50, 1, 100]))
+    _gpu.compare(out[[0, 2]], ref[[0, 2]], "bf16", "the valid sequences")
+    assert hn.canaries_intact()
+
+
 def test_int8_attention_stays_close_to_the_unquantised_attention():
     """The quality side of section 4.4 ("a small quality cost"): on N(0,1)
     rows the int8 cache's attention output stays within 0.05 of the bf16
