@@ -255,7 +255,11 @@ kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new,
  *   out[b, i, :] = softmax_j( q[b, i, :] . K_l[b, i / g, j, :] / sqrt(d_h) )
  *                  . V_l[b, i / g, j, :]       over j < valid_len[b]
  * with g = n_heads / n_kv_heads (query head i reads KV head i / g, the
- * contiguous grouping).  Rows at or past valid_len[b] are never read.
+ * contiguous grouping).  Rows at or past valid_len[b] never reach the
+ * output: the 16-bit and fp32 kernels never read them; on an int8 cache a
+ * ragged last tile may be copied whole (codes of up to 127 rows past
+ * valid_len[b], within max_context), and those codes are discarded
+ * unused (their scales are never read).
  * Arithmetic: fp32 products and accumulation, one round-to-nearest-even to
  * the cache type at the end.
  *   layer           0 <= layer < n_layers

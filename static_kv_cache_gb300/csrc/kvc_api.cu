@@ -37,6 +37,7 @@ struct kvc_cache {
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
     CUtensorMap pf_k32, pf_k8, pf_v32, pf_v8;  // the chunked prefill's (64-column blocks)
     CUtensorMap pf_k128, pf_v128;             // and its whole-tile boxes (128 rows)
+    CUtensorMap q8_k64, q8_v64, q8_k32, q8_v32;  // int8 caches: 64- and 32-row boxes
 };
 
 namespace {
@@ -237,11 +238,16 @@ bool kvc::encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, c
 bool kvc::encode_row_box_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                               const void *v_base, int rows, CUtensorMap *k, CUtensorMap *v) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16) || rows < 1 || rows > 256) return false;
-    const CUtensorMapDataType dt = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!encode || (dtype != KVC_BF16 && dtype != KVC_FP16 && dtype != KVC_INT8) || rows < 1 || rows > 256)
+        return false;
+    // 128 bytes of a row per box: 64 16-bit elements or 128 int8 codes
+    const int eb = dtype == KVC_INT8 ? 1 : 2;
+    const CUtensorMapDataType dt = dtype == KVC_INT8   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_ctx), cuuint64_t(n_segs)};
-    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(max_ctx) * D * 2};
-    const cuuint32_t box[3] = {64, cuuint32_t(rows), 1};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * eb, cuuint64_t(max_ctx) * D * eb};
+    const cuuint32_t box[3] = {cuuint32_t(128 / eb), cuuint32_t(rows), 1};
     const cuuint32_t elem[3] = {1, 1, 1};
     const void *bases[2] = {k_base, v_base};
     CUtensorMap *outs[2] = {k, v};
@@ -452,6 +458,14 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
             delete h;
             return KVC_ERR_CUDA;
         }
+        if (cfg->dtype == KVC_INT8 &&
+            (!kvc::encode_row_box_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base, 64,
+                                       &h->q8_k64, &h->q8_v64) ||
+             !kvc::encode_row_box_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base, 32,
+                                       &h->q8_k32, &h->q8_v32))) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
     }
     *out = h;
     return KVC_OK;
@@ -571,7 +585,7 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
     a.block_table = h->block_table;
     a.max_blocks = c.max_context / 16;
     a.num_blocks = h->num_blocks;
-    a.gran = h->block_table ? 16 : 1;
+    a.gran = h->block_table ? 16 : h->decode->split_gran > 1 ? h->decode->split_gran : 1;
     if (h->block_table) a.seg_base = layer * h->num_blocks * c.n_kv_heads;
     if (kp == 2) {  // segments are head pairs; the pair maps address blocks
         a.H_kv = c.n_kv_heads / 2;
@@ -586,6 +600,12 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
         a.tm_v128 = h->pf_v128;
         a.tm_kr32 = h->pf_k32;
         a.tm_vr32 = h->pf_v32;
+        if (c.dtype == KVC_INT8) {
+            a.tm_k64 = h->q8_k64;
+            a.tm_v64 = h->q8_v64;
+            a.tm_kr32 = h->q8_k32;
+            a.tm_vr32 = h->q8_v32;
+        }
     }
     const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;

@@ -148,19 +148,39 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t kdst = stage0 + uint32_t(stage) * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
             const uint32_t sdst = scale0 + uint32_t(stage) * C::SCALE_BYTES;
-            // rows boxes may cover: all but a new row (always the tile's last)
-            const int nb = (new_row >= row0 && new_row < row0 + nr) ? new_row - row0 : nr;
-            const int q = nb >> 3, rem = nr - 8 * q;  // 8-row groups (boxes), rows after them
+            // A tile without the new row comes as one 128-row box per tensor,
+            // a segment's ragged last tile included: its rows past nr are
+            // copied but never used (their scores are -inf and their scaled
+            // probabilities 0, both by selection, and a code is always a
+            // finite integer).  Only a box that would run past max_ctx, and
+            // the tile holding a fused step's new row, take boxes of 64, 32
+            // and 8 rows over the rows before that row, and cp.async for the
+            // last few.
+            const bool has_new = new_row >= row0 && new_row < row0 + nr;
+            const int nb = has_new ? new_row - row0 : nr;  // rows read from the cache
+            const bool whole = !has_new && row0 + TILE <= a.max_ctx;
+            const int boxed = whole ? TILE : (nb & ~7);    // rows the boxes bring
             if (lane == 0) {
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
-                dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
-                if (q == TILE / 8) {  // a whole tile: one box of K, one of V
+                dev::mbar_expect_tx(full, 2u * uint32_t(boxed) * C::ROW_BYTES);
+                if (whole) {
                     dev::tma_load_3d(kdst, &a.tm_k32, 0, row0, z, full);
                     dev::tma_load_3d(vdst, &a.tm_v32, 0, row0, z, full);
                 } else {
-                    for (int j = 0; j < q; ++j) {
-                        dev::tma_load_3d(kdst + j * 8 * 128, &a.tm_k8, 0, row0 + 8 * j, z, full);
-                        dev::tma_load_3d(vdst + j * 8 * 128, &a.tm_v8, 0, row0 + 8 * j, z, full);
+                    int r = 0;
+                    if (boxed - r >= 64) {
+                        dev::tma_load_3d(kdst, &a.tm_k64, 0, row0, z, full);
+                        dev::tma_load_3d(vdst, &a.tm_v64, 0, row0, z, full);
+                        r += 64;
+                    }
+                    if (boxed - r >= 32) {
+                        dev::tma_load_3d(kdst + r * 128, &a.tm_kr32, 0, row0 + r, z, full);
+                        dev::tma_load_3d(vdst + r * 128, &a.tm_vr32, 0, row0 + r, z, full);
+                        r += 32;
+                    }
+                    for (; r < boxed; r += 8) {
+                        dev::tma_load_3d(kdst + r * 128, &a.tm_k8, 0, row0 + r, z, full);
+                        dev::tma_load_3d(vdst + r * 128, &a.tm_v8, 0, row0 + r, z, full);
                     }
                 }
             }
@@ -173,16 +193,16 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
                     dev::cp_async_4(sdst + 4 * (TILE + r), vss + row0 + r);
                 }
             }
-            if (rem) {
-                const int per = (nb - 8 * q) * C::CHUNKS;  // the rows before a new row
+            if (!whole) {
+                const int per = (nb - boxed) * C::CHUNKS;  // rows after the boxes, before a new row
                 for (int i = lane; i < 2 * per; i += 32) {
                     const bool is_v = i >= per;
                     const int j = is_v ? i - per : i;
-                    const int r = 8 * q + j / C::CHUNKS, c16 = j % C::CHUNKS;
+                    const int r = boxed + j / C::CHUNKS, c16 = j % C::CHUNKS;
                     const uint8_t *src = (is_v ? vseg : kseg) + int64_t(row0 + r) * C::ROW_BYTES + c16 * 16;
                     dev::cp_async_16(C::swz(is_v ? vdst : kdst, r, c16), src);
                 }
-                if (nb < nr) {
+                if (has_new) {
                     // the new row, K then V: lane l quantises elements
                     // [4l, 4l + 4) and stores their codes in the stage (16-byte
                     // chunk l / 4 of the swizzled row) and in the cache, with
@@ -561,7 +581,7 @@ const DecodeKernelInfo *q8_decode_info() {
     using C = Q8Cfg<D, G>;
     // one stage per stream in use, one more being filled
     static const DecodeKernelInfo info = {C::TILE, C::NW / C::WPT, C::STAGE_BYTES + 16 + C::SCALE_BYTES, C::FIXED_SMEM,
-                                          &set_q8_max_smem<D, G>, &launch_q8<D, G>, true};
+                                          &set_q8_max_smem<D, G>, &launch_q8<D, G>, true, false, false, C::TILE};
     return &info;
 }
 

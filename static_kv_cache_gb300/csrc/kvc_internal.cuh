@@ -93,8 +93,11 @@ struct DecodeArgs {
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // the type carries its own alignment
     // The tcgen05 kernel of large head groups: boxes of 64 columns x 128 and
     // x 32 rows over the same caches (one column block per box); it takes
-    // its 8-row boxes from tm_k8 / tm_v8.
+    // its 8-row boxes from tm_k8 / tm_v8.  The int8 kernel: boxes of 128
+    // codes x 32 rows in tm_kr32 / tm_vr32 and x 64 rows in tm_k64 / tm_v64,
+    // for the tile that holds a fused step's new row.
     CUtensorMap tm_k128, tm_v128, tm_kr32, tm_vr32;
+    CUtensorMap tm_k64, tm_v64;
 };
 
 // One compiled decode kernel and what the host needs to launch it.
@@ -108,6 +111,7 @@ struct DecodeKernelInfo {
     bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
     bool tile_box;       // its full-tile map is the 4-D one of encode_cache_maps
     bool row_box_maps;   // also reads through the 128- and 32-row maps (tm_k128 ...)
+    int split_gran;      // split points fall on multiples of this many rows (0: 1)
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -203,8 +207,9 @@ bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const 
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
                        CUtensorMap *v8, bool tile_box = false);
 
-// Tensor maps of 16-bit K and V caches [n_segs][max_ctx][D] with boxes of 64
-// columns x `rows` rows (at most 256), 128-byte swizzle.  Host only.
+// Tensor maps of K and V caches [n_segs][max_ctx][D] with boxes of 128 bytes
+// of a row (64 16-bit elements or 128 int8 codes) x `rows` rows (at most
+// 256), 128-byte swizzle.  Host only.
 bool encode_row_box_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                          const void *v_base, int rows, CUtensorMap *k, CUtensorMap *v);
 
