@@ -1299,7 +1299,7 @@ const DecodeKernelInfo *mma_decode_info() {
     using C = MmaCfg<T, D, G>;
     static const DecodeKernelInfo info = {PAIR ? 16 : C::TILE, C::NW, C::STAGE_BYTES + 16, C::FIXED_SMEM,
                                           &set_mma_max_smem<T, D, G, PG, PAIR>, &launch_mma<T, D, G, PG, PAIR>,
-                                          true, true};
+                                          true, true, false, PAIR ? 16 : C::TILE};
     return &info;
 }
 

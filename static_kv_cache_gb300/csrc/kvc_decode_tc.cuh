@@ -750,7 +750,7 @@ template <typename T, int G>
 const DecodeKernelInfo *tc_decode_info() {
     using C = TcDecodeCfg<T, G>;
     static const DecodeKernelInfo info = {C::TK, 0, 1, C::SMEM, &set_tc_decode_max_smem<T, G>,
-                                          &launch_tc_decode<T, G>, true, true, true};
+                                          &launch_tc_decode<T, G>, true, true, true, C::TK};
     return &info;
 }
 

@@ -111,7 +111,11 @@ struct DecodeKernelInfo {
     bool tensor_maps;    // reads K/V through the tensor maps in DecodeArgs
     bool tile_box;       // its full-tile map is the 4-D one of encode_cache_maps
     bool row_box_maps;   // also reads through the 128- and 32-row maps (tm_k128 ...)
-    int split_gran;      // split points fall on multiples of this many rows (0: 1)
+    // Split points fall on multiples of this many rows of a segment (0: any
+    // row).  A kernel's tile: then only a segment's last tile is ragged, not
+    // also the last tile of every piece that ends inside a segment (each
+    // ragged tile costs the copy issuer several small boxes).
+    int split_gran;
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
