@@ -37,7 +37,7 @@ struct kvc_cache {
     CUtensorMap tm_k32, tm_k8, tm_v32, tm_v8;  // used by kernels with info->tensor_maps
     CUtensorMap pf_k32, pf_k8, pf_v32, pf_v8;  // the chunked prefill's (64-column blocks)
     CUtensorMap pf_k128, pf_v128;             // and its whole-tile boxes (128 rows)
-    CUtensorMap q8_k64, q8_v64, q8_k32, q8_v32;  // int8 caches: 64- and 32-row boxes
+    CUtensorMap rb_k64, rb_v64, rb_k32, rb_v32;  // kernels with info->ragged_maps: 64- and 32-row boxes
 };
 
 namespace {
@@ -458,11 +458,11 @@ kvc_status alloc_impl(const kvc_config *cfg, void *k_base, void *v_base, void *k
             delete h;
             return KVC_ERR_CUDA;
         }
-        if (cfg->dtype == KVC_INT8 &&
+        if (info->ragged_maps &&
             (!kvc::encode_row_box_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base, 64,
-                                       &h->q8_k64, &h->q8_v64) ||
+                                       &h->rb_k64, &h->rb_v64) ||
              !kvc::encode_row_box_maps(cfg->dtype, cfg->d_head, cfg->max_context, n_segs, k_base, v_base, 32,
-                                       &h->q8_k32, &h->q8_v32))) {
+                                       &h->rb_k32, &h->rb_v32))) {
             delete h;
             return KVC_ERR_CUDA;
         }
@@ -600,11 +600,11 @@ kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32
         a.tm_v128 = h->pf_v128;
         a.tm_kr32 = h->pf_k32;
         a.tm_vr32 = h->pf_v32;
-        if (c.dtype == KVC_INT8) {
-            a.tm_k64 = h->q8_k64;
-            a.tm_v64 = h->q8_v64;
-            a.tm_kr32 = h->q8_k32;
-            a.tm_vr32 = h->q8_v32;
+        if (h->decode->ragged_maps && !h->block_table) {
+            a.tm_k64 = h->rb_k64;
+            a.tm_v64 = h->rb_v64;
+            a.tm_kr32 = h->rb_k32;
+            a.tm_vr32 = h->rb_v32;
         }
     }
     const cudaError_t e = h->decode->launch(a, grid, h->smem_bytes, static_cast<cudaStream_t>(stream));

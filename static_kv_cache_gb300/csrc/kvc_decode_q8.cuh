@@ -581,7 +581,8 @@ const DecodeKernelInfo *q8_decode_info() {
     using C = Q8Cfg<D, G>;
     // one stage per stream in use, one more being filled
     static const DecodeKernelInfo info = {C::TILE, C::NW / C::WPT, C::STAGE_BYTES + 16 + C::SCALE_BYTES, C::FIXED_SMEM,
-                                          &set_q8_max_smem<D, G>, &launch_q8<D, G>, true, false, false, C::TILE};
+                                          &set_q8_max_smem<D, G>, &launch_q8<D, G>, true, false, false, C::TILE,
+                                          true};
     return &info;
 }
 

@@ -116,6 +116,9 @@ struct DecodeKernelInfo {
     // also the last tile of every piece that ends inside a segment (each
     // ragged tile costs the copy issuer several small boxes).
     int split_gran;
+    // Also reads a ragged tile through boxes of 128-byte row slices x 64 and
+    // x 32 rows (tm_k64 / tm_v64, tm_kr32 / tm_vr32; contiguous caches).
+    bool ragged_maps;
 };
 
 // Registry of compiled decode kernels, one lookup per (element type, D);
@@ -204,9 +207,9 @@ KVC_DECLARE_PREFILL_TABLE(f16, 128)
 // x 8 rows (one 64-column block of a tile each).  With tile_box the 32-row
 // map is 4-D instead, (64 columns, rows, D / 64 column blocks, segments) with
 // the blocks 128 bytes apart, so one box brings a whole 32-row tile laid out
-// block after block.  int8 codes: boxes of 128 columns x 64 rows (a whole
-// int8 decode tile) and x 8 rows.  Host only; returns false if the driver
-// refuses.
+// block after block.  int8 codes: boxes of 128 columns x 128
+// rows (a whole int8 decode tile) and x 8 rows.  Host only; returns false if
+// the driver refuses.
 bool encode_cache_maps(int32_t dtype, int D, int max_ctx, int64_t n_segs, const void *k_base,
                        const void *v_base, CUtensorMap *k32, CUtensorMap *k8, CUtensorMap *v32,
                        CUtensorMap *v8, bool tile_box = false);
