@@ -299,6 +299,7 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
+    const uint64_t pol = dev::l2_evict_first_policy();  // K/V rows are read once per launch
     Piece pc;
     while (ok && walk.next(a, pc)) {
         const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
@@ -317,8 +318,8 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             dev::mbar_arrive_expect_tx(full, 2 * bytes);
-            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full);
-            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full);
+            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
+            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
             ++issued;
             if (++stage == ns) {
                 stage = 0;

@@ -158,6 +158,7 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
     uint32_t round = 0;
     uint32_t generic_written = 0;  // stages whose last fill used cp.async
     bool ok = true;
+    const uint64_t pol = dev::l2_evict_first_policy();  // K/V rows are read once per launch
     Piece pc;
     while (ok && walk.next(a, pc)) {
         const int seg = pc.b * a.H_kv + pc.kv;
@@ -192,15 +193,15 @@ __device__ __forceinline__ uint32_t produce_tiles_tma(const DecodeArgs &a, Walke
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(8 * q) * C::ROW_BYTES);
                 if (q == 4) {
-                    dev::tma_load_4d(kdst, &a.tm_k32, 0, row0, 0, z, full);
-                    dev::tma_load_4d(vdst, &a.tm_v32, 0, row0, 0, z, full);
+                    dev::tma_load_4d(kdst, &a.tm_k32, 0, row0, 0, z, full, pol);
+                    dev::tma_load_4d(vdst, &a.tm_v32, 0, row0, 0, z, full, pol);
                 } else {
                     for (int j = 0; j < q; ++j)
 #pragma unroll
                         for (int cb = 0; cb < CB; ++cb) {
                             const uint32_t off = cb * C::BLOCK_BYTES + j * 8 * 128;
-                            dev::tma_load_3d(kdst + off, &a.tm_k8, cb * 64, row0 + 8 * j, z, full);
-                            dev::tma_load_3d(vdst + off, &a.tm_v8, cb * 64, row0 + 8 * j, z, full);
+                            dev::tma_load_3d(kdst + off, &a.tm_k8, cb * 64, row0 + 8 * j, z, full, pol);
+                            dev::tma_load_3d(vdst + off, &a.tm_v8, cb * 64, row0 + 8 * j, z, full, pol);
                         }
                 }
             }
@@ -255,6 +256,7 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
+    const uint64_t pol = dev::l2_evict_first_policy();  // K/V rows are read once per launch
     Piece pc;
     while (ok && walk.next(a, pc)) {
         const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
@@ -321,7 +323,7 @@ __device__ __forceinline__ uint32_t produce_tiles_paged(const DecodeArgs &a, Wal
                 if (bx) {
                     const int z = a.seg_base + (jj ? phys[1] : phys[0]) * a.H_kv + pc.kv;
                     const CUtensorMap *m = bx == BS ? (is_v ? &a.tm_v32 : &a.tm_k32) : (is_v ? &a.tm_v8 : &a.tm_k8);
-                    dev::tma_load_3d((is_v ? vdst : kdst) + jj * BS * C::ROW_BYTES, m, 0, 0, z, full);
+                    dev::tma_load_3d((is_v ? vdst : kdst) + jj * BS * C::ROW_BYTES, m, 0, 0, z, full, pol);
                 }
             }
             bool generic = false;
@@ -389,6 +391,7 @@ __device__ __forceinline__ uint32_t produce_tiles_paged_pair(const DecodeArgs &a
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
+    const uint64_t pol = dev::l2_evict_first_policy();  // K/V rows are read once per launch
     Piece pc;
     while (ok && walk.next(a, pc)) {
         const int32_t *trow = a.block_table + int64_t(pc.b) * a.max_blocks;
@@ -433,13 +436,13 @@ __device__ __forceinline__ uint32_t produce_tiles_paged_pair(const DecodeArgs &a
                 // lane 0: K, lane 1: V, both heads in one box each
                 if (lane < 2)
                     dev::tma_load_5d(lane ? vdst : kdst, lane ? &a.tm_v32 : &a.tm_k32, 0, 0, 0, 2 * pc.kv, wblk,
-                                     full);
+                                     full, pol);
             } else if (boxed == 8 && lane < 4 * CB) {
                 // one 8-row box per (tensor, head, column block)
                 const bool is_v = lane & 1;
                 const int z = (lane >> 1) & 1, cb = lane >> 2;
                 dev::tma_load_5d((is_v ? vdst : kdst) + z * HEAD_BYTES + cb * 2048, is_v ? &a.tm_v8 : &a.tm_k8, 0, 0,
-                                 cb, 2 * pc.kv + z, wblk, full);
+                                 cb, 2 * pc.kv + z, wblk, full, pol);
             }
             const int rem = rows - boxed;
             if (rem > 0) {

@@ -119,6 +119,7 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
+    const uint64_t pol = dev::l2_evict_first_policy();  // codes are read once per launch
     Piece pc;
     while (ok && walk.next(a, pc)) {
         const int seg = pc.b * a.H_kv + pc.kv;
@@ -164,23 +165,23 @@ __device__ __forceinline__ uint32_t produce_tiles_q8(const DecodeArgs &a, Walker
                 if (generic_written & (1u << stage)) dev::fence_proxy_async_smem();
                 dev::mbar_expect_tx(full, 2u * uint32_t(boxed) * C::ROW_BYTES);
                 if (whole) {
-                    dev::tma_load_3d(kdst, &a.tm_k32, 0, row0, z, full);
-                    dev::tma_load_3d(vdst, &a.tm_v32, 0, row0, z, full);
+                    dev::tma_load_3d(kdst, &a.tm_k32, 0, row0, z, full, pol);
+                    dev::tma_load_3d(vdst, &a.tm_v32, 0, row0, z, full, pol);
                 } else {
                     int r = 0;
                     if (boxed - r >= 64) {
-                        dev::tma_load_3d(kdst, &a.tm_k64, 0, row0, z, full);
-                        dev::tma_load_3d(vdst, &a.tm_v64, 0, row0, z, full);
+                        dev::tma_load_3d(kdst, &a.tm_k64, 0, row0, z, full, pol);
+                        dev::tma_load_3d(vdst, &a.tm_v64, 0, row0, z, full, pol);
                         r += 64;
                     }
                     if (boxed - r >= 32) {
-                        dev::tma_load_3d(kdst + r * 128, &a.tm_kr32, 0, row0 + r, z, full);
-                        dev::tma_load_3d(vdst + r * 128, &a.tm_vr32, 0, row0 + r, z, full);
+                        dev::tma_load_3d(kdst + r * 128, &a.tm_kr32, 0, row0 + r, z, full, pol);
+                        dev::tma_load_3d(vdst + r * 128, &a.tm_vr32, 0, row0 + r, z, full, pol);
                         r += 32;
                     }
                     for (; r < boxed; r += 8) {
-                        dev::tma_load_3d(kdst + r * 128, &a.tm_k8, 0, row0 + r, z, full);
-                        dev::tma_load_3d(vdst + r * 128, &a.tm_v8, 0, row0 + r, z, full);
+                        dev::tma_load_3d(kdst + r * 128, &a.tm_k8, 0, row0 + r, z, full, pol);
+                        dev::tma_load_3d(vdst + r * 128, &a.tm_v8, 0, row0 + r, z, full, pol);
                     }
                 }
             }

@@ -374,6 +374,7 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
         const CUtensorMap *m128 = is_v ? &a.tm_v128 : &a.tm_k128;
         const CUtensorMap *m32 = is_v ? &a.tm_vr32 : &a.tm_kr32;
         const CUtensorMap *m8 = is_v ? &a.tm_v8 : &a.tm_k8;
+        const uint64_t pol = dev::l2_evict_first_policy();  // K/V rows are read once per launch
         uint32_t generic = 0;  // stages whose last fill had generic-proxy stores
         bool ok = true;
         Piece pc;
@@ -408,7 +409,7 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
                     if (lane == 0) {
                         dev::mbar_arrive_expect_tx(full, uint32_t(TK) * C::ROW_BYTES);
 #pragma unroll
-                        for (int cb = 0; cb < CB; ++cb) dev::tma_load_3d(dst + cb * BLK, m128, cb * 64, row0, z, full);
+                        for (int cb = 0; cb < CB; ++cb) dev::tma_load_3d(dst + cb * BLK, m128, cb * 64, row0, z, full, pol);
                     }
                     generic &= ~(1u << s);
                 } else {
@@ -421,12 +422,12 @@ __global__ void __maxnreg__(128) decode_tc_kernel(const __grid_constant__ Decode
                         for (int g = 0; g < n32; ++g)
 #pragma unroll
                             for (int cb = 0; cb < CB; ++cb)
-                                dev::tma_load_3d(dst + cb * BLK + g * 32 * 128, m32, cb * 64, row0 + 32 * g, z, full);
+                                dev::tma_load_3d(dst + cb * BLK + g * 32 * 128, m32, cb * 64, row0 + 32 * g, z, full, pol);
                         for (int g = 0; g < n8; ++g)
 #pragma unroll
                             for (int cb = 0; cb < CB; ++cb) {
                                 const int r = 32 * n32 + 8 * g;
-                                dev::tma_load_3d(dst + cb * BLK + r * 128, m8, cb * 64, row0 + r, z, full);
+                                dev::tma_load_3d(dst + cb * BLK + r * 128, m8, cb * 64, row0 + r, z, full, pol);
                             }
                     }
                     for (int i = lane; i < (TK - boxed) * C::CHUNKS; i += 32) {

@@ -401,6 +401,16 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// The same copy with an L2 cache policy (l2_evict_first_policy ...).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Four 8x8 matrices of 16-bit elements from shared memory; lane l supplies
 // the address of row (l % 8) of matrix (l / 8).  Lane l receives, from each
 // matrix, the 32-bit pair (row l/4, columns 2*(l%4) and 2*(l%4)+1); with
@@ -464,12 +474,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
 
 // One box of a 3-D tensor map (coordinates innermost first) into shared
 // memory through the TMA unit, completion signalled on `bar`.
+// L2 policies for the cache hint of a copy.  evict_first: the lines a copy
+// brings in are the first to go, for K/V (or latent) tiles that a decode
+// launch reads exactly once; they then do not push the small arrays that
+// every launch reuses (queries, lengths, block tables, split partials) out
+// of L2 on their way through.  evict_normal: the default behaviour.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
                                            uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// The same copy with an L2 cache policy (l2_evict_first_policy ...).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                           uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -483,6 +519,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same copy with an L2 cache policy (l2_evict_first_policy ...).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                           uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // The same for a 5-D tensor map.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w, int u,
                                            uint32_t bar) {
@@ -490,6 +536,16 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(u), "r"(bar)
+        : "memory");
+}
+
+// The same copy with an L2 cache policy (l2_evict_first_policy ...).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w, int u,
+                                           uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(u), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -279,6 +279,9 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
     if (warp == 0) {
         uint32_t t = 0;
         bool ok = true;
+        // one head group: the latent rows are read once per launch; several:
+        // the split's other groups read the same rows from L2 alongside
+        const uint64_t pol = a.groups > 1 ? dev::l2_evict_normal_policy() : dev::l2_evict_first_policy();
         Piece pc;
         while (ok && walk.next(a, pc)) {
             const int z = a.seg_base + pc.b;
@@ -303,14 +306,14 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
                     if (nr == TILE) {
                         dev::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
 #pragma unroll
-                        for (int cb = 0; cb < C::CB; ++cb) dev::tma_load_3d(dst + cb * BB, &a.tm64, cb * 64, row0, z, full);
+                        for (int cb = 0; cb < C::CB; ++cb) dev::tma_load_3d(dst + cb * BB, &a.tm64, cb * 64, row0, z, full, pol);
                     } else {
                         const int nb = (nr + 15) >> 4;
                         dev::mbar_arrive_expect_tx(full, uint32_t(nb) * C::CB * 16 * 128);
                         for (int j = 0; j < nb; ++j)
 #pragma unroll
                             for (int cb = 0; cb < C::CB; ++cb)
-                                dev::tma_load_3d(dst + cb * BB + j * 2048, &a.tm16, cb * 64, row0 + 16 * j, z, full);
+                                dev::tma_load_3d(dst + cb * BB + j * 2048, &a.tm16, cb * 64, row0 + 16 * j, z, full, pol);
                     }
                 }
                 __syncwarp();
