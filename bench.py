@@ -310,8 +310,8 @@ class DeviceState:
         self.v_new = synth.normal((L, B, w.n_kv_heads, 1, w.d_head), act, synth.sub_seed(w.seed, "vn"), dev)
         self.out = torch.empty((L, B, w.n_heads, w.d_head), dtype=adt, device=dev)
         self.valid_len = self.lengths.to(dev)
-        # the step is one fused launch on the TMA-fed kernels, else append + attention
-        self.launches_per_layer = 2 if decode_kernel_name(w) == "decode_split_kernel" else 1
+        # the step is one launch: every decode kernel appends as it streams
+        self.launches_per_layer = 1
         self.cfg = kvc.make_config(L, B, w.n_heads, w.n_kv_heads, w.d_head, w.max_context, w.dtype)
         self.ws = torch.empty(kvc.kvc_workspace_bytes(self.cfg), dtype=torch.uint8, device=dev)
         if w.paged:

@@ -283,11 +283,10 @@ kvc_status kvc_decode_attn(kvc_cache *h, int32_t layer, const void *q,
  * rows [0, valid_len[b]).  The result equals kvc_append(h, layer, k_new,
  * v_new, valid_len[b] - 1, T_new = 1) followed by kvc_decode_attn with the
  * same arguments: the cache bytes are identical and the output agrees to
- * fp32 rounding.  For 16-bit caches with head groups of 2 to 8, 16, 32 or 64 and d_h of 64
- * or 128, and for int8 caches, it is one launch that reads the new rows
- * straight from k_new / v_new (an int8 cache: quantises them, with the
- * codes and scale kvc_append would write) while it streams the older ones;
- * otherwise it enqueues the append and the attention back to back.
+ * fp32 rounding.  It is one launch, which reads the new rows straight from
+ * k_new / v_new (an int8 cache: quantises them, with the codes and scale
+ * kvc_append would write) while it streams the older ones, and stores them
+ * into the cache.
  *   layer, q, max_valid_hint, out   as for kvc_decode_attn
  *   k_new, v_new    device, [B, H_kv, 1, d_h], 16-byte aligned
  *   valid_len       device int32 [B]: live rows after this step's append.  A

@@ -547,7 +547,7 @@ kvc_status kvc_append(kvc_cache *h, int32_t layer, const void *k_new, const void
 namespace {
 
 // Launch the decode kernel of one layer; k_new / v_new non-null make it the
-// fused step (tensor-core kernel only).  Arguments are already validated.
+// fused step.  Arguments are already validated.
 kvc_status launch_decode(kvc_cache *h, int32_t layer, const void *q, const int32_t *valid_len,
                          int32_t max_valid_hint, void *out, void *stream, const void *k_new,
                          const void *v_new) {
@@ -630,17 +630,9 @@ kvc_status kvc_decode_step(kvc_cache *h, int32_t layer, const void *q, const voi
         return KVC_ERR_INVALID;
     if (max_valid_hint < 0 || max_valid_hint > h->cfg.max_context) return KVC_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGNMENT;
-    const uint64_t slab = layer_slab_bytes(h);
-    if (h->decode->tensor_maps)  // one launch: the kernel appends (an int8 cache: quantises) as it streams
-        return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, k_new, v_new);
-    // the CUDA-core kernel: the append, then the attention, on the same stream
-    const cudaError_t e = kvc::launch_append(
-        h->k_base + slab * layer, h->v_base + slab * layer, static_cast<const uint8_t *>(k_new),
-        static_cast<const uint8_t *>(v_new), valid_len, -1, h->cfg.batch, h->cfg.n_kv_heads, 1,
-        h->cfg.max_context, h->cfg.d_head * h->elem_bytes, reinterpret_cast<int32_t *>(h->ws), h->num_sms,
-        static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return KVC_ERR_CUDA;
-    return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, nullptr, nullptr);
+    // one launch: every decode kernel appends (an int8 cache: quantises) the
+    // step's new rows as it streams
+    return launch_decode(h, layer, q, valid_len, max_valid_hint, out, stream, k_new, v_new);
 }
 
 kvc_status kvc_prefill_attn(kvc_cache *h, int32_t layer, const void *q, const int32_t *cache_index,

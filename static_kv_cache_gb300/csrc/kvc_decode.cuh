@@ -305,6 +305,9 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
         const int64_t seg = int64_t(pc.b) * a.H_kv + pc.kv;
         const uint8_t *kseg = a.K + seg * kv_slab;
         const uint8_t *vseg = a.V + seg * kv_slab;
+        // In a fused step the segment's last row is this step's new row: it
+        // is copied from k_new / v_new, never from the stale cache row.
+        const int new_row = a.k_new ? pc.n - 1 : -1;
         for (int row = pc.lo; row < pc.hi; row += TILE) {
             const int nr = min(TILE, pc.hi - row);
             if (round > 0 &&
@@ -318,8 +321,18 @@ __device__ __forceinline__ uint32_t produce_tiles(const DecodeArgs &a, Walker wa
             const uint32_t full = bar0 + 8 * stage;
             const uint32_t dst = stage0 + uint32_t(stage) * C::STAGE_BYTES;
             dev::mbar_arrive_expect_tx(full, 2 * bytes);
-            dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
-            dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
+            if (new_row >= row && new_row < row + nr) {  // the new row is the tile's last
+                const uint32_t old_bytes = uint32_t(new_row - row) * C::ROW_BYTES;
+                if (old_bytes) {
+                    dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, old_bytes, full, pol);
+                    dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, old_bytes, full, pol);
+                }
+                dev::bulk_copy_g2s(dst + old_bytes, a.k_new + seg * C::ROW_BYTES, C::ROW_BYTES, full);
+                dev::bulk_copy_g2s(dst + C::TILE_BYTES + old_bytes, a.v_new + seg * C::ROW_BYTES, C::ROW_BYTES, full);
+            } else {
+                dev::bulk_copy_g2s(dst, kseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
+                dev::bulk_copy_g2s(dst + C::TILE_BYTES, vseg + int64_t(row) * C::ROW_BYTES, bytes, full, pol);
+            }
             ++issued;
             if (++stage == ns) {
                 stage = 0;
@@ -354,6 +367,19 @@ __device__ __forceinline__ void merge_piece(const DecodeArgs &a, const Plan &pla
     const int H = a.H_kv * G;
 
     const int seg = pc.b * a.H_kv + pc.kv;
+    if (a.k_new && pc.hi == pc.n) {
+        // fused step: this CTA holds the segment's last row; store the new K
+        // and V rows into the cache (nobody in this launch reads them there)
+        constexpr int VECS = D * int(sizeof(T)) / 16;  // 16-byte vectors of a row
+        const int64_t row_off = (int64_t(seg) * a.max_ctx + pc.n - 1) * (D * int64_t(sizeof(T)));
+        for (int i = ctid; i < 2 * VECS; i += NW * 32) {
+            const bool is_v = i >= VECS;
+            const int v = is_v ? i - VECS : i;
+            const uint4 x = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.v_new : a.k_new) +
+                                                                  int64_t(seg) * D * int64_t(sizeof(T))) + v);
+            reinterpret_cast<uint4 *>(const_cast<uint8_t *>(is_v ? a.V : a.K) + row_off)[v] = x;
+        }
+    }
     const int c0 = int(pc.seg_start / plan.chunk);
     const int c1 = int((pc.seg_start + pc.len - 1) / plan.chunk);
     const bool whole = (c0 == c1);

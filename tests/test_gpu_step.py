@@ -2,10 +2,9 @@
 
 "10.3 -- KV cache implementation details", section 5 (the decode loop): the
 step appends k_t, v_t to the layer's cache, then the single query row attends
-over the entire cache.  kvc_decode_step does both; for 16-bit caches with
-head groups of 2 to 8 and d_h of 64 or 128 it is one launch that takes the
-new rows from k_new / v_new directly, otherwise the append and the attention
-run back to back.  Checked here: the cache bytes after the step equal those of
+over the entire cache.  kvc_decode_step does both in one launch that takes
+the new rows from k_new / v_new directly (on the tensor-core kernels and on
+the CUDA-core kernel alike).  Checked here: the cache bytes after the step equal those of
 a list-append cache (bit-exact, padded rows still poisoned), the output
 matches the fp64 oracle within the decode tolerances, and the fused launch
 agrees with append + decode_attn wherever the new row falls in a tile or a
@@ -62,7 +61,7 @@ def _check_cache(hn, lc, layer, lengths, dtype):
             assert (kh[b, :, n] == poison).all() and (vh[b, :, n] == poison).all()
 
 
-# Sequences of steps: fused one-launch shapes and the two-launch fallback.
+# Sequences of steps on every kernel (all of them fuse the step's append).
 SEQ = [
     # name, dtype, d_h, H, H_kv, B, max_ctx, prefilled rows per sequence
     ("bf16_g4_d128", "bf16", 128, 16, 4, 5, 700, [0, 31, 32, 250, 690]),
@@ -71,8 +70,9 @@ SEQ = [
     ("bf16_g32_d128_mqa", "bf16", 128, 32, 1, 3, 600, [0, 33, 590]),
     ("fp16_g16_d64", "fp16", 64, 32, 2, 2, 400, [64, 391]),
     ("fp16_g16_d128_tc", "fp16", 128, 32, 2, 3, 400, [0, 127, 383]),
-    ("fp32_g6_d128_two_launches", "fp32", 128, 12, 2, 3, 300, [0, 40, 290]),
-    ("bf16_g1_d128_two_launches", "bf16", 128, 4, 4, 2, 300, [5, 100]),
+    ("fp32_g6_d128_cuda_core", "fp32", 128, 12, 2, 3, 300, [0, 40, 290]),
+    ("bf16_g1_d128_cuda_core", "bf16", 128, 4, 4, 2, 300, [5, 100]),
+    ("bf16_g4_d32_cuda_core", "bf16", 32, 16, 4, 3, 200, [0, 63, 190]),
 ]
 
 
@@ -114,7 +114,10 @@ EDGE_LENGTHS = [1, 2, 8, 9, 31, 32, 33, 40, 64, 65, 511, 700]
 
 @pytest.mark.parametrize("splits", [0, 1, 3, 13, 152])
 @pytest.mark.parametrize("dtype,D,H,H_kv", [("bf16", 128, 16, 4), ("fp16", 64, 6, 2), ("bf16", 128, 32, 1),
-                                           ("fp16", 128, 32, 2)])
+                                           ("fp16", 128, 32, 2),
+                                           # the CUDA-core kernel: fp32, one head per KV head, d_h 32 / 256
+                                           ("fp32", 128, 8, 2), ("bf16", 128, 8, 8), ("fp16", 32, 4, 4),
+                                           ("bf16", 256, 4, 2)])
 def test_fused_step_equals_append_then_decode(splits, dtype, D, H, H_kv):
     B, T = len(EDGE_LENGTHS), 700
     w = synth.Workload(f"edge_{dtype}", 1, B, H, H_kv, D, T, dtype, steps=1, seed=931)
