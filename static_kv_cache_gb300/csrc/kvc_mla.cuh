@@ -263,11 +263,14 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
         dev::prefetch_tensormap(&a.tm64);
         dev::prefetch_tensormap(&a.tm16);
     }
-    // the set-up above overlaps the previous kernel on the stream (the absorb);
-    // nothing below runs before it has completed
-    dev::grid_dependency_wait();
-    dev::allow_dependents();
-    __syncthreads();
+    __syncthreads();  // the barriers are initialised for every role
+    // The set-up above overlaps the previous kernel on the stream: the absorb
+    // launch of the same call.  The consumers touch nothing before it has
+    // completed; the producer starts earlier (below).
+    if (warp != 0) {
+        dev::grid_dependency_wait();
+        dev::allow_dependents();
+    }
 
     const int split = int(blockIdx.x) / a.groups, head0 = (int(blockIdx.x) % a.groups) * H;
     const Plan plan = make_plan(a, a.valid_len, lane, split, int(gridDim.x) / a.groups);
@@ -277,6 +280,16 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
 
     // ---------------------------------------------------------------- producer
     if (warp == 0) {
+        // The producer plans and copies before its dependency wait.  This
+        // launch can only start once every CTA of the absorb launch has passed
+        // its own wait for the kernel before it (the absorb signals its
+        // dependents right after that wait), so the valid lengths and every
+        // latent row but each sequence's last live one (the new row, which
+        // the absorb itself writes) are in place.  Tiles that do not hold a
+        // sequence's last live row go ahead; the wait comes before the first
+        // tile that does, or before the ring's first reuse, whichever is
+        // first.
+        bool waited = false;
         uint32_t t = 0;
         bool ok = true;
         // one head group: the latent rows are read once per launch; several:
@@ -289,6 +302,11 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
                 const int nr = min(TILE, pc.hi - row0);
                 const int s = int(t % uint32_t(ns));
                 const uint32_t r = t / uint32_t(ns);
+                if (!waited && (r > 0 || row0 + nr == pc.n)) {
+                    dev::grid_dependency_wait();
+                    dev::allow_dependents();
+                    waited = true;
+                }
                 if (r > 0) {
                     const bool w = dev::mbar_wait_bounded(bar0 + 8 * (ns + s), (r - 1) & 1, flags, a.timeout_ns);
                     if (!__all_sync(FULL, w)) {
@@ -318,6 +336,10 @@ __global__ void __launch_bounds__(MlaCfg<T, DC, H>::THREADS, 1) mla_decode_kerne
                 }
                 __syncwarp();
             }
+        }
+        if (!waited) {
+            dev::grid_dependency_wait();
+            dev::allow_dependents();
         }
         __syncwarp();
         dev::named_barrier_sync(2, C::THREADS);  // every warp is done
@@ -609,9 +631,11 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr unsigned FULL = 0xffffffffu;
     const int rows = min(64, a.d_h - i0);
-    dev::grid_dependency_wait();   // the previous kernel on the stream (the attention) has completed
-    dev::allow_dependents();
     {
+        // W_UV rows start towards shared memory before the dependency wait:
+        // this launch follows the attention launch of the same call, which
+        // signals its dependents only after its own wait for the absorb,
+        // which had waited for everything before the call; W_UV is in place.
         const T *w = static_cast<const T *>(a.w_uv) + (int64_t(h) * a.d_h + i0) * DC;
         for (int v = threadIdx.x; v < rows * (DC / 8); v += 512) {
             const int r = v / (DC / 8), c = (v - r * (DC / 8)) * 8;
@@ -619,6 +643,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(const MlaCombineArgs a
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    dev::grid_dependency_wait();   // the attention launch has completed: its partials are in place
+    dev::allow_dependents();
     if (warp == 0) {
         // the decode launch's plan: flattened offsets of the sequences and the split length
         int64_t base = 0, mine = 0;
