@@ -187,6 +187,48 @@ def test_mla_step_sequence_and_cache_bytes(dtype, H, d_h, d_c):
     assert hn.canaries_intact()
 
 
+@pytest.mark.parametrize("splits", [1, 3, 152])
+@pytest.mark.parametrize("H", [16, 32])
+def test_mla_steps_with_forced_splits(splits, H):
+    """Fused steps whose new rows fall at every position of a 64-row tile
+    (the first, the last, across a tile edge), under forced splits: the
+    attention launch copies the tiles without a new row before its
+    dependency wait and the new-row tiles after it; outputs against the
+    oracle, the cache bytes against a list-append cache."""
+    B, T, L, steps = 7, 300, 1, 3
+    hn = MlaHarness(L, B, H, 128, 512, T, "bf16", seed=4700 + splits + H)
+    assert hn.kvc.kvc_mla_set_num_splits(hn.h, splits) == 0
+    lc = ListAppendCache(L, B, 1, 512 * 2)
+    pre = [0, 1, 62, 63, 64, 127, 200]
+    c = hn.fill(0, pre, "pre")
+    cb = _gpu.bits(c)
+    for b, n in enumerate(pre):
+        for t in range(n):
+            lc.k[0][b][0].append(cb[b, t].view(np.uint8).tobytes())
+    lengths = np.array(pre)
+    for step in range(steps):
+        ci = lengths.copy()
+        lengths = lengths + 1
+        vl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+        c_new = hn.latents(1, "fstep", step)
+        q = hn.query("fstep", step)
+        out = torch.empty((B, H, 128), dtype=hn.tdt, device="cuda")
+        assert hn.kvc.kvc_mla_decode_step(hn.h, 0, q, c_new, hn.wk, hn.wv, vl, int(lengths.max()), out) == 0
+        cnb = _gpu.bits(c_new)[:, None]
+        lc.append(0, cnb, cnb, ci, 1)
+        ctx = int(lengths.max())
+        ref = oracle.mla_decode_attn(_gpu.bits(q), lc.dense(0, "k", ctx).view(np.uint16)[:, 0],
+                                     _gpu.bits(hn.wk), _gpu.bits(hn.wv), lengths, "bf16")
+        mla_compare(out, ref, f"step {step} splits {splits} H {H}")
+    assert hn.kvc.kvc_mla_get_error(hn.h) == 0
+    got = _gpu.bits(hn.C[0])
+    want = lc.dense(0, "k", int(lengths.max())).view(np.uint16)[:, 0]
+    for b in range(B):
+        n = int(lengths[b])
+        assert np.array_equal(got[b, :n], want[b, :n]), f"latent rows of sequence {b}"
+    assert hn.canaries_intact()
+
+
 def test_mla_multi_row_append_is_bit_exact():
     hn = MlaHarness(2, 3, 8, 64, 256, 200, "bf16", seed=4300)
     c = hn.latents(50, "multi")
